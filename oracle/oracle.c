@@ -1,0 +1,639 @@
+/*
+ * oracle.c -- plain, slow CPU reference for the exact ternary weight apply.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the smoke check and the bench's CPU
+ * baseline leg are the only callers. The CUDA path never includes, links or
+ * loads this file, and this file shares no code, header, table or constant
+ * with it. Inputs come from the seeded generators; nothing here is computed
+ * from a GPU result.
+ *
+ * Every function is the plain definition, written as naive loops in int64 (and
+ * fp64 / long double where a real number is materialised). Sources, by page:
+ *
+ *   [BitState]  "BitState / HSDR PoC Technical Brief v0.5"
+ *               (huggingface.co/datasets/mktnhr/BitState)
+ *   [SKaiNET]   SKaiNET-transformers issue #337, "[bitnet] T2: lm_head via
+ *               BITNET_PLANES weight format (WeightForm) + two-stage top-k decode"
+ *   [IntEngine] integer_engine.md, "A standalone deterministic integer inference
+ *               engine for BitNet-style LLMs, with Ollama interop"
+ *
+ * Readings taken where the pages leave a step open (each is listed with its
+ * reason in the design notes):
+ *   - per-group arshift(., frac) of [IntEngine] §4.1/§4.2 is taken with frac = 0;
+ *   - K must be a multiple of 128 (the group size); other K is rejected;
+ *   - LNS8 product code k = a + d - 74: k <= 0 is exact zero, k > 127 saturates
+ *     to 127; an activation with code 0 is zero whatever its sign bit;
+ *   - lm_head plane p carries the integer weight 3^(7-p) (the pages' 3^-p
+ *     scaled by 3^7), so the planes 4..7 truncation bound is 40 = 27+9+3+1;
+ *   - top-k order is (score descending, row index ascending), which makes the
+ *     argmax the lowest index among equal maxima.
+ *
+ * All functions return 0 on success and -1 on an invalid argument.
+ */
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_GROUP 128
+
+/* Population count of a 64-bit word by clearing the lowest set bit. */
+static int oracle_popcount64(uint64_t v)
+{
+    int n = 0;
+    while (v) {
+        v &= v - 1;
+        n++;
+    }
+    return n;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 1. Ternary GEMV with int8 activations and per-group integer scales.       */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * y[m][r] = sum_g d[r][g] * ( sum_{i in group g} t[r][i] * x[m][i] )
+ *
+ * [IntEngine] §4.2 (BitNet b1.58 ternary): the per-group signed sum is the sum
+ * of x over the +1 weights minus the sum over the -1 weights (zeros drop out);
+ * it is multiplied by the per-group integer scale and summed over groups
+ * (§4.1/§4.2 "out_o", frac = 0). §4.4 fixes int8 activations with integer
+ * accumulation. Layouts: t [N][K] int8 in {-1,0,1}; d [N][K/128] int32;
+ * x [M][K] int8; y [M][N] int64.
+ */
+int oracle_gemv_i8(int64_t M, int64_t N, int64_t K, const int8_t *t,
+                   const int32_t *d, const int8_t *x, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            int64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                int64_t signed_sum = 0;
+                for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++)
+                    signed_sum += (int64_t)t[r * K + i] * (int64_t)x[m * K + i];
+                out += (int64_t)d[r * G + g] * signed_sum;
+            }
+            y[m * N + r] = out;
+        }
+    }
+    return 0;
+}
+
+/* Build the W_nonzero / W_negative bitmask pair of one 128-weight group. */
+static void oracle_group_masks(const int8_t *trow, int64_t g, uint64_t nz[2], uint64_t neg[2])
+{
+    nz[0] = nz[1] = neg[0] = neg[1] = 0;
+    for (int j = 0; j < ORACLE_GROUP; j++) {
+        int8_t v = trow[g * ORACLE_GROUP + j];
+        if (v != 0)
+            nz[j >> 6] |= (uint64_t)1 << (j & 63);
+        if (v < 0)
+            neg[j >> 6] |= (uint64_t)1 << (j & 63);
+    }
+}
+
+/*
+ * The same GEMV through the two-bitmask masked sum: per group the row is held
+ * as W_nonzero / W_negative ([BitState] §4), and the signed sum is
+ * sum_{nz & !neg} x - sum_{nz & neg} x ([IntEngine] §4.2).
+ */
+int oracle_gemv_i8_masked(int64_t M, int64_t N, int64_t K, const int8_t *t,
+                          const int32_t *d, const int8_t *x, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            int64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                uint64_t nz[2], neg[2];
+                oracle_group_masks(t + r * K, g, nz, neg);
+                int64_t pos_sum = 0, neg_sum = 0;
+                for (int j = 0; j < ORACLE_GROUP; j++) {
+                    uint64_t bit = (uint64_t)1 << (j & 63);
+                    int64_t xv = x[m * K + g * ORACLE_GROUP + j];
+                    if ((nz[j >> 6] & bit) && !(neg[j >> 6] & bit))
+                        pos_sum += xv;
+                    if ((nz[j >> 6] & bit) && (neg[j >> 6] & bit))
+                        neg_sum += xv;
+                }
+                out += (int64_t)d[r * G + g] * (pos_sum - neg_sum);
+            }
+            y[m * N + r] = out;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The same GEMV through signed state populations ([BitState] §4). The
+ * activation state is the magnitude s = |x_i| (0..128). For each state:
+ *   A_s  = lanes whose activation magnitude is s
+ *   M    = A_s & W_nonzero
+ *   PNEG = activation_sign XOR W_negative
+ *   C_s  = popcount(M) - 2 * popcount(M & PNEG)
+ * and the group's signed sum is sum_s s * C_s.
+ */
+int oracle_gemv_i8_stateset(int64_t M, int64_t N, int64_t K, const int8_t *t,
+                            const int32_t *d, const int8_t *x, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            int64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                uint64_t nz[2], neg[2], asign[2] = {0, 0};
+                oracle_group_masks(t + r * K, g, nz, neg);
+                for (int j = 0; j < ORACLE_GROUP; j++)
+                    if (x[m * K + g * ORACLE_GROUP + j] < 0)
+                        asign[j >> 6] |= (uint64_t)1 << (j & 63);
+                int64_t signed_sum = 0;
+                for (int s = 1; s <= 128; s++) {
+                    uint64_t As[2] = {0, 0};
+                    for (int j = 0; j < ORACLE_GROUP; j++) {
+                        int xv = x[m * K + g * ORACLE_GROUP + j];
+                        if ((xv < 0 ? -xv : xv) == s)
+                            As[j >> 6] |= (uint64_t)1 << (j & 63);
+                    }
+                    int64_t C = 0;
+                    for (int h = 0; h < 2; h++) {
+                        uint64_t Mh = As[h] & nz[h];
+                        uint64_t pneg = asign[h] ^ neg[h];
+                        C += oracle_popcount64(Mh) - 2 * oracle_popcount64(Mh & pneg);
+                    }
+                    signed_sum += (int64_t)s * C;
+                }
+                out += (int64_t)d[r * G + g] * signed_sum;
+            }
+            y[m * N + r] = out;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 2. LNS8 S1|E4|L3 product states, eight phase accumulators.                */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Product state of one lane ([BitState] §3, §3.1, §4 generic variant).
+ * Activation byte xa = sign<<7 | code; code 0 is exact zero. Weight t in
+ * {-1,0,1} with the group's scale code dcode. The scale is applied before the
+ * L3/E4 split (the generic variant of §4): k = a + dcode - 74, which is the
+ * product of the magnitudes 2^((a-74)/8) * 2^((dcode-74)/8) written as a code.
+ * k <= 0 -> exact zero; k > 127 -> 127. Sign S1 = activation sign XOR [t < 0].
+ * Returns 0 for an exact-zero product, else 1 with *k_out in 1..127 and
+ * *neg_out the sign.
+ */
+static int oracle_lns8_product(uint8_t xa, int8_t t, uint8_t dcode, int *k_out, int *neg_out)
+{
+    int a = xa & 0x7f;
+    int s_a = xa >> 7;
+    if (t == 0 || a == 0)
+        return 0;
+    int k = a + (int)dcode - 74;
+    if (k <= 0)
+        return 0;
+    if (k > 127)
+        k = 127;
+    *k_out = k;
+    *neg_out = s_a ^ (t < 0 ? 1 : 0);
+    return 1;
+}
+
+/*
+ * Direct eight-phase accumulation ([BitState] §3.1): for every nonzero product
+ * state k, phase = k & 7 (L3), payload = sign * (1 << (k >> 3)) (E4), and
+ * A[phase] += payload. Layouts: t [N][K]; dcode [N][K/128] uint8;
+ * xa [K] uint8; A [N][8] int64.
+ */
+int oracle_lns8_direct(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode,
+                       const uint8_t *xa, int64_t *A)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < N; r++) {
+        int64_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int64_t i = 0; i < K; i++) {
+            int k, neg;
+            if (!oracle_lns8_product(xa[i], t[r * K + i], dcode[r * G + i / ORACLE_GROUP], &k, &neg))
+                continue;
+            int64_t payload = (int64_t)1 << (k >> 3);
+            acc[k & 7] += neg ? -payload : payload;
+        }
+        for (int p = 0; p < 8; p++)
+            A[r * 8 + p] = acc[p];
+    }
+    return 0;
+}
+
+/*
+ * Histogram path ([BitState] §3.1, last formula; §7 Phase A "signed POPCOUNT
+ * histogram" and "histogram-to-A[0..7] equivalence"): build the signed count
+ * H[phase][band] first, then A[p] = sum_b H[p][b] << b.
+ */
+int oracle_lns8_histogram(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode,
+                          const uint8_t *xa, int64_t *A)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < N; r++) {
+        int64_t H[8][16];
+        memset(H, 0, sizeof(H));
+        for (int64_t i = 0; i < K; i++) {
+            int k, neg;
+            if (!oracle_lns8_product(xa[i], t[r * K + i], dcode[r * G + i / ORACLE_GROUP], &k, &neg))
+                continue;
+            H[k & 7][k >> 3] += neg ? -1 : 1;
+        }
+        for (int p = 0; p < 8; p++) {
+            int64_t a = 0;
+            for (int b = 0; b < 16; b++)
+                a += H[p][b] * ((int64_t)1 << b);
+            A[r * 8 + p] = a;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Tile64 x 2 phase-mask path ([BitState] §3.1, the spreadsheet procedure, read
+ * from its prose since the workbook is not available): the 128 inputs of a
+ * group are two 64-lane tiles; in each tile L3 builds eight phase selector
+ * masks (lanes whose product phase is p), E4 supplies the power-of-two payload
+ * and S1 the sign of each selected lane.
+ */
+int oracle_lns8_tile64(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode,
+                       const uint8_t *xa, int64_t *A)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < N; r++) {
+        int64_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int64_t g = 0; g < G; g++) {
+            for (int tile = 0; tile < 2; tile++) {
+                uint64_t sel[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                int e4[64], s1[64];
+                for (int j = 0; j < 64; j++) {
+                    int64_t i = g * ORACLE_GROUP + tile * 64 + j;
+                    int k, neg;
+                    e4[j] = 0;
+                    s1[j] = 0;
+                    if (!oracle_lns8_product(xa[i], t[r * K + i], dcode[r * G + g], &k, &neg))
+                        continue;
+                    sel[k & 7] |= (uint64_t)1 << j;
+                    e4[j] = k >> 3;
+                    s1[j] = neg;
+                }
+                for (int p = 0; p < 8; p++) {
+                    for (int j = 0; j < 64; j++) {
+                        if (!(sel[p] >> j & 1))
+                            continue;
+                        int64_t payload = (int64_t)1 << e4[j];
+                        acc[p] += s1[j] ? -payload : payload;
+                    }
+                }
+            }
+        }
+        for (int p = 0; p < 8; p++)
+            A[r * 8 + p] = acc[p];
+    }
+    return 0;
+}
+
+/*
+ * State-set population path ([BitState] §4 with §6): the activation state is
+ * its code a (1..127; code 0 is excluded as exact zero). Per group and state,
+ *   C_a = popcount(A_a & W_nonzero) - 2 * popcount(A_a & W_nonzero & PNEG),
+ *   PNEG = activation_sign XOR W_negative,
+ * is the signed population of state a, and all lanes of that state share one
+ * product code k = a + dcode - 74 (the group shares dcode), so
+ * A[k & 7] += C_a * 2^(k >> 3) after the same zero / saturation rule.
+ */
+int oracle_lns8_stateset(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode,
+                         const uint8_t *xa, int64_t *A)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < N; r++) {
+        int64_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int64_t g = 0; g < G; g++) {
+            uint64_t nz[2], neg[2], asign[2] = {0, 0};
+            oracle_group_masks(t + r * K, g, nz, neg);
+            for (int j = 0; j < ORACLE_GROUP; j++)
+                if (xa[g * ORACLE_GROUP + j] >> 7)
+                    asign[j >> 6] |= (uint64_t)1 << (j & 63);
+            for (int a = 1; a <= 127; a++) {
+                uint64_t As[2] = {0, 0};
+                for (int j = 0; j < ORACLE_GROUP; j++)
+                    if ((xa[g * ORACLE_GROUP + j] & 0x7f) == a)
+                        As[j >> 6] |= (uint64_t)1 << (j & 63);
+                int64_t C = 0;
+                for (int h = 0; h < 2; h++) {
+                    uint64_t Mh = As[h] & nz[h];
+                    uint64_t pneg = asign[h] ^ neg[h];
+                    C += oracle_popcount64(Mh) - 2 * oracle_popcount64(Mh & pneg);
+                }
+                if (C == 0)
+                    continue;
+                int k = a + (int)dcode[r * G + g] - 74;
+                if (k <= 0)
+                    continue;
+                if (k > 127)
+                    k = 127;
+                acc[k & 7] += C * ((int64_t)1 << (k >> 3));
+            }
+        }
+        for (int p = 0; p < 8; p++)
+            A[r * 8 + p] = acc[p];
+    }
+    return 0;
+}
+
+/* F[p] = 2^((p - 2) / 8) ([BitState] §3), as fp64 from libm's exp2. */
+void oracle_lns8_F(double F[8])
+{
+    for (int p = 0; p < 8; p++)
+        F[p] = exp2((double)(p - 2) / 8.0);
+}
+
+/*
+ * Dyadic materialisation ([BitState] §3.1): S = 2^-9 * sum_p A[p] * F[p],
+ * summed in the fixed order p = 0..7 in fp64, each product and sum rounded
+ * once (this file is built without FP contraction), then scaled by 2^-9.
+ * F is the caller's table of 8 doubles.
+ */
+int oracle_lns8_materialise(int64_t N, const int64_t *A, const double *F, double *S)
+{
+    if (N < 0)
+        return -1;
+    for (int64_t r = 0; r < N; r++) {
+        double acc = 0.0;
+        for (int p = 0; p < 8; p++) {
+            double term = (double)A[r * 8 + p] * F[p];
+            acc = acc + term;
+        }
+        S[r] = acc * 0x1p-9;
+    }
+    return 0;
+}
+
+/*
+ * The same materialisation in long double with F from exp2l, rounded to double
+ * at the end: a higher-precision reference for S. S_abs receives
+ * 2^-9 * sum_p |A[p]| * F[p], the scale against which rounding error is judged.
+ */
+int oracle_lns8_materialise_hi(int64_t N, const int64_t *A, double *S_hi, double *S_abs)
+{
+    if (N < 0)
+        return -1;
+    long double F[8];
+    for (int p = 0; p < 8; p++)
+        F[p] = exp2l((long double)(p - 2) / 8.0L);
+    for (int64_t r = 0; r < N; r++) {
+        long double acc = 0.0L, mag = 0.0L;
+        for (int p = 0; p < 8; p++) {
+            long double v = (long double)A[r * 8 + p] * F[p];
+            acc += v;
+            mag += v < 0 ? -v : v;
+        }
+        S_hi[r] = (double)(acc / 512.0L);
+        S_abs[r] = (double)(mag / 512.0L);
+    }
+    return 0;
+}
+
+/*
+ * Direct FP64 decode ([BitState] §7 Phase A "exact LNS8 decode reference"):
+ * every nonzero product state contributes sign * 2^((k - 74) / 8), summed in
+ * lane order. Also returns the sum of magnitudes for an error bound.
+ */
+int oracle_lns8_decode_fp64(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode,
+                            const uint8_t *xa, double *S, double *S_abs)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t r = 0; r < N; r++) {
+        double acc = 0.0, mag = 0.0;
+        for (int64_t i = 0; i < K; i++) {
+            int k, neg;
+            if (!oracle_lns8_product(xa[i], t[r * K + i], dcode[r * G + i / ORACLE_GROUP], &k, &neg))
+                continue;
+            double v = exp2((double)(k - 74) / 8.0);
+            acc += neg ? -v : v;
+            mag += v;
+        }
+        S[r] = acc;
+        S_abs[r] = mag;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* 3. Vocab-scale lm_head over 8 base-3 planes.                              */
+/* ------------------------------------------------------------------------- */
+
+static const int64_t oracle_pow3[8] = {2187, 729, 243, 81, 27, 9, 3, 1}; /* 3^(7-p) */
+
+/*
+ * Exact logits ([SKaiNET] BITNET_PLANES: 8 ternary planes, plane p weighted
+ * 3^-p; here scaled by 3^7 so every weight is an integer):
+ *   W[r][i] = sum_p planes[p][r][i] * 3^(7-p),   logit[r] = s[r] * sum_i W[r][i] * x[i].
+ * Layouts: planes [8][N][K] int8; s [N] int32; x [K] int8; logits [N] int64.
+ */
+int oracle_lmhead_logits(int64_t N, int64_t K, const int8_t *planes, const int32_t *s,
+                         const int8_t *x, int64_t *logits)
+{
+    if (N < 1 || K < 1)
+        return -1;
+    for (int64_t r = 0; r < N; r++) {
+        int64_t dot = 0;
+        for (int64_t i = 0; i < K; i++) {
+            int64_t w = 0;
+            for (int p = 0; p < 8; p++)
+                w += (int64_t)planes[(int64_t)p * N * K + r * K + i] * oracle_pow3[p];
+            dot += w * (int64_t)x[i];
+        }
+        logits[r] = (int64_t)s[r] * dot;
+    }
+    return 0;
+}
+
+/* Ordering for the top-k: score descending, then row index ascending. */
+static const int64_t *oracle_sort_scores;
+
+static int oracle_cmp_desc(const void *pa, const void *pb)
+{
+    int64_t a = *(const int64_t *)pa, b = *(const int64_t *)pb;
+    int64_t sa = oracle_sort_scores[a], sb = oracle_sort_scores[b];
+    if (sa != sb)
+        return sa > sb ? -1 : 1;
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+/* Rows sorted by (score desc, index asc); the first k are the top-k. */
+static int64_t *oracle_sorted_rows(int64_t n, const int64_t *scores)
+{
+    int64_t *idx = (int64_t *)malloc((size_t)n * sizeof(int64_t));
+    if (!idx)
+        return NULL;
+    for (int64_t r = 0; r < n; r++)
+        idx[r] = r;
+    oracle_sort_scores = scores;
+    qsort(idx, (size_t)n, sizeof(int64_t), oracle_cmp_desc);
+    return idx;
+}
+
+/*
+ * Argmax with the lowest-index tie-break ([IntEngine] §3.3 "Argmax / sampling:
+ * lowest-index tie-break", §3.2).
+ */
+int64_t oracle_argmax(int64_t N, const int64_t *scores)
+{
+    if (N < 1)
+        return -1;
+    int64_t best = 0;
+    for (int64_t r = 1; r < N; r++)
+        if (scores[r] > scores[best])
+            best = r;
+    return best;
+}
+
+/* Top-k of a score vector under (score desc, index asc): the full sort, first k. */
+int oracle_topk(int64_t N, const int64_t *scores, int64_t k, int32_t *ids, int64_t *top)
+{
+    if (N < 1 || k < 1 || k > N)
+        return -1;
+    int64_t *idx = oracle_sorted_rows(N, scores);
+    if (!idx)
+        return -1;
+    for (int64_t j = 0; j < k; j++) {
+        ids[j] = (int32_t)idx[j];
+        top[j] = scores[idx[j]];
+    }
+    free(idx);
+    return 0;
+}
+
+/*
+ * Two-stage top-k ([SKaiNET] closing comments, BitNetTwoStageDecode):
+ *   stage 1: a scan of planes 0..3 over the whole vocabulary,
+ *            stage1[r] = sum_i (sum_{p<4} planes[p][r][i] * 3^(7-p)) * x[i];
+ *   bound:   the truncation of row r is at most rowScale(r) * (sum_{p=4..7} 3^-p)
+ *            * sum|x|, i.e. B[r] = s[r] * 40 * sum_i |x_i| in integer units;
+ *            lo[r] = s[r]*stage1[r] - B[r], hi[r] = s[r]*stage1[r] + B[r];
+ *   select:  tau = the k-th best lower bound; every row whose upper bound
+ *            reaches it (hi[r] >= tau) is rescored exactly with planes 4..7;
+ *   result:  the top-k of the rescored rows, equal to the full-matmul top-k.
+ * The candidate cap of the page (maxCandidates) is not applied: this is the
+ * exact procedure. lo, hi may be NULL; n_cand receives the candidate count.
+ */
+int oracle_lmhead_two_stage(int64_t N, int64_t K, const int8_t *planes, const int32_t *s,
+                            const int8_t *x, int64_t k, int32_t *ids, int64_t *top,
+                            int64_t *lo_out, int64_t *hi_out, int64_t *n_cand)
+{
+    if (N < 1 || K < 1 || k < 1 || k > N)
+        return -1;
+    int64_t sum_abs_x = 0;
+    for (int64_t i = 0; i < K; i++)
+        sum_abs_x += x[i] < 0 ? -(int64_t)x[i] : (int64_t)x[i];
+
+    int64_t *stage1 = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    int64_t *lo = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    int64_t *hi = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    int64_t *exact = (int64_t *)malloc((size_t)N * sizeof(int64_t));
+    if (!stage1 || !lo || !hi || !exact) {
+        free(stage1); free(lo); free(hi); free(exact);
+        return -1;
+    }
+    for (int64_t r = 0; r < N; r++) {
+        int64_t dot = 0;
+        for (int64_t i = 0; i < K; i++) {
+            int64_t w = 0;
+            for (int p = 0; p < 4; p++)
+                w += (int64_t)planes[(int64_t)p * N * K + r * K + i] * oracle_pow3[p];
+            dot += w * (int64_t)x[i];
+        }
+        stage1[r] = dot;
+        int64_t B = (int64_t)s[r] * 40 * sum_abs_x;
+        lo[r] = (int64_t)s[r] * dot - B;
+        hi[r] = (int64_t)s[r] * dot + B;
+    }
+    /* tau = k-th largest lower bound. */
+    int64_t *order = oracle_sorted_rows(N, lo);
+    if (!order) {
+        free(stage1); free(lo); free(hi); free(exact);
+        return -1;
+    }
+    int64_t tau = lo[order[k - 1]];
+    free(order);
+
+    /* Rescore every candidate exactly; non-candidates get the lowest score. */
+    int64_t C = 0;
+    for (int64_t r = 0; r < N; r++) {
+        if (hi[r] < tau) {
+            exact[r] = INT64_MIN;
+            continue;
+        }
+        C++;
+        int64_t rest = 0;
+        for (int64_t i = 0; i < K; i++) {
+            int64_t w = 0;
+            for (int p = 4; p < 8; p++)
+                w += (int64_t)planes[(int64_t)p * N * K + r * K + i] * oracle_pow3[p];
+            rest += w * (int64_t)x[i];
+        }
+        exact[r] = (int64_t)s[r] * (stage1[r] + rest);
+    }
+    int64_t *idx = oracle_sorted_rows(N, exact);
+    if (!idx) {
+        free(stage1); free(lo); free(hi); free(exact);
+        return -1;
+    }
+    for (int64_t j = 0; j < k; j++) {
+        ids[j] = (int32_t)idx[j];
+        top[j] = exact[idx[j]];
+    }
+    if (lo_out)
+        memcpy(lo_out, lo, (size_t)N * sizeof(int64_t));
+    if (hi_out)
+        memcpy(hi_out, hi, (size_t)N * sizeof(int64_t));
+    if (n_cand)
+        *n_cand = C;
+    free(idx);
+    free(stage1); free(lo); free(hi); free(exact);
+    return 0;
+}
+
+/*
+ * Balanced-ternary digits of an integer weight ([SKaiNET] BITNET_PLANES: plane
+ * p is the base-3 digit of weight 3^(7-p) in {-1,0,1}). w must lie in
+ * [-3280, 3280] = +-(3^8 - 1)/2. Digits are produced least significant first
+ * by taking the remainder in {-1,0,1}.
+ */
+int oracle_planes_of_weight(int32_t w, int8_t digits[8])
+{
+    if (w < -3280 || w > 3280)
+        return -1;
+    int32_t v = w;
+    for (int p = 7; p >= 0; p--) {
+        int32_t rem = ((v % 3) + 3) % 3; /* 0, 1, 2 */
+        int32_t digit = rem == 2 ? -1 : rem;
+        digits[p] = (int8_t)digit;
+        v = (v - digit) / 3;
+    }
+    return v == 0 ? 0 : -1;
+}
