@@ -1,0 +1,286 @@
+// gemv_i8.cu -- exact ternary GEMV with int8 activations and per-group integer
+// scales (integer_engine.md §4.2 "BitNet b1.58 ternary" with §4.4 int8
+// activations; the row is held as the W_nonzero / W_negative mask pair of the
+// BitState brief §4):
+//
+//     y[m][r] = sum_g d[r][g] * P[m][r][g],   P = sum_{i in g} t[r][i] * x[m][i]
+//
+// P is an int32 (|P| <= 128 * 128), the sum over groups an int64; every sum is
+// an integer sum, so the result does not depend on the launch geometry.
+//
+// Lane arithmetic. One 32-bit mask word holds 16 lanes: lane 4j + b of the word
+// sits at bits 8b + 2j (nonzero) and 8b + 2j + 1 (negative). For a canonical
+// pair the 2-bit field f is 0 (t = 0), 1 (t = +1) or 3 (t = -1), so f ^ 2 =
+// t + 2. Masking column j of the word in place and flipping its high bit,
+// (w & (0x03030303 << 2j)) ^ (0x02020202 << 2j), gives four unsigned bytes
+// (t + 2) * 4^j, and one dp4a against the four activations of that column
+// accumulates 4^j * sum (t + 2) x. Per group the four column sums are shifted
+// back (exactly: each is a multiple of 4^j) and 2 * sum_{i in g} x is
+// subtracted (the block-total reuse of integer_engine.md §4.1, computed once
+// per group and shared by every row). Cost: one LOP3 and one dp4a per four
+// weights, plus one broadcast 16-byte shared-memory load per sixteen.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "tg.h"
+#include "tg_internal.h"
+
+TGI_DEFINE_DEVICE_ERROR(gemv_take_device_error)
+
+namespace {
+
+using tgi::dp4a_us;
+using tgi::kTileRows;
+
+// Column sums of one 128-lane group for one row: w[0..7] are the row's eight
+// mask words (half 0 then half 1), xg the group's 128 activations in shared
+// memory. Returns sum_i (t_i + 2) x_i.
+__device__ __forceinline__ int group_dot_t2(const uint32_t w[8], const int8_t *xg)
+{
+    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const uint4 xv = *reinterpret_cast<const uint4 *>(xg + 16 * u);
+        a0 = dp4a_us((w[u] & 0x03030303u) ^ 0x02020202u, xv.x, a0);
+        a1 = dp4a_us((w[u] & 0x0C0C0C0Cu) ^ 0x08080808u, xv.y, a1);
+        a2 = dp4a_us((w[u] & 0x30303030u) ^ 0x20202020u, xv.z, a2);
+        a3 = dp4a_us((w[u] & 0xC0C0C0C0u) ^ 0x80808080u, xv.w, a3);
+    }
+    return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
+}
+
+// ---------------------------------------------------------------------------
+// Batch 1. One CTA per tile of 32 rows; lane l of every warp owns row 32T + l;
+// the CTA's warps split the row's groups (warp w takes g = w, w + W, ...), and
+// the per-warp int64 partials are summed through shared memory at the end.
+// All mask loads of a warp's batch are issued before the activation tile is
+// staged, so the whole tile is in flight while x lands in shared memory.
+// ---------------------------------------------------------------------------
+template <int WARPS, int GPW>
+__global__ void __launch_bounds__(WARPS * 32)
+gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    int8_t *xs = reinterpret_cast<int8_t *>(smem);                   // [G*128]
+    int *tsum = reinterpret_cast<int *>(smem + G * 128);             // [G]
+    int64_t *red = reinterpret_cast<int64_t *>(smem + G * 128 + ((G * 4 + 15) & ~15));  // [WARPS][32]
+
+    const int tile = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint4 *tmask = masks + (size_t)tile * G * 64;               // 64 uint4 per (tile, group)
+    const int32_t *tscale = scales + (size_t)tile * G * kTileRows;
+
+    uint4 m0[GPW], m1[GPW];
+    int32_t dg[GPW];
+    auto load_batch = [&](int g0) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = g0 + j * WARPS;
+            if (g < G) {
+                m0[j] = tgi::ldg_stream(tmask + g * 64 + lane);
+                m1[j] = tgi::ldg_stream(tmask + g * 64 + 32 + lane);
+                dg[j] = __ldg(tscale + g * kTileRows + lane);
+            } else {
+                m0[j] = m1[j] = make_uint4(0, 0, 0, 0);
+                dg[j] = 0;
+            }
+        }
+    };
+    load_batch(warp);
+
+    // Stage x and the per-group activation totals.
+    const int K = G * 128;
+    for (int i = threadIdx.x; i < K / 16; i += WARPS * 32)
+        reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
+    for (int g = warp; g < G; g += WARPS) {
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + g * 128) + lane);
+        const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
+        if (lane == 0)
+            tsum[g] = s;
+    }
+    __syncthreads();
+
+    int64_t acc = 0;
+    for (int g0 = warp;;) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = g0 + j * WARPS;
+            if (g < G) {
+                const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                       m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                const int P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
+                acc += (int64_t)dg[j] * (int64_t)P;
+            }
+        }
+        g0 += WARPS * GPW;
+        if (g0 >= G)
+            break;
+        load_batch(g0);
+    }
+
+    red[warp * 32 + lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t sum = 0;
+#pragma unroll
+        for (int w = 0; w < WARPS; w++)
+            sum += red[w * 32 + lane];
+        const int row = tile * kTileRows + lane;
+        if (row < N)
+            y[row] = sum;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Small batch (M tokens). One CTA per tile of 32 rows; warp w owns tokens
+// 16w .. 16w + 15 and lane l row 32T + l. K is walked in chunks of KC groups:
+// the chunk's activations for every token go to shared memory, then each
+// thread decodes its row's mask words once per group and reuses them for all
+// of its tokens.
+// ---------------------------------------------------------------------------
+constexpr int kMT = 16;   // tokens per warp
+constexpr int kKC = 4;    // groups per shared-memory chunk
+
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+gemv_i8_mb_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int M)
+{
+    __shared__ __align__(16) int8_t xs[WARPS * kMT][kKC * 128];
+    __shared__ int tsum[WARPS * kMT][kKC];
+
+    const int tile = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int K = G * 128;
+    const int mbase = warp * kMT;
+    const uint4 *tmask = masks + (size_t)tile * G * 64;
+    const int32_t *tscale = scales + (size_t)tile * G * kTileRows;
+
+    int64_t acc[kMT];
+#pragma unroll
+    for (int m = 0; m < kMT; m++)
+        acc[m] = 0;
+
+    for (int c0 = 0; c0 < G; c0 += kKC) {
+        const int cg = min(kKC, G - c0);
+        __syncthreads();
+        // stage x[m][c0*128 .. (c0+cg)*128) for every token
+        const int vec_per_tok = cg * 8;   // uint4 per token
+        for (int i = threadIdx.x; i < M * vec_per_tok; i += WARPS * 32) {
+            const int m = i / vec_per_tok, v = i % vec_per_tok;
+            reinterpret_cast<uint4 *>(xs[m])[v] =
+                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * K + c0 * 128) + v);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < M * cg; i += WARPS * 32) {
+            const int m = i / cg, g = i % cg;
+            int s = 0;
+            for (int b = 0; b < 32; b++)
+                s += tgi::byte_sum_s8(reinterpret_cast<const uint32_t *>(xs[m] + g * 128)[b]);
+            tsum[m][g] = s;
+        }
+        __syncthreads();
+
+        for (int gl = 0; gl < cg; gl++) {
+            const int g = c0 + gl;
+            const uint4 q0 = __ldg(tmask + g * 64 + lane);
+            const uint4 q1 = __ldg(tmask + g * 64 + 32 + lane);
+            const int64_t d = __ldg(tscale + g * kTileRows + lane);
+            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            uint32_t c[4][8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                c[0][u] = (w[u] & 0x03030303u) ^ 0x02020202u;
+                c[1][u] = (w[u] & 0x0C0C0C0Cu) ^ 0x08080808u;
+                c[2][u] = (w[u] & 0x30303030u) ^ 0x20202020u;
+                c[3][u] = (w[u] & 0xC0C0C0C0u) ^ 0x80808080u;
+            }
+#pragma unroll
+            for (int mm = 0; mm < kMT; mm++) {
+                const int m = mbase + mm;
+                if (m < M) {
+                    const int8_t *xg = xs[m] + gl * 128;
+                    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xg + 16 * u);
+                        a0 = dp4a_us(c[0][u], xv.x, a0);
+                        a1 = dp4a_us(c[1][u], xv.y, a1);
+                        a2 = dp4a_us(c[2][u], xv.z, a2);
+                        a3 = dp4a_us(c[3][u], xv.w, a3);
+                    }
+                    const int P = a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6) - 2 * tsum[m][gl];
+                    acc[mm] += d * (int64_t)P;
+                }
+            }
+        }
+    }
+
+    const int row = tile * kTileRows + lane;
+    if (row < N) {
+#pragma unroll
+        for (int mm = 0; mm < kMT; mm++) {
+            const int m = mbase + mm;
+            if (m < M)
+                y[(size_t)m * N + row] = acc[mm];
+        }
+    }
+}
+
+constexpr int kM1Warps = 4;
+constexpr int kM1Gpw = 6;
+
+size_t m1_smem_bytes(int G) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + kM1Warps * 32 * 8; }
+
+}  // namespace
+
+extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, int64_t M,
+                          int64_t *y, void *stream)
+{
+    if (!L || !w || !x || !y)
+        return TG_ERR_ARG;
+    if (L->kind != TG_TERNARY_I8 || L->version != 1)
+        return TG_ERR_ARG;
+    if (!tgi::aligned(w, 256) || !tgi::aligned(x, 16) || !tgi::aligned(y, 8))
+        return TG_ERR_ARG;
+    if (L->N < 1 || L->K < TG_GROUP || L->K % TG_GROUP || M < 1 || M > TG_MAX_M)
+        return TG_ERR_SHAPE;
+    // |y| <= G * 128 * 128 * max|d| must stay well inside int64.
+    if ((double)L->G * 16384.0 * (double)L->max_abs_scale >= 4.0e18)
+        return TG_ERR_BOUND;
+
+    const auto *base = static_cast<const unsigned char *>(w);
+    const uint4 *masks = reinterpret_cast<const uint4 *>(base + L->mask_off);
+    const int32_t *scales = reinterpret_cast<const int32_t *>(base + L->scale_off);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = (int)L->G, N = (int)L->N;
+    const int tiles = (int)L->tiles;
+
+    if (M == 1) {
+        const size_t smem = m1_smem_bytes(G);
+        auto kern = gemv_i8_m1_kernel<kM1Warps, kM1Gpw>;
+        if (smem > 48 * 1024) {
+            if (smem > 200 * 1024)
+                return TG_ERR_SHAPE;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+                return TG_ERR_CUDA;
+        }
+        kern<<<tiles, kM1Warps * 32, smem, s>>>(masks, scales, x, y, N, G);
+    } else {
+        const int warps = (int)((M + kMT - 1) / kMT);
+        switch (warps) {
+        case 1: gemv_i8_mb_kernel<1><<<tiles, 32, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
+        case 2: gemv_i8_mb_kernel<2><<<tiles, 64, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
+        case 3: gemv_i8_mb_kernel<3><<<tiles, 96, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
+        default: gemv_i8_mb_kernel<4><<<tiles, 128, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
+        }
+    }
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}

@@ -1,0 +1,247 @@
+// pack.cpp -- host side of libtg: status strings, layouts and the weight packer.
+//
+// The packer turns host trits into the device layouts described in tg.h:
+//  * ternary rows as the W_nonzero / W_negative bitmask pair (BitState brief
+//    §4), two bits per weight, interleaved so that one 32-bit word yields four
+//    lanes per byte-masked extract and one warp reads 512 contiguous bytes;
+//  * the 8 base-3 planes of the lm_head (SKaiNET issue #337, BITNET_PLANES)
+//    as two balanced base-3 digit groups of four planes, one byte per weight
+//    each, plus the row's own bound on the planes 4-7 residual.
+// Rows are split across host threads; the output does not depend on the
+// thread count.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "tg.h"
+#include "tg_internal.h"
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+
+int64_t align_up(int64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+template <class F>
+void parallel_rows(int64_t n, F fn)
+{
+    unsigned hw = std::thread::hardware_concurrency();
+    int64_t nt = std::max<int64_t>(1, std::min<int64_t>(hw ? hw : 1, 32));
+    if (n < 256)
+        nt = 1;
+    nt = std::min(nt, n);
+    if (nt <= 1) {
+        fn(0, n);
+        return;
+    }
+    std::vector<std::thread> pool;
+    int64_t per = (n + nt - 1) / nt;
+    for (int64_t t = 0; t < nt; t++) {
+        int64_t a = t * per, b = std::min(n, a + per);
+        if (a < b)
+            pool.emplace_back(fn, a, b);
+    }
+    for (auto &th : pool)
+        th.join();
+}
+
+void store_u32(uint8_t *p, uint32_t v)
+{
+    p[0] = (uint8_t)(v & 0xff);
+    p[1] = (uint8_t)((v >> 8) & 0xff);
+    p[2] = (uint8_t)((v >> 16) & 0xff);
+    p[3] = (uint8_t)((v >> 24) & 0xff);
+}
+
+}  // namespace
+
+extern "C" const char *tg_status_string(int status)
+{
+    switch (status) {
+    case TG_OK: return "ok";
+    case TG_ERR_ARG: return "invalid argument (null or misaligned pointer, unknown kind, wrong layout)";
+    case TG_ERR_SHAPE: return "invalid shape (N, K, M or k out of range)";
+    case TG_ERR_VALUE: return "invalid value (trit outside {-1,0,1} or row scale <= 0)";
+    case TG_ERR_BOUND: return "integer bound exceeded: a worst-case sum could overflow";
+    case TG_ERR_WORKSPACE: return "workspace or output buffer missing, misaligned or too small";
+    case TG_ERR_CUDA: return "CUDA error";
+    case TG_ERR_DEVICE: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int tg_layout_init(int kind, int64_t N, int64_t K, tg_layout *out)
+{
+    if (!out)
+        return TG_ERR_ARG;
+    if (kind != TG_TERNARY_I8 && kind != TG_TERNARY_LNS8 && kind != TG_PLANES8)
+        return TG_ERR_ARG;
+    if (N < 1 || K < TG_GROUP || K % TG_GROUP != 0 || N > ((int64_t)1 << 31) - 1 ||
+        K > ((int64_t)1 << 24))
+        return TG_ERR_SHAPE;
+    tg_layout L;
+    std::memset(&L, 0, sizeof(L));
+    L.kind = kind;
+    L.version = 1;
+    L.N = N;
+    L.K = K;
+    L.G = K / TG_GROUP;
+    if (kind == TG_PLANES8) {
+        L.tiles = 0;
+        L.mask_off = 0;
+        L.mask_bytes = N * K;
+        L.aux_off = align_up(L.mask_off + L.mask_bytes);
+        L.aux_bytes = N * K;
+        L.scale_off = align_up(L.aux_off + L.aux_bytes);
+        L.scale_bytes = N * 4;
+        L.aux2_off = align_up(L.scale_off + L.scale_bytes);
+        L.aux2_bytes = N;
+        L.total_bytes = align_up(L.aux2_off + L.aux2_bytes);
+    } else {
+        L.tiles = (N + tgi::kTileRows - 1) / tgi::kTileRows;
+        L.mask_off = 0;
+        L.mask_bytes = L.tiles * L.G * tgi::kTileRows * 32;
+        L.scale_off = align_up(L.mask_bytes);
+        L.scale_bytes = L.tiles * L.G * tgi::kTileRows * (kind == TG_TERNARY_I8 ? 4 : 1);
+        L.total_bytes = align_up(L.scale_off + L.scale_bytes);
+    }
+    *out = L;
+    return TG_OK;
+}
+
+extern "C" size_t tg_packed_bytes(int kind, int64_t N, int64_t K)
+{
+    tg_layout L;
+    if (tg_layout_init(kind, N, K, &L) != TG_OK)
+        return 0;
+    return (size_t)L.total_bytes;
+}
+
+namespace {
+
+// Two-bit field of one weight: bit 0 = W_nonzero, bit 1 = W_negative.
+inline uint32_t mask_field(int8_t v) { return (uint32_t)(v != 0) | ((uint32_t)(v < 0) << 1); }
+
+// Pack ternary rows [N][K] into the tiled mask layout; returns false on a bad trit.
+bool pack_masks(const tg_layout &L, const int8_t *t, uint8_t *out)
+{
+    const int64_t N = L.N, K = L.K, G = L.G;
+    std::vector<char> bad((size_t)L.tiles, 0);
+    parallel_rows(L.tiles, [&](int64_t t0, int64_t t1) {
+        for (int64_t T = t0; T < t1; T++) {
+            for (int64_t g = 0; g < G; g++) {
+                uint8_t *blk = out + L.mask_off + (T * G + g) * 1024;
+                for (int h = 0; h < 2; h++) {
+                    for (int l = 0; l < tgi::kTileRows; l++) {
+                        const int64_t r = T * tgi::kTileRows + l;
+                        uint8_t *chunk = blk + (h * 32 + l) * 16;
+                        for (int u = 0; u < 4; u++) {
+                            uint32_t word = 0;
+                            if (r < N) {
+                                const int8_t *src = t + r * K + g * TG_GROUP + h * 64 + u * 16;
+                                for (int j = 0; j < 4; j++) {
+                                    for (int b = 0; b < 4; b++) {
+                                        int8_t v = src[4 * j + b];
+                                        if (v < -1 || v > 1)
+                                            bad[(size_t)T] = 1;
+                                        word |= mask_field(v) << (8 * b + 2 * j);
+                                    }
+                                }
+                            }
+                            store_u32(chunk + 4 * u, word);
+                        }
+                    }
+                }
+            }
+        }
+    });
+    for (char b : bad)
+        if (b)
+            return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *trits,
+                               const void *scales, void *out_v, size_t out_bytes, tg_layout *layout)
+{
+    if (!trits || !scales || !out_v || !layout)
+        return TG_ERR_ARG;
+    tg_layout L;
+    int st = tg_layout_init(kind, N, K, &L);
+    if (st != TG_OK)
+        return st;
+    if (out_bytes < (size_t)L.total_bytes)
+        return TG_ERR_WORKSPACE;
+    uint8_t *out = static_cast<uint8_t *>(out_v);
+    std::memset(out, 0, (size_t)L.total_bytes);
+
+    if (kind == TG_TERNARY_I8 || kind == TG_TERNARY_LNS8) {
+        if (!pack_masks(L, trits, out))
+            return TG_ERR_VALUE;
+        const int64_t G = L.G;
+        int64_t maxabs = 0;
+        for (int64_t T = 0; T < L.tiles; T++) {
+            for (int64_t g = 0; g < G; g++) {
+                for (int l = 0; l < tgi::kTileRows; l++) {
+                    const int64_t r = T * tgi::kTileRows + l;
+                    const int64_t slot = (T * G + g) * tgi::kTileRows + l;
+                    if (kind == TG_TERNARY_I8) {
+                        int32_t d = r < N ? static_cast<const int32_t *>(scales)[r * G + g] : 0;
+                        int64_t a = d < 0 ? -(int64_t)d : (int64_t)d;
+                        maxabs = std::max(maxabs, a);
+                        store_u32(out + L.scale_off + slot * 4, (uint32_t)d);
+                    } else {
+                        uint8_t c = r < N ? static_cast<const uint8_t *>(scales)[r * G + g] : 0;
+                        maxabs = std::max<int64_t>(maxabs, c);
+                        out[L.scale_off + slot] = c;
+                    }
+                }
+            }
+        }
+        L.max_abs_scale = maxabs;
+    } else {
+        // TG_PLANES8: two balanced base-3 digit groups per weight, W = 81*hi + lo.
+        const int32_t *s = static_cast<const int32_t *>(scales);
+        int64_t maxs = 0;
+        for (int64_t r = 0; r < N; r++) {
+            if (s[r] <= 0)
+                return TG_ERR_VALUE;
+            maxs = std::max<int64_t>(maxs, s[r]);
+        }
+        const int64_t plane = N * K;
+        std::vector<char> bad((size_t)N, 0);
+        parallel_rows(N, [&](int64_t r0, int64_t r1) {
+            for (int64_t r = r0; r < r1; r++) {
+                int m = 0;
+                for (int64_t i = 0; i < K; i++) {
+                    int hi = 0, lo = 0;
+                    for (int p = 0; p < 8; p++) {
+                        int8_t v = trits[p * plane + r * K + i];
+                        if (v < -1 || v > 1)
+                            bad[(size_t)r] = 1;
+                        if (p < 4)
+                            hi = hi * 3 + v;
+                        else
+                            lo = lo * 3 + v;
+                    }
+                    out[L.mask_off + r * K + i] = (uint8_t)(int8_t)hi;
+                    out[L.aux_off + r * K + i] = (uint8_t)(int8_t)lo;
+                    m = std::max(m, lo < 0 ? -lo : lo);
+                }
+                out[L.aux2_off + r] = (uint8_t)m;
+                store_u32(out + L.scale_off + r * 4, (uint32_t)s[r]);
+            }
+        });
+        for (char b : bad)
+            if (b)
+                return TG_ERR_VALUE;
+        L.max_abs_scale = maxs;
+    }
+    *layout = L;
+    return TG_OK;
+}

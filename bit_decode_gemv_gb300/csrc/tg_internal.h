@@ -1,0 +1,24 @@
+// tg_internal.h -- definitions shared by the translation units of libtg.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "tg.h"
+
+namespace tgi {
+
+constexpr int kTileRows = 32;   // rows per mask tile: one row per lane of a warp
+
+// Largest number of warps the lm_head scan kernels launch; sizes the workspace.
+constexpr int kLmhMaxWarps = 8192;
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per translation unit: read-and-clear of that unit's device error word.
+// Each returns 0 or TG_ERR_DEVICE, or TG_ERR_CUDA if the query failed.
+int gemv_take_device_error(void *stream);
+int lns8_take_device_error(void *stream);
+int lmhead_take_device_error(void *stream);
+
+}  // namespace tgi

@@ -1,0 +1,218 @@
+"""Host-side checks of libtg.so that need no GPU.
+
+The library must load and export every entry point include/tg.h declares; the
+packer (pure host code) must write exactly the layout tg.h documents, checked
+here by decoding it with an independent reader; and every argument error must
+be reported before anything is enqueued. No test here launches a kernel.
+"""
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bit_decode_gemv_gb300 as tg
+from bit_decode_gemv_gb300 import build as tgbuild
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tgbuild.build()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "tg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 9
+    lib = C.CDLL(tg.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(tg.EXPORTS) == names
+
+
+def test_status_strings():
+    for code in range(-7, 1):
+        s = tg.tg_status_string(code)
+        assert s and s != "unknown status"
+    assert tg.tg_status_string(-99) == "unknown status"
+
+
+def test_layout_sizes():
+    L = tg.tg_layout_init(tg.TG_TERNARY_I8, 6912, 2560)
+    assert (L.tiles, L.G) == (216, 20)
+    assert L.mask_bytes == 216 * 20 * 1024 and L.scale_bytes == 216 * 20 * 32 * 4
+    assert L.scale_off % 256 == 0 and L.total_bytes % 256 == 0
+    assert tg.tg_packed_bytes(tg.TG_TERNARY_I8, 6912, 2560) == L.total_bytes
+    P = tg.tg_layout_init(tg.TG_PLANES8, 128256, 2560)
+    assert P.mask_bytes == P.aux_bytes == 128256 * 2560
+    assert P.scale_bytes == 128256 * 4 and P.aux2_bytes == 128256
+    for off in (P.aux_off, P.scale_off, P.aux2_off):
+        assert off % 256 == 0
+    assert tg.tg_packed_bytes(tg.TG_TERNARY_I8, 10, 100) == 0
+    for kind, N, K in ((tg.TG_TERNARY_I8, 0, 128), (tg.TG_TERNARY_I8, 4, 64), (tg.TG_PLANES8, 4, 200)):
+        with pytest.raises(tg.TgError) as e:
+            tg.tg_layout_init(kind, N, K)
+        assert e.value.status == tg.TG_ERR_SHAPE
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_layout_init(7, 4, 128)
+    assert e.value.status == tg.TG_ERR_ARG
+
+
+def decode_masked(blob, L, scale_dtype):
+    """Independent reader of the tiled mask layout -> (t [N][K], scales [N][G])."""
+    N, K, G, T = L.N, L.K, L.G, L.tiles
+    m = blob[L.mask_off:L.mask_off + L.mask_bytes].reshape(T, G, 2, 32, 16)
+    words = m.view("<u4").reshape(T, G, 2, 32, 4)                  # [T][G][h][row][u]
+    t = np.zeros((T * 32, K), dtype=np.int8)
+    for j in range(4):
+        for b in range(4):
+            sh = 8 * b + 2 * j
+            nz = (words >> sh) & 1
+            ng = (words >> (sh + 1)) & 1
+            assert not (ng & ~nz).any(), "W_negative outside W_nonzero"
+            val = nz.astype(np.int8) - 2 * ng.astype(np.int8)       # [T][G][h][row][u]
+            # lane within group = 64h + 16u + 4j + b
+            for h in range(2):
+                for u in range(4):
+                    lanes = np.arange(G) * 128 + 64 * h + 16 * u + 4 * j + b
+                    t[:, lanes] = val[:, :, h, :, u].transpose(0, 2, 1).reshape(T * 32, G)
+    s = blob[L.scale_off:L.scale_off + L.scale_bytes].view(scale_dtype).reshape(T, G, 32)
+    scales = s.transpose(0, 2, 1).reshape(T * 32, G)
+    return t, scales
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 256), (70, 640)])
+def test_pack_i8_layout(N, K):
+    w = W.tiny(seed=N, N=N, K=K)
+    blob, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    assert L.kind == tg.TG_TERNARY_I8 and L.max_abs_scale == int(np.abs(w["d"].astype(np.int64)).max())
+    t, s = decode_masked(blob, L, "<i4")
+    np.testing.assert_array_equal(t[:N], w["t"])
+    np.testing.assert_array_equal(s[:N], w["d"])
+    assert not t[N:].any() and not s[N:].any()          # padding rows are zero
+
+
+def test_pack_lns8_layout():
+    w = W.lns8(seed=1, N=45, K=384)
+    blob, L = tg.tg_pack_weights(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    t, s = decode_masked(blob, L, np.uint8)
+    np.testing.assert_array_equal(t[:45], w["t"])
+    np.testing.assert_array_equal(s[:45], w["dcode"])
+
+
+def test_pack_planes_layout():
+    w = W.lm_head(seed=2, N=37, K=256)
+    blob, L = tg.tg_pack_weights(tg.TG_PLANES8, w["planes"], w["s"])
+    N, K = 37, 256
+    hi = blob[L.mask_off:L.mask_off + N * K].view(np.int8).reshape(N, K).astype(np.int64)
+    lo = blob[L.aux_off:L.aux_off + N * K].view(np.int8).reshape(N, K).astype(np.int64)
+    pw = np.array([3 ** (7 - p) for p in range(8)], dtype=np.int64)
+    Wint = np.tensordot(pw, w["planes"].astype(np.int64), axes=(0, 0))
+    np.testing.assert_array_equal(81 * hi + lo, Wint)
+    assert np.abs(hi).max() <= 40 and np.abs(lo).max() <= 40
+    np.testing.assert_array_equal(blob[L.scale_off:L.scale_off + 4 * N].view("<i4"), w["s"])
+    m = blob[L.aux2_off:L.aux2_off + N]
+    np.testing.assert_array_equal(m, np.abs(lo).max(axis=1))
+    exact = ~w["planes"][1:].any(axis=(0, 2))
+    assert (m[exact] == 0).all()
+
+
+def test_pack_rejects_bad_values():
+    t = np.zeros((4, 128), np.int8)
+    t[2, 5] = 2
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_pack_weights(tg.TG_TERNARY_I8, t, np.ones((4, 1), np.int32))
+    assert e.value.status == tg.TG_ERR_VALUE
+    planes = np.zeros((8, 3, 128), np.int8)
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_pack_weights(tg.TG_PLANES8, planes, np.array([1, 0, 1], np.int32))
+    assert e.value.status == tg.TG_ERR_VALUE
+    planes[7, 1, 3] = -2
+    with pytest.raises(tg.TgError) as e:
+        tg.tg_pack_weights(tg.TG_PLANES8, planes, np.array([1, 1, 1], np.int32))
+    assert e.value.status == tg.TG_ERR_VALUE
+
+
+def test_pack_deterministic_across_calls():
+    w = W.ffn_up(seed=3, N=300, K=512)
+    a, _ = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    b, _ = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    np.testing.assert_array_equal(a, b)
+
+
+# Argument errors are all detected on the host, before any CUDA call; fake but
+# well-aligned addresses are enough to reach each check.
+A256 = 1 << 20
+
+
+def status_of(fn, *args):
+    with pytest.raises(tg.TgError) as e:
+        fn(*args)
+    return e.value.status
+
+
+def test_gemv_argument_errors():
+    w = W.tiny(seed=0, N=8, K=256)
+    _, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    f = tg.tg_gemv_i8
+    assert status_of(f, L, None, A256, 1, A256, 0) == tg.TG_ERR_ARG
+    assert status_of(f, L, A256 + 16, A256, 1, A256, 0) == tg.TG_ERR_ARG      # w not 256-aligned
+    assert status_of(f, L, A256, A256 + 1, 1, A256, 0) == tg.TG_ERR_ARG       # x not 16-aligned
+    assert status_of(f, L, A256, A256, 1, A256 + 4, 0) == tg.TG_ERR_ARG       # y not 8-aligned
+    assert status_of(f, L, A256, A256, 0, A256, 0) == tg.TG_ERR_SHAPE
+    assert status_of(f, L, A256, A256, 65, A256, 0) == tg.TG_ERR_SHAPE
+    bad = tg.tg_layout.from_buffer_copy(L)
+    bad.kind = tg.TG_PLANES8
+    assert status_of(f, bad, A256, A256, 1, A256, 0) == tg.TG_ERR_ARG
+    big = tg.tg_layout.from_buffer_copy(L)
+    big.G, big.K, big.max_abs_scale = 1 << 20, 128 << 20, (1 << 31) - 1
+    assert status_of(f, big, A256, A256, 1, A256, 0) == tg.TG_ERR_BOUND
+
+
+def test_lns8_argument_errors():
+    w = W.lns8(seed=0, N=8, K=256)
+    _, L = tg.tg_pack_weights(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    f = tg.tg_gemv_lns8_phase
+    assert status_of(f, L, A256, A256, None, None, 0) == tg.TG_ERR_ARG
+    assert status_of(f, L, A256, A256 + 8, A256, None, 0) == tg.TG_ERR_ARG
+    assert status_of(f, L, A256, A256, A256, A256 + 3, 0) == tg.TG_ERR_ARG
+    big = tg.tg_layout.from_buffer_copy(L)
+    big.K, big.G = 65536, 512
+    assert status_of(f, big, A256, A256, A256, None, 0) == tg.TG_ERR_BOUND
+
+
+def test_lmhead_argument_errors():
+    w = W.lm_head(seed=0, N=64, K=256)
+    _, L = tg.tg_pack_weights(tg.TG_PLANES8, w["planes"], w["s"])
+    wsb = tg.tg_lmhead_workspace_bytes(L, 10)
+    assert wsb >= 64 * 16
+    f = tg.tg_lmhead_argmax_topk
+    ok = dict(w=A256, x=A256, k=10, logits=None, argmax=A256, ids=A256, scores=A256, ncand=None,
+              ws=A256, ws_bytes=wsb)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return status_of(f, L, a["w"], a["x"], a["k"], a["logits"], a["argmax"], a["ids"],
+                         a["scores"], a["ncand"], a["ws"], a["ws_bytes"], 0)
+
+    assert call(argmax=None) == tg.TG_ERR_ARG
+    assert call(scores=A256 + 4) == tg.TG_ERR_ARG
+    assert call(k=0) == tg.TG_ERR_SHAPE
+    assert call(k=65) == tg.TG_ERR_SHAPE
+    assert call(ws=None) == tg.TG_ERR_WORKSPACE
+    assert call(ws_bytes=wsb - 1) == tg.TG_ERR_WORKSPACE
+    assert call(ws=A256 + 64) == tg.TG_ERR_WORKSPACE
+    big = tg.tg_layout.from_buffer_copy(L)
+    big.max_abs_scale = 1 << 31
+    assert status_of(f, big, A256, A256, 10, None, A256, A256, A256, None, A256, wsb, 0) == tg.TG_ERR_BOUND
+    assert tg.tg_lmhead_workspace_bytes(tg.tg_layout_init(tg.TG_TERNARY_I8, 8, 128), 4) == 0

@@ -1,0 +1,107 @@
+"""GPU parity of tg_gemv_i8 against the CPU oracle: bit-exact int64 outputs.
+
+Sizes the oracle finishes in seconds span several tiles and a ragged tail;
+the full-size workloads (ffn_up for batch 1, the batched M=64 case) run in the
+launch configuration the bench times and are compared on every output (batch
+1) or on sampled rows the oracle computes one by one (batched).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gpu_helpers import ensure_built
+    ensure_built()
+
+
+def check(w, rows=None):
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import gemv, pack_to_device
+    wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
+    y = gemv(wd, L, w["x"])
+    if rows is None:
+        ref = oracle.gemv_i8(w["t"], w["d"], w["x"])
+        np.testing.assert_array_equal(y, ref)
+    else:
+        ref = oracle.gemv_i8(w["t"][rows], w["d"][rows], w["x"])
+        np.testing.assert_array_equal(y[:, rows], ref)
+    return y
+
+
+def test_tiny_workload():
+    check(W.tiny())
+
+
+def test_ffn_up_workload_full_size():
+    check(W.ffn_up())
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (31, 128), (33, 256), (100, 384), (257, 2560),
+                                 (6913, 2560), (64, 6912), (40, 16384)])
+def test_ragged_shapes(N, K):
+    check(W.ffn_up(seed=N + K, N=N, K=K))
+
+
+def test_extreme_values():
+    N, K = 70, 1024
+    t = -np.ones((N, K), np.int8)
+    d = np.full((N, K // 128), np.iinfo(np.int32).min, np.int32)
+    d[::2] = np.iinfo(np.int32).max
+    x = np.full((1, K), -128, np.int8)
+    y = check(dict(t=t, d=d, x=x))
+    assert y[0, 0] == (K // 128) * 128 * 128 * np.iinfo(np.int32).max
+    # mixed signs, zero rows, a single nonzero lane
+    w = W.tiny(seed=1, N=N, K=K)
+    w["t"][5] = 0
+    w["x"][:] = 0
+    w["x"][0, 777] = -128
+    check(w)
+
+
+@pytest.mark.parametrize("M", [2, 7, 16, 17, 33, 64])
+def test_small_batch(M):
+    check(W.batched(seed=M, M=M, N=97, K=640))
+
+
+def test_batched_workload_full_size_sampled_rows():
+    w = W.batched()
+    rows = np.concatenate([np.arange(0, 40), np.arange(6900, 6950),
+                           np.random.default_rng(0).choice(13824, 100, replace=False),
+                           np.arange(13800, 13824)])
+    check(w, rows=np.unique(rows))
+
+
+def test_deterministic_and_shard_invariant():
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import gemv, pack_to_device
+    w = W.ffn_up(seed=5, N=1000, K=2560)
+    wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
+    y1 = gemv(wd, L, w["x"])
+    y2 = gemv(wd, L, w["x"])
+    np.testing.assert_array_equal(y1, y2)
+    # rows split into two independently packed shards give the same outputs
+    parts = []
+    for sl in (slice(0, 413), slice(413, 1000)):
+        wd_s, L_s = pack_to_device(tg.TG_TERNARY_I8, w["t"][sl], w["d"][sl])
+        parts.append(gemv(wd_s, L_s, w["x"]))
+    np.testing.assert_array_equal(np.concatenate(parts, axis=1), y1)
+
+
+def test_output_untouched_on_argument_error():
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import dev, pack_to_device
+    w = W.tiny(seed=2, N=64, K=256)
+    wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
+    y = torch.full((1, 64), 12345, dtype=torch.int64, device="cuda")
+    with pytest.raises(tg.TgError):
+        tg.tg_gemv_i8(L, wd, dev(w["x"]), 0, y)
+    torch.cuda.synchronize()
+    assert (y == 12345).all()
