@@ -266,6 +266,7 @@ def capture_graph(torch, fn, count):
 
 
 def event_time(torch, fn, reps, stream):
+    """Seconds for reps calls of fn, between CUDA events on `stream` (a torch.cuda.Stream)."""
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -378,7 +379,7 @@ def run_row_only(args):
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
-    print(json.dumps(measure_rows(tg, torch, torch.cuda.current_stream().cuda_stream, dev,
+    print(json.dumps(measure_rows(tg, torch, torch.cuda.current_stream(), dev,
                                   args.row.split(","))), flush=True)
 
 
@@ -523,7 +524,7 @@ def run_ours(args):
     del wd
     torch.cuda.empty_cache()
     if not args.no_rows:
-        line["rows"] = measure_rows(tg, torch, s_handle, dev)
+        line["rows"] = measure_rows(tg, torch, stream, dev)
     print(json.dumps(line), flush=True)
 
 
