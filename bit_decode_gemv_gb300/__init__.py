@@ -34,6 +34,7 @@ TG_PLANES8 = 3
 TG_GROUP = 128
 TG_MAX_M = 64
 TG_MAX_K = 1024
+TG_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 # Every symbol include/tg.h declares.
 EXPORTS = (
@@ -45,6 +46,7 @@ EXPORTS = (
     "tg_gemv_lns8_phase",
     "tg_lmhead_workspace_bytes",
     "tg_lmhead_argmax_topk",
+    "tg_lmhead_argmax_topk_noalloc",
     "tg_device_error",
 )
 
@@ -91,9 +93,10 @@ def lib():
         L.tg_lmhead_workspace_bytes.argtypes = [lp, i32]
         L.tg_lmhead_workspace_bytes.restype = sz
         L.tg_lmhead_argmax_topk.argtypes = [lp, p, p, i32, p, p, p, p, p, p, sz, p]
+        L.tg_lmhead_argmax_topk_noalloc.argtypes = [lp, p, p, i32, p, p, p, p, p, p]
         L.tg_device_error.argtypes = [p, C.POINTER(i32)]
         for name in ("tg_layout_init", "tg_pack_weights", "tg_gemv_i8", "tg_gemv_lns8_phase",
-                     "tg_lmhead_argmax_topk", "tg_device_error"):
+                     "tg_lmhead_argmax_topk", "tg_lmhead_argmax_topk_noalloc", "tg_device_error"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -190,6 +193,16 @@ def tg_lmhead_argmax_topk(layout: tg_layout, w, x, k: int, logits, argmax, ids, 
     _check(lib().tg_lmhead_argmax_topk(C.byref(layout), _ptr(w), _ptr(x), int(k), _ptr(logits),
                                        _ptr(argmax), _ptr(ids), _ptr(scores), _ptr(ncand), _ptr(ws),
                                        int(ws_bytes), _stream(stream)), "tg_lmhead_argmax_topk")
+
+
+def tg_lmhead_argmax_topk_noalloc(layout: tg_layout, w, x, k: int, logits, argmax, ids, scores,
+                                  ncand, stream=None) -> None:
+    """tg_lmhead_argmax_topk on the library's own fixed scratch, for callers that
+    cannot allocate device memory (see include/tg.h for the limit and the sharing rules)."""
+    _check(lib().tg_lmhead_argmax_topk_noalloc(C.byref(layout), _ptr(w), _ptr(x), int(k),
+                                               _ptr(logits), _ptr(argmax), _ptr(ids), _ptr(scores),
+                                               _ptr(ncand), _stream(stream)),
+           "tg_lmhead_argmax_topk_noalloc")
 
 
 def tg_device_error(stream=None) -> int:

@@ -202,6 +202,36 @@ int tg_lmhead_argmax_topk(const tg_layout *layout, const void *w, const int8_t *
                           int64_t *logits, int32_t *argmax, int32_t *ids, int64_t *scores,
                           int32_t *ncand, void *ws, size_t ws_bytes, void *stream);
 
+/* Size of the library's own lm_head scratch used by tg_lmhead_argmax_topk_noalloc. */
+#define TG_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/*
+ * tg_lmhead_argmax_topk without a caller workspace. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory themselves: a plugin whose host framework hands out device memory only
+ * through its own allocator, a serving process whose device memory is already
+ * reserved by a cache pool, or a latency-critical loop that may not call
+ * cudaMalloc because it can block on the device.
+ *
+ * Same arguments, results and errors as tg_lmhead_argmax_topk, minus ws and
+ * ws_bytes: the workspace is a fixed array of TG_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory, which every GPU that loads the library keeps
+ * until the process exits. The call itself allocates nothing.
+ *   - Limit: problems whose tg_lmhead_workspace_bytes(layout, k) exceeds
+ *     TG_NOALLOC_SCRATCH_BYTES (N above about 258,000 rows) are rejected with
+ *     TG_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current and caches it; make that first call before any stream
+ *     capture. A failed lookup returns TG_ERR_CUDA.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (nothing needs to be cleared: the kernels write what they read).
+ *     Calls whose work overlaps on the GPU race on it; the caller must order
+ *     them (one stream, or explicit events).
+ */
+int tg_lmhead_argmax_topk_noalloc(const tg_layout *layout, const void *w, const int8_t *x,
+                                  int32_t k, int64_t *logits, int32_t *argmax, int32_t *ids,
+                                  int64_t *scores, int32_t *ncand, void *stream);
+
 /*
  * Read and clear the device error word: *code receives 0, or TG_ERR_DEVICE if
  * a kernel gave up a bounded wait since the last read. Synchronises `stream`.
