@@ -35,6 +35,7 @@ TG_GROUP = 128
 TG_MAX_M = 64
 TG_MAX_K = 1024
 TG_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
+TG_FLAG_CONST_WEIGHTS = 1
 
 # Every symbol include/tg.h declares.
 EXPORTS = (
@@ -60,7 +61,8 @@ class tg_layout(C.Structure):
         ("aux_off", C.c_int64), ("aux_bytes", C.c_int64),
         ("aux2_off", C.c_int64), ("aux2_bytes", C.c_int64),
         ("total_bytes", C.c_int64), ("max_abs_scale", C.c_int64),
-        ("reserved", C.c_int64 * 4),
+        ("flags", C.c_int64),
+        ("reserved", C.c_int64 * 3),
     ]
 
 

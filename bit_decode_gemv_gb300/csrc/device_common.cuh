@@ -47,6 +47,13 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v)
 
 __device__ __forceinline__ int warp_sum_i32(int v) { return __reduce_add_sync(0xffffffffu, v); }
 
+// Programmatic dependent launch: allow the next kernel on the stream to start
+// launching, and wait until the previous kernel on the stream has finished and
+// its writes are visible. Both are no-ops for a kernel launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace tgi
 
 // Each translation unit holds one device error word, set by a kernel that

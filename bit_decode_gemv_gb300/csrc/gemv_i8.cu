@@ -35,6 +35,14 @@ namespace {
 using tgi::dp4a_us;
 using tgi::kTileRows;
 
+// (w & mask) ^ flip in one LOP3 (truth table 0x6A = (a & b) ^ c).
+__device__ __forceinline__ uint32_t and_xor(uint32_t w, uint32_t mask, uint32_t flip)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(w), "r"(mask), "r"(flip));
+    return r;
+}
+
 // Column sums of one 128-lane group for one row: w[0..7] are the row's eight
 // mask words (half 0 then half 1), xg the group's 128 activations in shared
 // memory. Returns sum_i (t_i + 2) x_i.
@@ -44,32 +52,38 @@ __device__ __forceinline__ int group_dot_t2(const uint32_t w[8], const int8_t *x
 #pragma unroll
     for (int u = 0; u < 8; u++) {
         const uint4 xv = *reinterpret_cast<const uint4 *>(xg + 16 * u);
-        a0 = dp4a_us((w[u] & 0x03030303u) ^ 0x02020202u, xv.x, a0);
-        a1 = dp4a_us((w[u] & 0x0C0C0C0Cu) ^ 0x08080808u, xv.y, a1);
-        a2 = dp4a_us((w[u] & 0x30303030u) ^ 0x20202020u, xv.z, a2);
-        a3 = dp4a_us((w[u] & 0xC0C0C0C0u) ^ 0x80808080u, xv.w, a3);
+        a0 = dp4a_us(and_xor(w[u], 0x03030303u, 0x02020202u), xv.x, a0);
+        a1 = dp4a_us(and_xor(w[u], 0x0C0C0C0Cu, 0x08080808u), xv.y, a1);
+        a2 = dp4a_us(and_xor(w[u], 0x30303030u, 0x20202020u), xv.z, a2);
+        a3 = dp4a_us(and_xor(w[u], 0xC0C0C0C0u, 0x80808080u), xv.w, a3);
     }
     return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
 }
 
 // ---------------------------------------------------------------------------
 // Batch 1. One CTA per tile of 32 rows; lane l of every warp owns row 32T + l;
-// the CTA's warps split the row's groups (warp w takes g = w, w + W, ...), and
-// the per-warp int64 partials are summed through shared memory at the end.
-// All mask loads of a warp's batch are issued before the activation tile is
-// staged, so the whole tile is in flight while x lands in shared memory.
+// the CTA's W warps split the row's groups (warp w takes g = w, w + W, ...;
+// W = ceil(G / GPW), so each thread holds at most GPW groups), and the per-warp
+// int64 partials are summed through shared memory at the end. Every weight
+// load of the CTA is issued first, so a whole tile is in flight at once.
+// Launched as a programmatic dependent (constant weights), the kernel streams
+// its weights before it waits for the previous kernel on the stream, reads x
+// only after that wait, and lets the next kernel launch once its own compute
+// is done -- which keeps one GEMV's weight stream ahead of the current one's
+// compute without flooding the memory system with several.
 // ---------------------------------------------------------------------------
-template <int WARPS, int GPW>
-__global__ void __launch_bounds__(WARPS * 32)
+template <int GPW>
+__global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
 gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
                   const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     int8_t *xs = reinterpret_cast<int8_t *>(smem);                   // [G*128]
     int *tsum = reinterpret_cast<int *>(smem + G * 128);             // [G]
-    int64_t *red = reinterpret_cast<int64_t *>(smem + G * 128 + ((G * 4 + 15) & ~15));  // [WARPS][32]
+    int64_t *red = reinterpret_cast<int64_t *>(smem + G * 128 + ((G * 4 + 15) & ~15));  // [W][32]
 
     const int tile = blockIdx.x;
+    const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint4 *tmask = masks + (size_t)tile * G * 64;               // 64 uint4 per (tile, group)
@@ -80,7 +94,7 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     auto load_batch = [&](int g0) {
 #pragma unroll
         for (int j = 0; j < GPW; j++) {
-            const int g = g0 + j * WARPS;
+            const int g = g0 + j * nwarps;
             if (g < G) {
                 m0[j] = tgi::ldg_stream(tmask + g * 64 + lane);
                 m1[j] = tgi::ldg_stream(tmask + g * 64 + 32 + lane);
@@ -92,12 +106,13 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         }
     };
     load_batch(warp);
+    tgi::pdl_wait();
 
     // Stage x and the per-group activation totals.
     const int K = G * 128;
-    for (int i = threadIdx.x; i < K / 16; i += WARPS * 32)
+    for (int i = threadIdx.x; i < K / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-    for (int g = warp; g < G; g += WARPS) {
+    for (int g = warp; g < G; g += nwarps) {
         const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + g * 128) + lane);
         const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
         if (lane == 0)
@@ -109,7 +124,7 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     for (int g0 = warp;;) {
 #pragma unroll
         for (int j = 0; j < GPW; j++) {
-            const int g = g0 + j * WARPS;
+            const int g = g0 + j * nwarps;
             if (g < G) {
                 const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
                                        m1[j].x, m1[j].y, m1[j].z, m1[j].w};
@@ -117,18 +132,18 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
                 acc += (int64_t)dg[j] * (int64_t)P;
             }
         }
-        g0 += WARPS * GPW;
+        g0 += nwarps * GPW;
         if (g0 >= G)
             break;
         load_batch(g0);
     }
 
+    tgi::pdl_launch_dependents();
     red[warp * 32 + lane] = acc;
     __syncthreads();
     if (warp == 0) {
         int64_t sum = 0;
-#pragma unroll
-        for (int w = 0; w < WARPS; w++)
+        for (int w = 0; w < nwarps; w++)
             sum += red[w * 32 + lane];
         const int row = tile * kTileRows + lane;
         if (row < N)
@@ -233,10 +248,35 @@ gemv_i8_mb_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     }
 }
 
-constexpr int kM1Warps = 4;
-constexpr int kM1Gpw = 6;
+size_t m1_smem_bytes(int G, int warps) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + warps * 32 * 8; }
 
-size_t m1_smem_bytes(int G) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + kM1Warps * 32 * 8; }
+template <int GPW>
+cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
+                      int G, int tiles, bool pdl, cudaStream_t s)
+{
+    auto kern = gemv_i8_m1_kernel<GPW>;
+    const int max_warps = GPW >= 4 ? 16 : 32;
+    int warps = (G + GPW - 1) / GPW;
+    if (warps > max_warps)
+        warps = max_warps;
+    const size_t smem = m1_smem_bytes(G, warps);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G);
+}
 
 }  // namespace
 
@@ -263,16 +303,20 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
     const int tiles = (int)L->tiles;
 
     if (M == 1) {
-        const size_t smem = m1_smem_bytes(G);
-        auto kern = gemv_i8_m1_kernel<kM1Warps, kM1Gpw>;
-        if (smem > 48 * 1024) {
-            if (smem > 200 * 1024)
-                return TG_ERR_SHAPE;
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess)
-                return TG_ERR_CUDA;
-        }
-        kern<<<tiles, kM1Warps * 32, smem, s>>>(masks, scales, x, y, N, G);
+        if (m1_smem_bytes(G, 32) > 200 * 1024)
+            return TG_ERR_SHAPE;
+        const bool pdl = (L->flags & TG_FLAG_CONST_WEIGHTS) != 0;
+        // One group per warp up to K = 4096 (32 warps), then two per warp up to
+        // K = 8192; beyond that 16 warps loop over batches of four groups each.
+        cudaError_t e;
+        if (G <= 32)
+            e = launch_m1<1>(masks, scales, x, y, N, G, tiles, pdl, s);
+        else if (G <= 64)
+            e = launch_m1<2>(masks, scales, x, y, N, G, tiles, pdl, s);
+        else
+            e = launch_m1<4>(masks, scales, x, y, N, G, tiles, pdl, s);
+        if (e != cudaSuccess)
+            return TG_ERR_CUDA;
     } else {
         const int warps = (int)((M + kMT - 1) / kMT);
         switch (warps) {

@@ -10,15 +10,26 @@
 //   1. scan     every row: s1 = 81 * sum hi*x. Its planes 4-7 residual is at
 //               most m[r] * sum|x| (m[r] = the row's max |lo| <= 40), so
 //               lo_r = s*s1 - s*m*sum|x| <= exact_r <= s*s1 + s*m*sum|x| = hi_r.
-//               Each warp also keeps the largest lo_r it saw.
-//   2. select   tau = the k-th largest of those per-warp maxima. They are k or
-//               more distinct rows' lower bounds, so tau <= the k-th largest
-//               lower bound over all rows <= the k-th largest exact logit.
-//   3. rescore  every row with hi_r >= tau (this includes every row of the true
-//               top-k) is rescored exactly with planes 4-7 and appended as a key.
-//   4. final    the top-k of the appended keys.
+//               Each warp counts the largest lo_r it saw in a histogram of
+//               scores (below).
+//   2. rescore  tau = the lower edge of the histogram bin that holds the k-th
+//               largest of those per-warp maxima. They are lower bounds of k or
+//               more distinct rows, so tau <= the k-th largest lower bound over
+//               all rows <= the k-th largest exact logit; every row with
+//               hi_r >= tau (this includes every row of the true top-k) is
+//               rescored exactly with planes 4-7, appended as a key, and its
+//               exact logit counted in a second histogram.
+//   3. final    tau2 = the lower edge of the bin that holds the k-th largest
+//               rescored logit; the candidates at or above it (about k) are
+//               ranked against each other and written in order.
 // Full path (logits != NULL): one scan over both digit groups writes every
-// exact logit and each warp's best key; 2-4 as above on the exact keys.
+// exact logit and counts each warp's largest; the rows at or above the k-th
+// bin's edge are appended and step 3 runs on them.
+//
+// Score histogram. 6144 bins on a log scale: one bin for every score <= 0,
+// one per integer for 1..63, then 64 bins per power of two (the leading bit's
+// position and the next six bits), so a bin spans under 1/64 of its values.
+// A bin's lower edge is a valid lower bound for every score in it.
 //
 // Keys. A score and its row pack into one int64, key = score * 2^b +
 // (2^b - 1 - r) with 2^b >= N, so that a larger key means a larger score or,
@@ -40,41 +51,131 @@ namespace {
 using tgi::dp4a_ss;
 
 constexpr int kScanWarps = 8;       // warps per CTA of the scan kernels
-constexpr int kSelThreads = 1024;   // threads of the selection kernels
-constexpr int kSortMax = 8192;      // keys sorted at once in shared memory
+constexpr int kSelThreads = 1024;   // threads of the final selection
+constexpr int kHistBins = 6144;     // score histogram bins
+constexpr int kFilterMax = 4096;    // candidates at or above tau2 ranked directly
 constexpr uint64_t kSignBit = 0x8000000000000000ull;
 
+// Workspace: a region cleared at the start of every call, then per-row data.
 struct Ws {
-    int64_t *s1;      // [N]  stage-1 sum (two-stage path)
-    int64_t *best;    // [kLmhMaxWarps]  per-warp largest lower bound / key
-    int64_t *ctl;     // [0] tau, [1] candidate count
-    uint64_t *cand;   // [N]  candidate keys, sign bit flipped (unsigned order)
+    unsigned long long *count;   // candidates appended
+    unsigned *hist_row;          // [kHistBins] scores of every row
+    unsigned *hist_cand;         // [kHistBins] exact scores of the candidates
+    int64_t *s1;                 // [N] stage-1 sums (two-stage path)
+    uint64_t *cand;              // [N] candidate keys, sign bit flipped (unsigned order)
 };
+constexpr size_t kClearedBytes = 256 + 2 * (size_t)kHistBins * sizeof(unsigned);
 
 __device__ __forceinline__ uint64_t to_ordered(int64_t v) { return (uint64_t)v ^ kSignBit; }
 __device__ __forceinline__ int64_t from_ordered(uint64_t u) { return (int64_t)(u ^ kSignBit); }
 
+__device__ __forceinline__ int score_bin(int64_t v)
+{
+    if (v <= 0)
+        return 0;
+    if (v < 64)
+        return 2048 + (int)v;
+    const int e = 63 - __clzll(v);                  // 6..62
+    const int m = (int)((v >> (e - 6)) & 63);
+    return 2048 + 64 * (e - 5) + m;                 // 2112..5759
+}
+
+__device__ __forceinline__ int64_t bin_edge(int b)
+{
+    if (b < 2048)
+        return INT64_MIN;
+    if (b < 2112)
+        return (int64_t)(b - 2048);
+    const int t = b - 2048;
+    return (int64_t)(64 + (t & 63)) << (t / 64 - 1);
+}
+
+// Lower edge of the bin that holds the k-th largest counted score, found by
+// one warp from the top of the histogram in two levels (32 ranges of 192
+// bins, then the chosen range as 32 runs of 6), every level's loads issued
+// together. INT64_MIN if fewer than k scores were counted.
+__device__ int64_t warp_kth_bin_edge(const unsigned *hist, int k)
+{
+    constexpr int per = kHistBins / 32;              // 192 bins per lane
+    constexpr int run = per / 32;                    // 6 bins per lane in level 2
+    const int lane = threadIdx.x & 31;
+
+    // level 1: lane l owns bins [top - per, top) with top = kHistBins - per * l
+    const int top = kHistBins - per * lane;
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(hist + top - per);
+    unsigned mine = 0;
+#pragma unroll 8
+    for (int j = 0; j < per / 4; j++) {
+        const uint4 v = h4[j];
+        mine += v.x + v.y + v.z + v.w;
+    }
+    unsigned incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    unsigned owner = __ballot_sync(0xffffffffu, incl - mine < (unsigned)k && (unsigned)k <= incl);
+    if (!owner)
+        return INT64_MIN;
+    int src = __ffs(owner) - 1;
+    const unsigned before1 = __shfl_sync(0xffffffffu, incl - mine, src);
+    const int top1 = kHistBins - per * src;
+
+    // level 2: lane j owns bins [top1 - run*(j+1), top1 - run*j)
+    const int top2 = top1 - run * lane;
+    unsigned c[run], mine2 = 0;
+#pragma unroll
+    for (int i = 0; i < run; i++) {
+        c[i] = hist[top2 - 1 - i];
+        mine2 += c[i];
+    }
+    unsigned incl2 = mine2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl2, o);
+        if (lane >= o)
+            incl2 += v;
+    }
+    const unsigned start2 = before1 + incl2 - mine2;
+    int found = -1;
+    if (start2 < (unsigned)k && (unsigned)k <= before1 + incl2) {
+        unsigned cum = start2;
+#pragma unroll
+        for (int i = 0; i < run; i++) {
+            if (found < 0 && cum + c[i] >= (unsigned)k)
+                found = top2 - 1 - i;
+            cum += c[i];
+        }
+    }
+    owner = __ballot_sync(0xffffffffu, found >= 0);
+    found = __shfl_sync(0xffffffffu, found, __ffs(owner) - 1);
+    return bin_edge(found);
+}
+
+// sum_i |x_i| computed by warp 0 (|v| = v * (v < 0 ? -1 : 1) per byte in one dp4a).
+__device__ __forceinline__ int64_t warp_sum_abs(const int8_t *x, int K)
+{
+    const int lane = threadIdx.x & 31;
+    int sa = 0;
+    for (int i = lane; i < K / 4; i += 32) {
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x) + i);
+        const uint32_t neg = (v & 0x80808080u) >> 7;
+        sa = dp4a_ss(v, (neg * 0xFEu) | 0x01010101u, sa);
+    }
+    return (int64_t)tgi::warp_sum_i32(sa);
+}
+
 // The lane's CPL chunks of x (16 bytes each): chunk lane + 32 j.
 template <int CPL>
-__device__ __forceinline__ void load_x(const int8_t *x, int C16, int lane, uint4 (&xr)[CPL],
-                                       int64_t &sum_abs)
+__device__ __forceinline__ void load_x(const int8_t *x, int C16, int lane, uint4 (&xr)[CPL])
 {
-    int sa = 0;
 #pragma unroll
     for (int j = 0; j < CPL; j++) {
         const int c = lane + 32 * j;
         xr[j] = c < C16 ? __ldg(reinterpret_cast<const uint4 *>(x) + c) : make_uint4(0, 0, 0, 0);
-        const uint32_t v[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int xb = (int)(int8_t)((v[q] >> (8 * b)) & 0xff);
-                sa += xb < 0 ? -xb : xb;
-            }
-        }
     }
-    sum_abs = (int64_t)tgi::warp_sum_i32(sa);
 }
 
 template <int CPL>
@@ -98,19 +199,26 @@ __device__ __forceinline__ int row_dot(const int8_t *row, int C16, int lane, con
 }
 
 // 1. Stage-1 scan over planes 0-3; two rows per warp iteration keep 2 * CPL
-// 16-byte loads per lane in flight.
+// 16-byte loads per lane in flight. Each warp counts its largest lower bound.
 template <int CPL>
 __global__ void __launch_bounds__(kScanWarps * 32)
 lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
                   const uint8_t *__restrict__ m, const int8_t *__restrict__ x, Ws ws, int N, int K)
 {
+    __shared__ int64_t sh_sum_abs;
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
     uint4 xr[CPL];
-    int64_t sum_abs;
-    load_x<CPL>(x, C16, lane, xr, sum_abs);
+    load_x<CPL>(x, C16, lane, xr);
+    if (threadIdx.x < 32) {
+        const int64_t sa = warp_sum_abs(x, K);
+        if (lane == 0)
+            sh_sum_abs = sa;
+    }
+    __syncthreads();
+    const int64_t sum_abs = sh_sum_abs;
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += 2 * NW) {
@@ -132,25 +240,23 @@ lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
             }
         }
     }
-    if (lane == 0)
-        ws.best[wg] = best;
+    if (lane == 0 && best != INT64_MIN)
+        atomicAdd(&ws.hist_row[score_bin(best)], 1u);
 }
 
-// Full path: exact logits from both digit groups, and each warp's best key.
+// Full path: exact logits from both digit groups; each warp counts its largest.
 template <int CPL>
 __global__ void __launch_bounds__(kScanWarps * 32)
 lmh_full_kernel(const int8_t *__restrict__ hi, const int8_t *__restrict__ lo,
                 const int32_t *__restrict__ s, const int8_t *__restrict__ x, int64_t *__restrict__ logits,
-                Ws ws, int N, int K, int idx_bits)
+                Ws ws, int N, int K)
 {
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
     uint4 xr[CPL];
-    int64_t sum_abs;
-    load_x<CPL>(x, C16, lane, xr, sum_abs);
-    const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
+    load_x<CPL>(x, C16, lane, xr);
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += NW) {
@@ -161,58 +267,16 @@ lmh_full_kernel(const int8_t *__restrict__ hi, const int8_t *__restrict__ lo,
         if (lane == 0) {
             const int64_t logit = (int64_t)__ldg(s + r) * (81 * (int64_t)th + (int64_t)tl);
             logits[r] = logit;
-            best = max(best, logit * (low_mask + 1) + (low_mask - r));
+            best = max(best, logit);
         }
     }
-    if (lane == 0)
-        ws.best[wg] = best;
+    if (lane == 0 && best != INT64_MIN)
+        atomicAdd(&ws.hist_row[score_bin(best)], 1u);
 }
 
-// Bitonic sort of P (a power of two) ordered keys in shared memory, descending.
-__device__ void block_sort_desc(uint64_t *v, int P)
-{
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            __syncthreads();
-            for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-                const int a = 2 * i - (i & (stride - 1));
-                const int b = a + stride;
-                const uint64_t ua = v[a], ub = v[b];
-                const bool desc = (a & size) == 0;
-                if (desc ? (ua < ub) : (ua > ub)) {
-                    v[a] = ub;
-                    v[b] = ua;
-                }
-            }
-        }
-    }
-    __syncthreads();
-}
-
-__host__ __device__ inline int next_pow2(int n)
-{
-    int p = 1;
-    while (p < n)
-        p <<= 1;
-    return p;
-}
-
-// 2. tau = the k-th largest per-warp entry (INT64_MIN if there are fewer than k).
-__global__ void __launch_bounds__(kSelThreads) lmh_threshold_kernel(Ws ws, int nw, int k)
-{
-    extern __shared__ __align__(16) uint64_t sv[];
-    const int P = next_pow2(nw < 2 ? 2 : nw);
-    for (int i = threadIdx.x; i < P; i += blockDim.x)
-        sv[i] = i < nw ? to_ordered(ws.best[i]) : 0ull;
-    block_sort_desc(sv, P);
-    if (threadIdx.x == 0) {
-        ws.ctl[0] = nw >= k ? from_ordered(sv[k - 1]) : INT64_MIN;
-        ws.ctl[1] = 0;
-    }
-}
-
-// Warp-aggregated append of this lane's key (if `take`) to the candidate list.
-__device__ __forceinline__ void append_key(Ws ws, bool take, uint64_t key)
+// Append this lane's key (if `take`) to the candidate list, one atomic per
+// warp, and count the candidate's exact score.
+__device__ __forceinline__ void append_key(Ws ws, bool take, uint64_t key, int64_t score)
 {
     const unsigned mask = __ballot_sync(0xffffffffu, take);
     if (!mask)
@@ -221,27 +285,38 @@ __device__ __forceinline__ void append_key(Ws ws, bool take, uint64_t key)
     const int leader = __ffs(mask) - 1;
     unsigned long long base = 0;
     if (lane == leader)
-        base = atomicAdd(reinterpret_cast<unsigned long long *>(ws.ctl + 1), (unsigned long long)__popc(mask));
+        base = atomicAdd(ws.count, (unsigned long long)__popc(mask));
     base = __shfl_sync(0xffffffffu, base, leader);
-    if (take)
+    if (take) {
         ws.cand[base + __popc(mask & ((1u << lane) - 1))] = key;
+        atomicAdd(&ws.hist_cand[score_bin(score)], 1u);
+    }
 }
 
-// 3. Rescore every row whose upper bound reaches tau, exactly, with planes 4-7.
+// 2. Rescore every row whose upper bound reaches tau, exactly, with planes 4-7.
 template <int CPL>
 __global__ void __launch_bounds__(kScanWarps * 32)
 lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
                    const uint8_t *__restrict__ m, const int8_t *__restrict__ x, Ws ws, int N, int K,
-                   int idx_bits)
+                   int k, int idx_bits)
 {
+    __shared__ int64_t sh[2];
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
     uint4 xr[CPL];
-    int64_t sum_abs;
-    load_x<CPL>(x, C16, lane, xr, sum_abs);
-    const int64_t tau = ws.ctl[0];
+    load_x<CPL>(x, C16, lane, xr);
+    if (threadIdx.x < 32) {
+        const int64_t sa = warp_sum_abs(x, K);
+        const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
+        if (lane == 0) {
+            sh[0] = sa;
+            sh[1] = tau;
+        }
+    }
+    __syncthreads();
+    const int64_t sum_abs = sh[0], tau = sh[1];
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
 
     for (int base = wg * 32; base < N; base += NW * 32) {
@@ -253,78 +328,266 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
             s1 = ws.s1[r];
             cand = sc * s1 + sc * (int64_t)__ldg(m + r) * sum_abs >= tau;
         }
+        // candidates of this block of 32 rows, two at a time so that both rows'
+        // loads are in flight together
         unsigned todo = __ballot_sync(0xffffffffu, cand);
         while (todo) {
-            const int src = __ffs(todo) - 1;
+            const int src0 = __ffs(todo) - 1;
             todo &= todo - 1;
-            const int rc = base + src;
-            const int64_t csc = __shfl_sync(0xffffffffu, sc, src);
-            const int64_t cs1 = __shfl_sync(0xffffffffu, s1, src);
-            const int t = tgi::warp_sum_i32(row_dot<CPL>(lo + (size_t)rc * K, C16, lane, xr));
-            const int64_t exact = csc * (cs1 + (int64_t)t);
-            const uint64_t key = to_ordered(exact * (low_mask + 1) + (low_mask - rc));
-            if (lane == 0) {
-                const unsigned long long slot =
-                    atomicAdd(reinterpret_cast<unsigned long long *>(ws.ctl + 1), 1ull);
-                ws.cand[slot] = key;
+            const int src1 = todo ? __ffs(todo) - 1 : src0;
+            const bool two = todo != 0;
+            if (two)
+                todo &= todo - 1;
+            const int r0 = base + src0, r1 = base + src1;
+            uint4 h0[CPL], h1[CPL];
+#pragma unroll
+            for (int j = 0; j < CPL; j++) {
+                const int c = lane + 32 * j;
+                h0[j] = c < C16 ? tgi::ldg_stream(lo + (size_t)r0 * K + (size_t)c * 16) : make_uint4(0, 0, 0, 0);
+                h1[j] = (two && c < C16) ? tgi::ldg_stream(lo + (size_t)r1 * K + (size_t)c * 16)
+                                         : make_uint4(0, 0, 0, 0);
             }
+            int a0 = 0, a1 = 0;
+#pragma unroll
+            for (int j = 0; j < CPL; j++) {
+                a0 = dp4a_ss(h0[j].x, xr[j].x, a0);
+                a0 = dp4a_ss(h0[j].y, xr[j].y, a0);
+                a0 = dp4a_ss(h0[j].z, xr[j].z, a0);
+                a0 = dp4a_ss(h0[j].w, xr[j].w, a0);
+                a1 = dp4a_ss(h1[j].x, xr[j].x, a1);
+                a1 = dp4a_ss(h1[j].y, xr[j].y, a1);
+                a1 = dp4a_ss(h1[j].z, xr[j].z, a1);
+                a1 = dp4a_ss(h1[j].w, xr[j].w, a1);
+            }
+            const int t0 = tgi::warp_sum_i32(a0);
+            const int t1 = tgi::warp_sum_i32(a1);
+            const int64_t sc0 = __shfl_sync(0xffffffffu, sc, src0), s10 = __shfl_sync(0xffffffffu, s1, src0);
+            const int64_t sc1 = __shfl_sync(0xffffffffu, sc, src1), s11 = __shfl_sync(0xffffffffu, s1, src1);
+            // lane 0 appends the first row, lane 1 the second
+            const int64_t e0 = sc0 * (s10 + (int64_t)t0), e1 = sc1 * (s11 + (int64_t)t1);
+            const bool take = lane == 0 || (two && lane == 1);
+            const int64_t e = lane == 0 ? e0 : e1;
+            const int rr = lane == 0 ? r0 : r1;
+            append_key(ws, take, to_ordered(e * (low_mask + 1) + (low_mask - rr)), e);
         }
     }
 }
 
-// Full path, 3: append every row whose exact key reaches tau.
+// Full path, 2: append every row whose exact logit reaches the k-th bin's edge.
 __global__ void __launch_bounds__(256)
-lmh_collect_kernel(const int64_t *__restrict__ logits, Ws ws, int N, int idx_bits)
+lmh_collect_kernel(const int64_t *__restrict__ logits, Ws ws, int N, int k, int idx_bits)
 {
-    const int64_t tau = ws.ctl[0];
+    __shared__ int64_t sh_tau;
+    if (threadIdx.x < 32) {
+        const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
+        if (threadIdx.x == 0)
+            sh_tau = tau;
+    }
+    __syncthreads();
+    const int64_t tau = sh_tau;
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
     const int stride = gridDim.x * blockDim.x;
     for (int base = blockIdx.x * blockDim.x; base < N; base += stride) {
         const int r = base + threadIdx.x;
-        int64_t key = INT64_MIN;
-        if (r < N)
-            key = logits[r] * (low_mask + 1) + (low_mask - r);
-        append_key(ws, r < N && key >= tau, to_ordered(key));
+        const int64_t logit = r < N ? logits[r] : INT64_MIN;
+        append_key(ws, r < N && logit >= tau, to_ordered(logit * (low_mask + 1) + (low_mask - r)), logit);
     }
 }
 
-// 4. Top-k of the candidate keys: a running top-k kept at the front of a
-// shared-memory buffer, refilled behind it chunk by chunk and re-sorted.
+// k-th largest (1-based, counting duplicates) of n ordered keys, by radix
+// select from the most significant byte (fallback of the final selection).
+// Leading bytes shared by every key (from the block's min and max) are
+// skipped. Each warp counts into its own histogram (lanes that share a bin are
+// merged first); the 32 histograms are then summed. Called by all threads of
+// the block; `key(i)` reads key i. Returns 0 (below every real key) if n < k.
+struct RadixSmem {
+    unsigned hist[32][256];
+    unsigned total[256];
+    uint64_t red_min[32], red_max[32];
+    uint64_t bcast[2];
+};
+
+template <class KeyAt>
+__device__ uint64_t block_kth_largest(KeyAt key, int n, int k, RadixSmem &sm)
+{
+    if (n < k)
+        return 0ull;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+
+    uint64_t lo = ~0ull, hi = 0ull;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t u = key(i);
+        lo = u < lo ? u : lo;
+        hi = u > hi ? u : hi;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t a = __shfl_xor_sync(0xffffffffu, lo, o), b = __shfl_xor_sync(0xffffffffu, hi, o);
+        lo = a < lo ? a : lo;
+        hi = b > hi ? b : hi;
+    }
+    if (lane == 0) {
+        sm.red_min[warp] = lo;
+        sm.red_max[warp] = hi;
+    }
+    __syncthreads();
+    lo = sm.red_min[0];
+    hi = sm.red_max[0];
+    for (int w = 1; w < nwarps; w++) {
+        lo = sm.red_min[w] < lo ? sm.red_min[w] : lo;
+        hi = sm.red_max[w] > hi ? sm.red_max[w] : hi;
+    }
+    if (lo == hi)
+        return lo;
+    int shift = 56;
+    while (((lo ^ hi) >> shift) == 0)   // bytes above `shift` are common
+        shift -= 8;
+    uint64_t pmask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+    uint64_t prefix = lo & pmask;
+    int kk = k;
+
+    for (; shift >= 0; shift -= 8) {
+        for (int i = lane; i < 256; i += 32)
+            sm.hist[warp][i] = 0;
+        __syncwarp();
+        for (int base = 0; base < n; base += blockDim.x) {
+            const int i = base + threadIdx.x;
+            uint64_t u = 0;
+            bool take = false;
+            if (i < n) {
+                u = key(i);
+                take = (u & pmask) == prefix;
+            }
+            const unsigned active = __ballot_sync(0xffffffffu, take);
+            if (take) {
+                const unsigned bin = (unsigned)(u >> shift) & 255u;
+                const unsigned peers = __match_any_sync(active, bin);
+                if (lane == __ffs(peers) - 1)
+                    sm.hist[warp][bin] += (unsigned)__popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        if (threadIdx.x < 256) {
+            unsigned t = 0;
+            for (int w = 0; w < nwarps; w++)
+                t += sm.hist[w][threadIdx.x];
+            sm.total[threadIdx.x] = t;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned cnt[8], mine = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                cnt[j] = sm.total[255 - 8 * lane - j];
+                mine += cnt[j];
+            }
+            unsigned incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            const unsigned before = incl - mine;
+            if (before < (unsigned)kk && (unsigned)kk <= incl) {
+                unsigned cum = before;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    if (cum < (unsigned)kk && (unsigned)kk <= cum + cnt[j]) {
+                        sm.bcast[0] = (uint64_t)(255 - 8 * lane - j);
+                        sm.bcast[1] = (uint64_t)cum;
+                    }
+                    cum += cnt[j];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= sm.bcast[0] << shift;
+        pmask |= 0xFFull << shift;
+        kk -= (int)sm.bcast[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// 3. Top-k of the candidate keys. The candidates whose exact score reaches
+// the k-th candidate bin's edge (about k of them, and every one of the top k)
+// are gathered and each is written at its rank among them. If a dense bin
+// makes that set too large, the k-th largest key is found by radix select and
+// the k keys at or above it are ranked instead.
 __global__ void __launch_bounds__(kSelThreads)
 lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32_t *__restrict__ ids,
                  int64_t *__restrict__ scores, int32_t *__restrict__ ncand)
 {
-    extern __shared__ __align__(16) uint64_t sv[];
-    const long long n = ws.ctl[1];
-    int cap = (int)(n < kSortMax ? n : kSortMax);
-    if (cap < 2 * k)
-        cap = 2 * k;
-    const int P = next_pow2(cap);
-    for (int i = threadIdx.x; i < P; i += blockDim.x)
-        sv[i] = i < n ? ws.cand[i] : 0ull;
-    block_sort_desc(sv, P);
-    for (long long off = P; off < n; off += P - k) {
-        for (int i = k + threadIdx.x; i < P; i += blockDim.x) {
-            const long long src = off + (i - k);
-            sv[i] = src < n ? ws.cand[src] : 0ull;
-        }
-        block_sort_desc(sv, P);
-    }
+    extern __shared__ __align__(16) unsigned char dyn[];
+    uint64_t *sel = reinterpret_cast<uint64_t *>(dyn);                                 // [kFilterMax]
+    RadixSmem &rs = *reinterpret_cast<RadixSmem *>(dyn + kFilterMax * sizeof(uint64_t));
+    __shared__ int64_t sh_tau;
+    __shared__ int nsel;
+    const int n = (int)*ws.count;
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
-    for (int j = threadIdx.x; j < k; j += blockDim.x) {
-        if (j < n) {
-            const int64_t key = from_ordered(sv[j]);
-            ids[j] = (int32_t)(low_mask - (key & low_mask));
-            scores[j] = key >> idx_bits;
-        } else {
-            ids[j] = -1;
-            scores[j] = INT64_MIN;
+    if (threadIdx.x < 32) {
+        const int64_t tau = warp_kth_bin_edge(ws.hist_cand, k);
+        if (threadIdx.x == 0) {
+            sh_tau = tau;
+            nsel = 0;
         }
+    }
+    __syncthreads();
+    const int64_t tau = sh_tau;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t u = ws.cand[i];
+        if ((from_ordered(u) >> idx_bits) >= tau) {
+            const int slot = atomicAdd(&nsel, 1);
+            if (slot < kFilterMax)
+                sel[slot] = u;
+        }
+    }
+    __syncthreads();
+    int m = nsel;
+    if (m > kFilterMax) {
+        // dense bin: radix select over every candidate, keep the k at or above
+        const uint64_t t = block_kth_largest([&](int i) { return ws.cand[i]; }, n, k, rs);
+        if (threadIdx.x == 0)
+            nsel = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint64_t u = ws.cand[i];
+            if (u >= t) {
+                const int slot = atomicAdd(&nsel, 1);
+                if (slot < kFilterMax)
+                    sel[slot] = u;
+            }
+        }
+        __syncthreads();
+        m = nsel < kFilterMax ? nsel : kFilterMax;
+    }
+    const int kout = m < k ? m : k;
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        const uint64_t u = sel[i];
+        int rank = 0;
+        for (int j = 0; j < m; j++)
+            rank += sel[j] > u;
+        if (rank < kout) {
+            const int64_t key = from_ordered(u);
+            ids[rank] = (int32_t)(low_mask - (key & low_mask));
+            scores[rank] = key >> idx_bits;
+            if (rank == 0)
+                argmax[0] = (int32_t)(low_mask - (key & low_mask));
+        }
+    }
+    for (int i = kout + threadIdx.x; i < k; i += blockDim.x) {
+        ids[i] = -1;
+        scores[i] = INT64_MIN;
     }
     if (threadIdx.x == 0) {
-        argmax[0] = n > 0 ? (int32_t)(low_mask - (from_ordered(sv[0]) & low_mask)) : -1;
+        if (kout == 0)
+            argmax[0] = -1;
         if (ncand)
-            ncand[0] = (int32_t)n;
+            ncand[0] = n;
     }
 }
 
@@ -334,33 +597,31 @@ Ws carve(void *ws, int64_t N)
 {
     auto *p = static_cast<unsigned char *>(ws);
     Ws w;
-    size_t off = 0;
+    w.count = reinterpret_cast<unsigned long long *>(p);
+    w.hist_row = reinterpret_cast<unsigned *>(p + 256);
+    w.hist_cand = w.hist_row + kHistBins;
+    size_t off = kClearedBytes;
     w.s1 = reinterpret_cast<int64_t *>(p + off);
     off += align256((size_t)N * 8);
-    w.best = reinterpret_cast<int64_t *>(p + off);
-    off += align256((size_t)tgi::kLmhMaxWarps * 8);
-    w.ctl = reinterpret_cast<int64_t *>(p + off);
-    off += 256;
     w.cand = reinterpret_cast<uint64_t *>(p + off);
     return w;
 }
 
 template <int CPL>
 void launch_scan(bool full, int grid, cudaStream_t st, const int8_t *hi, const int8_t *lo,
-                 const int32_t *s, const uint8_t *m, const int8_t *x, int64_t *logits, Ws ws, int N,
-                 int K, int idx_bits)
+                 const int32_t *s, const uint8_t *m, const int8_t *x, int64_t *logits, Ws ws, int N, int K)
 {
     if (full)
-        lmh_full_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(hi, lo, s, x, logits, ws, N, K, idx_bits);
+        lmh_full_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(hi, lo, s, x, logits, ws, N, K);
     else
         lmh_stage1_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(hi, s, m, x, ws, N, K);
 }
 
 template <int CPL>
 void launch_rescore(int grid, cudaStream_t st, const int8_t *lo, const int32_t *s, const uint8_t *m,
-                    const int8_t *x, Ws ws, int N, int K, int idx_bits)
+                    const int8_t *x, Ws ws, int N, int K, int k, int idx_bits)
 {
-    lmh_rescore_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(lo, s, m, x, ws, N, K, idx_bits);
+    lmh_rescore_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(lo, s, m, x, ws, N, K, k, idx_bits);
 }
 
 }  // namespace
@@ -369,8 +630,7 @@ extern "C" size_t tg_lmhead_workspace_bytes(const tg_layout *L, int32_t k)
 {
     if (!L || L->kind != TG_PLANES8 || L->N < 1 || k < 1)
         return 0;
-    return align256((size_t)L->N * 8) + align256((size_t)tgi::kLmhMaxWarps * 8) + 256 +
-           align256((size_t)L->N * 8);
+    return kClearedBytes + align256((size_t)L->N * 8) + align256((size_t)L->N * 8);
 }
 
 extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const int8_t *x, int32_t k,
@@ -415,55 +675,51 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return TG_ERR_CUDA;
     int grid = nsm * 4;
-    const int max_grid = tgi::kLmhMaxWarps / kScanWarps;
-    if (grid > max_grid)
-        grid = max_grid;
     const int need = (int)((N + kScanWarps - 1) / kScanWarps);
     if (grid > need)
         grid = need;
-    const int nw = grid * kScanWarps;
     const bool full = logits != nullptr;
     const int n = (int)N, kk = (int)K;
 
+    // the candidate count and both histograms start at zero every call
+    if (cudaMemsetAsync(ws, 0, kClearedBytes, st) != cudaSuccess)
+        return TG_ERR_CUDA;
+
 #define TGI_CPL_CASE(C)                                                                            \
     case C:                                                                                        \
-        launch_scan<C>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk, idx_bits);             \
+        launch_scan<C>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);                       \
         break;
     switch (cpl) {
         TGI_CPL_CASE(1) TGI_CPL_CASE(2) TGI_CPL_CASE(3) TGI_CPL_CASE(4) TGI_CPL_CASE(5)
         TGI_CPL_CASE(6) TGI_CPL_CASE(7) TGI_CPL_CASE(8)
     default:
-        launch_scan<16>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk, idx_bits);
+        launch_scan<16>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);
         break;
     }
 #undef TGI_CPL_CASE
 
-    const size_t sel_smem = (size_t)kSortMax * sizeof(uint64_t);
-    if (cudaFuncSetAttribute(lmh_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sel_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(lmh_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sel_smem) != cudaSuccess)
-        return TG_ERR_CUDA;
-    lmh_threshold_kernel<<<1, kSelThreads, sel_smem, st>>>(wsp, nw, k);
-
     if (full) {
-        const int cgrid = (int)((N + 255) / 256 < nsm * 8 ? (N + 255) / 256 : nsm * 8);
-        lmh_collect_kernel<<<cgrid, 256, 0, st>>>(logits, wsp, n, idx_bits);
+        const int cgrid = (int)((N + 255) / 256 < nsm * 4 ? (N + 255) / 256 : nsm * 4);
+        lmh_collect_kernel<<<cgrid, 256, 0, st>>>(logits, wsp, n, k, idx_bits);
     } else {
 #define TGI_CPL_CASE(C)                                                                            \
     case C:                                                                                        \
-        launch_rescore<C>(grid, st, lo, s, m, x, wsp, n, kk, idx_bits);                            \
+        launch_rescore<C>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);                         \
         break;
         switch (cpl) {
             TGI_CPL_CASE(1) TGI_CPL_CASE(2) TGI_CPL_CASE(3) TGI_CPL_CASE(4) TGI_CPL_CASE(5)
             TGI_CPL_CASE(6) TGI_CPL_CASE(7) TGI_CPL_CASE(8)
         default:
-            launch_rescore<16>(grid, st, lo, s, m, x, wsp, n, kk, idx_bits);
+            launch_rescore<16>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);
             break;
         }
 #undef TGI_CPL_CASE
     }
-    lmh_final_kernel<<<1, kSelThreads, sel_smem, st>>>(wsp, k, idx_bits, argmax, ids, scores, ncand);
+    const size_t final_smem = kFilterMax * sizeof(uint64_t) + sizeof(RadixSmem);
+    if (cudaFuncSetAttribute(lmh_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)final_smem) != cudaSuccess)
+        return TG_ERR_CUDA;
+    lmh_final_kernel<<<1, kSelThreads, final_smem, st>>>(wsp, k, idx_bits, argmax, ids, scores, ncand);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

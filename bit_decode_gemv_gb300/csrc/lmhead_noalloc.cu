@@ -12,9 +12,9 @@
 // array until the process exits.
 //
 // The array is shared by every call in the process on a given device and keeps
-// the last call's contents. The lm_head kernels write everything they read in
-// the workspace before reading it (the candidate count is reset by the
-// threshold kernel), so nothing has to be cleared between calls. Two calls
+// the last call's contents. Each lm_head call clears the counters and
+// histograms it relies on at its start and writes everything else it reads
+// before reading it, so nothing has to be cleared between calls. Two calls
 // whose work overlaps on the GPU (different streams, or different host threads
 // without ordering) use the same memory and race: the caller must order them.
 

@@ -10,9 +10,6 @@ namespace tgi {
 
 constexpr int kTileRows = 32;   // rows per mask tile: one row per lane of a warp
 
-// Largest number of warps the lm_head scan kernels launch; sizes the workspace.
-constexpr int kLmhMaxWarps = 8192;
-
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Per translation unit: read-and-clear of that unit's device error word.

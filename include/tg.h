@@ -110,8 +110,20 @@ typedef struct tg_layout {
     int64_t aux2_off, aux2_bytes;
     int64_t total_bytes;
     int64_t max_abs_scale;  /* max |scale| seen when packing (0 from tg_layout_init) */
-    int64_t reserved[4];
+    int64_t flags;          /* TG_FLAG_* bits, 0 after packing; the caller may set them */
+    int64_t reserved[3];
 } tg_layout;
+
+/*
+ * Layout flag: the packed weights are constant -- no device work on the stream
+ * of an apply call writes them. A batch-1 tg_gemv_i8 call on such weights is
+ * launched as a programmatic dependent of the previous kernel on the stream: it
+ * may start streaming its weights while that kernel is still running, and it
+ * waits for that kernel to finish (and its writes to be visible) before it
+ * reads x or writes y. Without the flag every call starts after the previous
+ * work on the stream has finished.
+ */
+#define TG_FLAG_CONST_WEIGHTS 1
 
 /* Static string naming a status code. Never NULL. */
 const char *tg_status_string(int status);
@@ -224,7 +236,7 @@ int tg_lmhead_argmax_topk(const tg_layout *layout, const void *w, const int8_t *
  *     that device current and caches it; make that first call before any stream
  *     capture. A failed lookup returns TG_ERR_CUDA.
  *   - Every call on a device shares the one array, which keeps the last call's
- *     contents (nothing needs to be cleared: the kernels write what they read).
+ *     contents (nothing needs to be cleared: each call resets what it counts).
  *     Calls whose work overlaps on the GPU race on it; the caller must order
  *     them (one stream, or explicit events).
  */
