@@ -7,14 +7,35 @@
 //     A[r][k & 7] += (s_a XOR [t < 0]) ? -(1 << (k >> 3)) : (1 << (k >> 3))
 //   S[r] = 2^-9 * sum_{p=0..7} A[r][p] * F[p],  F[p] = 2^((p - 2) / 8)
 //
-// Mapping: one CTA per tile of 32 rows, lane l of each warp owns row 32T + l,
-// the warps split the groups. Each thread keeps its eight phase accumulators
-// in its own shared-memory column (the phase index is data dependent, and a
-// register array indexed at run time would live in local memory). The
-// per-thread partials fit int32 (|A| <= K * 2^15 < 2^31 for K < 65536) and are
-// summed into int64 at the end. S is materialised in the same kernel with
+// Factorisation. Write the group's offset e = d - 74 = 8*beta + delta with
+// delta = e & 7, and an activation code a = 8c + q. A lane then lands in phase
+// (q + delta) & 7 with band c + beta + [q + delta >= 8]: the phase depends on
+// the activation only through q, and the row only through delta and beta. So
+// per (row, group) it is enough to form
+//   G[q] = sum over lanes with a & 7 == q of  t * s_a * 2^c
+// and add G[q] * 2^(beta + [q + delta >= 8]) into A[(q + delta) & 7]. This is
+// exact when no lane of that (row, group) is clamped (k in 1..127 for every
+// nonzero lane), which is checked per (row, group) from the group's smallest
+// and largest nonzero activation code; the rare (row, group) that can clamp
+// takes the per-lane route instead.
+//
+// G is a contraction t (rows x lanes) . V (lanes x 8) with V[i][q] = s_i 2^c_i
+// when a_i & 7 == q, else 0. Every entry (+-1, +-2^c) is exact in bf16 and
+// every partial sum is an integer below 2^23, so a bf16 tensor-core product
+// with fp32 accumulation is exact. A 16x8x16 warp-level MMA takes 16 rows x 16
+// lanes of t from registers (converted straight from the packed mask pair, two
+// integer ops per weight) against the 16 x 8 slice of V, N = 8 = the phases.
+// The tensor core here routes rather than multiplies: the work is the trit
+// conversion, and the warp-level MMA, fed from registers, avoids staging the
+// expanded weights anywhere.
+//
+// Mapping: a CTA owns 128 rows (warp w: rows 16w..16w+15) and a slice of the
+// groups; a cluster of up to 8 CTAs covers all groups of those rows. Each CTA
+// keeps int32 phase partials in shared memory; the cluster's first CTA sums
+// them through distributed shared memory into int64 A and materialises S with
 // explicitly rounded fp64 multiplies and adds in the order p = 0..7.
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,79 +49,198 @@ TGI_DEFINE_DEVICE_ERROR(lns8_take_device_error)
 
 namespace {
 
-using tgi::kTileRows;
+namespace cg = cooperative_groups;
+
+constexpr int kWarps = 8;                  // warps per CTA; warp w owns one 16-row block
+constexpr int kRows = kWarps * 16;         // rows per CTA
+constexpr int kChunkGroups = 4;            // groups per step: V fragments staged, weights in flight
+constexpr int kMaxCluster = 8;
 
 struct PhaseF {
     double f[8];
 };
 
-template <int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-lns8_phase_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
-                  const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
-                  PhaseF F, int N, int G)
+// bf16 bit pattern of (-1)^sign * 2^c.
+__device__ __forceinline__ uint32_t bf16_pow2(uint32_t sign, uint32_t c) { return (sign << 15) | ((127u + c) << 7); }
+
+// bf16x2 A register from pair rp of a packed word: W_nonzero bits at 7-rp and
+// 23-rp become the bf16 one (0x3F80) of each half, W_negative bits at 15-rp and
+// 31-rp its sign.
+template <int RP>
+__device__ __forceinline__ uint32_t frag_pair(uint32_t w)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint8_t *xs = smem;                                                  // [G*128]
-    int *acc = reinterpret_cast<int *>(smem + G * 128);                  // [8][WARPS*32]
-    constexpr int BD = WARPS * 32;
+    return ((w & (0x00800080u >> RP)) * (0x7Fu << RP)) | ((w << RP) & 0x80008000u);
+}
 
-    const int tile = blockIdx.x;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int tid = threadIdx.x;
-    const uint4 *tmask = masks + (size_t)tile * G * 64;
-    const uint8_t *tcode = codes + (size_t)tile * G * kTileRows;
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-    const int K = G * 128;
-    for (int i = tid; i < K / 16; i += BD)
-        reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(xa) + i);
-#pragma unroll
-    for (int p = 0; p < 8; p++)
-        acc[p * BD + tid] = 0;
-    __syncthreads();
+// One V value: (a != 0 and a & 7 == q) ? bf16(+-2^(a >> 3)) : 0.
+__device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
+{
+    const uint32_t a = xab & 0x7fu;
+    return (a != 0u && (a & 7u) == q) ? bf16_pow2(xab >> 7, a >> 3) : 0u;
+}
 
-    for (int g = warp; g < G; g += WARPS) {
-        const uint4 q0 = tgi::ldg_stream(tmask + g * 64 + lane);
-        const uint4 q1 = tgi::ldg_stream(tmask + g * 64 + 32 + lane);
-        const int e = (int)__ldg(tcode + g * kTileRows + lane) - 74;
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const uint8_t *xg = xs + g * 128;
+// Per-lane route for one (row, group) of this thread's 32 lanes (the exact
+// definition; used where the factorised form could meet a clamp).
+__device__ void route_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg,
+                            int *acc_row)
+{
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xg + 16 * u);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    for (int kc = 0; kc < 8; kc++) {
+        const uint32_t w = w4[kc >> 1];
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
+        for (int rr = 0; rr < 2; rr++) {
+            const int r = half + 2 * rr;                     // pairs of this row: half, half + 2
+            const int rp = 4 * (kc & 1) + r;
+            const int col = 16 * kc + 2 * tq + (rr ? 8 : 0);
 #pragma unroll
-                for (int b = 0; b < 4; b++) {
-                    // lane 16u + 4j + b of the group
-                    const uint32_t f = (w[u] >> (8 * b + 2 * j)) & 3u;
-                    const uint32_t av = (xw[j] >> (8 * b)) & 0xffu;
-                    const int a = (int)(av & 0x7fu);
-                    int k = a + e;
-                    if (f != 0u && a != 0 && k > 0) {
-                        k = min(k, 127);
-                        const int mag = 1 << (k >> 3);
-                        const bool neg = ((av >> 7) ^ (f >> 1)) & 1u;
-                        acc[(k & 7) * BD + tid] += neg ? -mag : mag;
-                    }
+            for (int h = 0; h < 2; h++) {
+                const uint32_t nz = (w >> (16 * h + 7 - rp)) & 1u;
+                const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
+                const uint32_t xab = xg[col + h];
+                const int a = (int)(xab & 0x7fu);
+                int k = a + e;
+                if (nz && a != 0 && k > 0) {
+                    k = min(k, 127);
+                    const int mag = 1 << (k >> 3);
+                    atomicAdd(acc_row + (k & 7), ((xab >> 7) ^ neg) ? -mag : mag);
                 }
             }
         }
     }
-    __syncthreads();
+}
 
-    if (warp == 0) {
-        const int row = tile * kTileRows + lane;
-        int64_t a8[8];
+__global__ void __launch_bounds__(kWarps * 32)
+lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
+                const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
+                PhaseF F, int N, int G, int gpc)
+{
+    __shared__ uint2 vfrag[kChunkGroups][8][32];   // V fragments (b0, b1) per group, chunk, lane
+    __shared__ unsigned gmin[kChunkGroups], gmax[kChunkGroups];
+    __shared__ int acc[kRows][8];                  // int32 phase partials of this CTA's groups
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int csize = (int)cluster.num_blocks();
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int rb = blockIdx.x * kWarps + warp;       // 16-row block of this warp
+    const int g_begin = rank * gpc;
+    const int g_end = min(G, g_begin + gpc);
+
+    for (int i = tid; i < kRows * 8; i += blockDim.x)
+        (&acc[0][0])[i] = 0;
+
+    const bool active = rb * 16 < N;   // warp-uniform
+    for (int c0 = g_begin; c0 < g_end; c0 += kChunkGroups) {
+        const int ng = min(kChunkGroups, g_end - c0);
+        // this warp's masks and scale codes for the chunk, issued before the
+        // shared-memory set-up so the weight stream overlaps it
+        uint4 wv[kChunkGroups];
+        int ec[kChunkGroups][2];
 #pragma unroll
-        for (int p = 0; p < 8; p++) {
-            int64_t s = 0;
+        for (int gl = 0; gl < kChunkGroups; gl++) {
+            wv[gl] = make_uint4(0, 0, 0, 0);
+            ec[gl][0] = ec[gl][1] = 0;
+            if (active && gl < ng) {
+                const size_t unit = (size_t)rb * G + c0 + gl;
+                wv[gl] = tgi::ldg_stream(masks + unit * 32 + lane);
+                ec[gl][0] = (int)__ldg(codes + unit * 16 + gq) - 74;
+                ec[gl][1] = (int)__ldg(codes + unit * 16 + gq + 8) - 74;
+            }
+        }
+        __syncthreads();
+        // V fragments: thread (q, j) of chunk kc holds V rows 2j, 2j+1 (b0) and
+        // 2j+8, 2j+9 (b1) of column q
+        for (int idx = tid; idx < ng * 256; idx += blockDim.x) {
+            const int gl = idx >> 8, kc = (idx >> 5) & 7, ln = idx & 31;
+            const uint32_t q = (uint32_t)(ln >> 2);
+            const uint8_t *xg = xa + (size_t)(c0 + gl) * TG_GROUP + 16 * kc + 2 * (ln & 3);
+            const uint32_t b0 = v_entry(xg[0], q) | (v_entry(xg[1], q) << 16);
+            const uint32_t b1 = v_entry(xg[8], q) | (v_entry(xg[9], q) << 16);
+            vfrag[gl][kc][ln] = make_uint2(b0, b1);
+        }
+        // smallest and largest nonzero activation code of each group
+        for (int gl = warp; gl < ng; gl += kWarps) {
+            const uint32_t v4 = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)(c0 + gl) * TG_GROUP) + lane);
+            unsigned lo = 128u, hi = 0u;
 #pragma unroll
-            for (int w = 0; w < WARPS; w++)
-                s += acc[p * BD + w * 32 + lane];
-            a8[p] = s;
+            for (int b = 0; b < 4; b++) {
+                const unsigned a = (v4 >> (8 * b)) & 0x7fu;
+                if (a) {
+                    lo = min(lo, a);
+                    hi = max(hi, a);
+                }
+            }
+            lo = __reduce_min_sync(0xffffffffu, lo);
+            hi = __reduce_max_sync(0xffffffffu, hi);
+            if (lane == 0) {
+                gmin[gl] = lo;
+                gmax[gl] = hi;
+            }
+        }
+        __syncthreads();
+
+        if (active) {
+#pragma unroll
+            for (int gl = 0; gl < kChunkGroups; gl++) {
+                if (gl >= ng)
+                    break;
+                const int grp = c0 + gl;
+                const uint32_t w4[4] = {wv[gl].x, wv[gl].y, wv[gl].z, wv[gl].w};
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kc = 0; kc < 8; kc++) {
+                    const uint32_t w = w4[kc >> 1];
+                    const uint2 b = vfrag[gl][kc][lane];
+                    if (kc & 1)
+                        mma_bf16_16816(d, frag_pair<4>(w), frag_pair<5>(w), frag_pair<6>(w), frag_pair<7>(w), b.x, b.y);
+                    else
+                        mma_bf16_16816(d, frag_pair<0>(w), frag_pair<1>(w), frag_pair<2>(w), frag_pair<3>(w), b.x, b.y);
+                }
+                const int lo = (int)gmin[gl], hi = (int)gmax[gl];
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    const int e = ec[gl][half];
+                    int *acc_row = acc[warp * 16 + gq + 8 * half];
+                    const bool clamp_free = lo > 127 || (lo + e >= 1 && hi + e <= 127);
+                    if (clamp_free) {
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            const int q = 2 * tq + j;
+                            const int v = __float2int_rn(d[2 * half + j]);
+                            const int sidx = q + (e & 7);
+                            const int sh = (e >> 3) + (sidx >> 3);
+                            acc_row[sidx & 7] += sh >= 0 ? (v << sh) : (v >> -sh);
+                        }
+                    } else {
+                        route_lanes(w4, half, tq, e, xa + (size_t)grp * TG_GROUP, acc_row);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+    __syncthreads();
+    cluster.sync();
+    if (rank == 0 && tid < kRows) {
+        const int row = blockIdx.x * kRows + tid;
+        int64_t a8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int r = 0; r < csize; r++) {
+            const int *remote = cluster.map_shared_rank(&acc[0][0], r);
+#pragma unroll
+            for (int p = 0; p < 8; p++)
+                a8[p] += remote[tid * 8 + p];
         }
         if (row < N) {
 #pragma unroll
@@ -115,9 +255,8 @@ lns8_phase_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ c
             }
         }
     }
+    cluster.sync();
 }
-
-constexpr int kWarps = 4;
 
 }  // namespace
 
@@ -133,7 +272,7 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
         return TG_ERR_ARG;
     if (L->N < 1 || L->K < TG_GROUP || L->K % TG_GROUP)
         return TG_ERR_SHAPE;
-    if (L->K >= 65536)   // per-thread int32 phase partials: K * 2^15 < 2^31
+    if (L->K >= 65536)   // int32 phase partials per CTA: |sum| <= K * 2^15 < 2^31
         return TG_ERR_BOUND;
 
     PhaseF F;
@@ -144,16 +283,23 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
     const uint4 *masks = reinterpret_cast<const uint4 *>(base + L->mask_off);
     const uint8_t *codes = base + L->scale_off;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = (int)L->G;
-    const size_t smem = (size_t)G * 128 + 8 * kWarps * 32 * sizeof(int);
-    auto kern = lns8_phase_kernel<kWarps>;
-    if (smem > 48 * 1024) {
-        if (smem > 200 * 1024)
-            return TG_ERR_SHAPE;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return TG_ERR_CUDA;
-    }
-    kern<<<(int)L->tiles, kWarps * 32, smem, s>>>(masks, codes, xa, A, S, F, (int)L->N, G);
+    const int G = (int)L->G, N = (int)L->N;
+    const int gpc = (G + kMaxCluster - 1) / kMaxCluster;   // groups per CTA
+    const int csize = (G + gpc - 1) / gpc;                 // CTAs per cluster, <= 8
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((N + kRows - 1) / kRows), (unsigned)csize);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)csize;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, lns8_mma_kernel, masks, codes, xa, A, S, F, N, G, gpc) != cudaSuccess)
+        return TG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

@@ -100,12 +100,20 @@ extern "C" int tg_layout_init(int kind, int64_t N, int64_t K, tg_layout *out)
         L.aux2_off = align_up(L.scale_off + L.scale_bytes);
         L.aux2_bytes = N;
         L.total_bytes = align_up(L.aux2_off + L.aux2_bytes);
-    } else {
+    } else if (kind == TG_TERNARY_I8) {
         L.tiles = (N + tgi::kTileRows - 1) / tgi::kTileRows;
         L.mask_off = 0;
         L.mask_bytes = L.tiles * L.G * tgi::kTileRows * 32;
         L.scale_off = align_up(L.mask_bytes);
-        L.scale_bytes = L.tiles * L.G * tgi::kTileRows * (kind == TG_TERNARY_I8 ? 4 : 1);
+        L.scale_bytes = L.tiles * L.G * tgi::kTileRows * 4;
+        L.total_bytes = align_up(L.scale_off + L.scale_bytes);
+    } else {
+        // LNS8: blocks of 16 rows, the masks in tensor-core fragment order
+        L.tiles = (N + tgi::kLnsBlockRows - 1) / tgi::kLnsBlockRows;
+        L.mask_off = 0;
+        L.mask_bytes = L.tiles * L.G * 32 * 16;
+        L.scale_off = align_up(L.mask_bytes);
+        L.scale_bytes = L.tiles * L.G * tgi::kLnsBlockRows;
         L.total_bytes = align_up(L.scale_off + L.scale_bytes);
     }
     *out = L;
@@ -164,6 +172,54 @@ bool pack_masks(const tg_layout &L, const int8_t *t, uint8_t *out)
     return true;
 }
 
+// Pack ternary rows [N][K] into the LNS8 fragment layout (tg.h); false on a bad trit.
+// Lane l = 4g + t of a warp holds, for each 16-lane chunk c of a group, the
+// eight trits of one 16 x 16 A fragment: rows g and g+8 of the 16-row block at
+// group lanes 16c + {2t, 2t+1, 2t+8, 2t+9}. Register r of chunk c (r' = 4(c%2)
+// + r in word c/2) takes its low trit's W_nonzero / W_negative bits at 7 - r'
+// and 15 - r', its high trit's at 23 - r' and 31 - r'.
+bool pack_lns8_fragments(const tg_layout &L, const int8_t *t, uint8_t *out)
+{
+    const int64_t N = L.N, K = L.K, G = L.G;
+    std::vector<char> bad((size_t)L.tiles, 0);
+    parallel_rows(L.tiles, [&](int64_t b0, int64_t b1) {
+        for (int64_t B = b0; B < b1; B++) {
+            for (int64_t g = 0; g < G; g++) {
+                for (int lane = 0; lane < 32; lane++) {
+                    const int gq = lane >> 2, tq = lane & 3;
+                    uint32_t words[4] = {0, 0, 0, 0};
+                    for (int c = 0; c < 8; c++) {
+                        for (int r = 0; r < 4; r++) {
+                            const int row = gq + ((r & 1) ? 8 : 0);
+                            const int col = 16 * c + 2 * tq + ((r & 2) ? 8 : 0);
+                            const int rp = 4 * (c & 1) + r;
+                            const int64_t grow = B * tgi::kLnsBlockRows + row;
+                            for (int h = 0; h < 2; h++) {
+                                int8_t v = 0;
+                                if (grow < N) {
+                                    v = t[grow * K + g * TG_GROUP + col + h];
+                                    if (v < -1 || v > 1)
+                                        bad[(size_t)B] = 1;
+                                }
+                                const uint32_t nz = v != 0, neg = v < 0;
+                                words[c >> 1] |= nz << (16 * h + 7 - rp);
+                                words[c >> 1] |= neg << (16 * h + 15 - rp);
+                            }
+                        }
+                    }
+                    uint8_t *dst = out + L.mask_off + ((B * G + g) * 32 + lane) * 16;
+                    for (int u = 0; u < 4; u++)
+                        store_u32(dst + 4 * u, words[u]);
+                }
+            }
+        }
+    });
+    for (char b : bad)
+        if (b)
+            return false;
+    return true;
+}
+
 }  // namespace
 
 extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *trits,
@@ -180,7 +236,7 @@ extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *tri
     uint8_t *out = static_cast<uint8_t *>(out_v);
     std::memset(out, 0, (size_t)L.total_bytes);
 
-    if (kind == TG_TERNARY_I8 || kind == TG_TERNARY_LNS8) {
+    if (kind == TG_TERNARY_I8) {
         if (!pack_masks(L, trits, out))
             return TG_ERR_VALUE;
         const int64_t G = L.G;
@@ -190,20 +246,30 @@ extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *tri
                 for (int l = 0; l < tgi::kTileRows; l++) {
                     const int64_t r = T * tgi::kTileRows + l;
                     const int64_t slot = (T * G + g) * tgi::kTileRows + l;
-                    if (kind == TG_TERNARY_I8) {
-                        int32_t d = r < N ? static_cast<const int32_t *>(scales)[r * G + g] : 0;
-                        int64_t a = d < 0 ? -(int64_t)d : (int64_t)d;
-                        maxabs = std::max(maxabs, a);
-                        store_u32(out + L.scale_off + slot * 4, (uint32_t)d);
-                    } else {
-                        uint8_t c = r < N ? static_cast<const uint8_t *>(scales)[r * G + g] : 0;
-                        maxabs = std::max<int64_t>(maxabs, c);
-                        out[L.scale_off + slot] = c;
-                    }
+                    int32_t d = r < N ? static_cast<const int32_t *>(scales)[r * G + g] : 0;
+                    int64_t a = d < 0 ? -(int64_t)d : (int64_t)d;
+                    maxabs = std::max(maxabs, a);
+                    store_u32(out + L.scale_off + slot * 4, (uint32_t)d);
                 }
             }
         }
         L.max_abs_scale = maxabs;
+    } else if (kind == TG_TERNARY_LNS8) {
+        if (!pack_lns8_fragments(L, trits, out))
+            return TG_ERR_VALUE;
+        const int64_t G = L.G;
+        int64_t maxc = 0;
+        for (int64_t B = 0; B < L.tiles; B++) {
+            for (int64_t g = 0; g < G; g++) {
+                for (int l = 0; l < tgi::kLnsBlockRows; l++) {
+                    const int64_t r = B * tgi::kLnsBlockRows + l;
+                    const uint8_t c = r < N ? static_cast<const uint8_t *>(scales)[r * G + g] : 0;
+                    maxc = std::max<int64_t>(maxc, c);
+                    out[L.scale_off + (B * G + g) * tgi::kLnsBlockRows + l] = c;
+                }
+            }
+        }
+        L.max_abs_scale = maxc;
     } else {
         // TG_PLANES8: two balanced base-3 digit groups per weight, W = 81*hi + lo.
         const int32_t *s = static_cast<const int32_t *>(scales);

@@ -9,6 +9,7 @@
 namespace tgi {
 
 constexpr int kTileRows = 32;   // rows per mask tile: one row per lane of a warp
+constexpr int kLnsBlockRows = 16;  // rows per LNS8 block: the M of one 16x8x16 tensor-core step
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

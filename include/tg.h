@@ -81,14 +81,25 @@ enum {
  * byte offsets from the start of the blob; every region starts on a 256-byte
  * boundary. The blob's device copy must be 256-byte aligned.
  *
- * TG_TERNARY_I8 and TG_TERNARY_LNS8 (rows tiled by 32, tiles = ceil(N/32)):
+ * TG_TERNARY_I8 (rows tiled by 32, tiles = ceil(N/32)):
  *   masks  [tiles][G][2][32][16 B]: for tile T, group g, half h (group lanes
  *          64h..64h+63) and row r = 32T + l, 16 bytes = four little-endian
  *          uint32 words; word u holds group lanes 64h + 16u + (0..15), lane
  *          64h + 16u + 4j + b in bits 8b+2j (W_nonzero) and 8b+2j+1
  *          (W_negative). W_negative is set only where W_nonzero is.
- *   scales [tiles][G][32]: int32 (I8) or uint8 code (LNS8) of row 32T + l.
+ *   scales [tiles][G][32]: int32 scale of row 32T + l.
  *   Rows N..32*tiles-1 are padding: zero masks, zero scales.
+ * TG_TERNARY_LNS8 (rows in blocks of 16, tiles = ceil(N/16)): the same mask
+ * pair, ordered for 16x8x16 tensor-core steps:
+ *   masks  [tiles][G][32][16 B]: entry l = 4q + j (q = 0..7, j = 0..3) holds,
+ *          for each 16-lane chunk c = 0..7 of group g, the trits of rows q and
+ *          q+8 of the block at group lanes 16c + {2j, 2j+1, 2j+8, 2j+9}: four
+ *          pairs r = 0..3 = (row q; 2j, 2j+1), (row q+8; 2j, 2j+1),
+ *          (row q; 2j+8, 2j+9), (row q+8; 2j+8, 2j+9). Pair r of chunk c sits in
+ *          word c/2 with r' = 4(c%2) + r: the first trit's W_nonzero /
+ *          W_negative bits at 7-r' and 15-r', the second's at 23-r' and 31-r'.
+ *   scales [tiles][G][16]: uint8 LNS8 code of row 16*tile + i.
+ *   Rows N..16*tiles-1 are padding: zero masks, zero codes.
  * TG_PLANES8:
  *   masks  [N][K] int8, planes 0-3 as one balanced base-3 number per weight,
  *          hi = 27 t0 + 9 t1 + 3 t2 + t3 in [-40, 40];
@@ -103,7 +114,7 @@ typedef struct tg_layout {
     int32_t version;        /* 1 */
     int64_t N, K;           /* rows, columns (K % 128 == 0) */
     int64_t G;              /* groups per row, K / 128 */
-    int64_t tiles;          /* ceil(N / 32) for the masked kinds, else 0 */
+    int64_t tiles;          /* ceil(N/32) (I8), ceil(N/16) (LNS8), else 0 */
     int64_t mask_off, mask_bytes;
     int64_t scale_off, scale_bytes;
     int64_t aux_off, aux_bytes;

@@ -102,12 +102,38 @@ def test_pack_i8_layout(N, K):
     assert not t[N:].any() and not s[N:].any()          # padding rows are zero
 
 
+def decode_lns8(blob, L):
+    """Independent reader of the LNS8 fragment layout -> (t [16*tiles][K], codes)."""
+    G, T, K = L.G, L.tiles, L.K
+    words = blob[L.mask_off:L.mask_off + L.mask_bytes].view("<u4").reshape(T, G, 32, 4)
+    t = np.zeros((T * 16, K), dtype=np.int8)
+    for lane in range(32):
+        q, j = lane >> 2, lane & 3
+        for c in range(8):
+            w = words[:, :, lane, c >> 1].astype(np.int64)            # [T][G]
+            for r in range(4):
+                row = q + (8 if r & 1 else 0)
+                col = 16 * c + 2 * j + (8 if r & 2 else 0)
+                rp = 4 * (c & 1) + r
+                for h in range(2):
+                    nz = (w >> (16 * h + 7 - rp)) & 1
+                    ng = (w >> (16 * h + 15 - rp)) & 1
+                    assert not (ng & ~nz).any()
+                    val = (nz - 2 * ng).astype(np.int8)                  # [T][G]
+                    for g in range(G):
+                        t[np.arange(T) * 16 + row, g * 128 + col + h] = val[:, g]
+    codes = blob[L.scale_off:L.scale_off + L.scale_bytes].reshape(T, G, 16).transpose(0, 2, 1).reshape(T * 16, G)
+    return t, codes
+
+
 def test_pack_lns8_layout():
     w = W.lns8(seed=1, N=45, K=384)
     blob, L = tg.tg_pack_weights(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
-    t, s = decode_masked(blob, L, np.uint8)
+    assert L.tiles == 3 and L.mask_bytes == 3 * 3 * 512
+    t, s = decode_lns8(blob, L)
     np.testing.assert_array_equal(t[:45], w["t"])
     np.testing.assert_array_equal(s[:45], w["dcode"])
+    assert not t[45:].any() and not s[45:].any()
 
 
 def test_pack_planes_layout():
