@@ -16,8 +16,10 @@
 // and add G[q] * 2^(beta + [q + delta >= 8]) into A[(q + delta) & 7]. This is
 // exact when no lane of that (row, group) is clamped (k in 1..127 for every
 // nonzero lane), which is checked per (row, group) from the group's smallest
-// and largest nonzero activation code; the rare (row, group) that can clamp
-// takes the per-lane route instead.
+// and largest nonzero activation code. In the rare (row, group) that can clamp,
+// the lanes that do clamp are found with bytewise compares, taken back out of
+// G, and their saturated value (+-2^15 in phase 7, or nothing for k <= 0) is
+// added directly; the rest stays on the factorised path.
 //
 // G is a contraction t (rows x lanes) . V (lanes x 8) with V[i][q] = s_i 2^c_i
 // when a_i & 7 == q, else 0. Every entry (+-1, +-2^c) is exact in bf16 and
@@ -31,8 +33,9 @@
 //
 // Mapping: a CTA owns 128 rows (warp w: rows 16w..16w+15) and a slice of the
 // groups; a cluster of up to 8 CTAs covers all groups of those rows. Each CTA
-// keeps int32 phase partials in shared memory; the cluster's first CTA sums
-// them through distributed shared memory into int64 A and materialises S with
+// keeps int32 phase partials in shared memory; each CTA of the cluster then
+// owns a slice of the rows, gathers their partials from the other CTAs through
+// distributed shared memory, sums them into int64 A and materialises S with
 // explicitly rounded fp64 multiplies and adds in the order p = 0..7.
 
 #include <cooperative_groups.h>
@@ -89,34 +92,44 @@ __device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
     return (a != 0u && (a & 7u) == q) ? bf16_pow2(xab >> 7, a >> 3) : 0u;
 }
 
-// Per-lane route for one (row, group) of this thread's 32 lanes (the exact
-// definition; used where the factorised form could meet a clamp).
-__device__ void route_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg,
-                            int *acc_row)
+// Lanes of one (row, group) whose product code k = a + e leaves 1..127, for the
+// 32 lanes this thread holds of that row: each such lane's term +-2^c is taken
+// back out of its class sum (added, negated, into gcorr[a & 7], the row's
+// class corrections in shared memory), and the value the lane really
+// contributes is returned: +-2^15 into phase 7 for k > 127, nothing for k <= 0.
+// With those lanes removed every remaining lane has k in 1..127 and the
+// factorised add is exact again.
+__device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg, int *gcorr)
 {
+    const uint32_t T = (uint32_t)min(max(127 - e, 0), 127) * 0x01010101u;   // a > 127 - e saturates
+    const uint32_t U = (uint32_t)min(max(1 - e, 1), 128) * 0x01010101u;     // 0 < a < 1 - e is zero
+    const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xg);
+    int clamp = 0;
 #pragma unroll
     for (int kc = 0; kc < 8; kc++) {
+        // lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1}: byte bi = 2 * rr + h
+        const uint32_t raw = (uint32_t)__ldg(x16 + 8 * kc + tq) | ((uint32_t)__ldg(x16 + 8 * kc + 4 + tq) << 16);
+        const uint32_t a4 = raw & 0x7f7f7f7fu;
+        uint32_t m = (__vcmpgtu4(a4, T) | (__vcmpltu4(a4, U) & __vcmpne4(a4, 0u))) & 0x80808080u;
         const uint32_t w = w4[kc >> 1];
-#pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-            const int r = half + 2 * rr;                     // pairs of this row: half, half + 2
-            const int rp = 4 * (kc & 1) + r;
-            const int col = 16 * kc + 2 * tq + (rr ? 8 : 0);
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const uint32_t nz = (w >> (16 * h + 7 - rp)) & 1u;
-                const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
-                const uint32_t xab = xg[col + h];
-                const int a = (int)(xab & 0x7fu);
-                int k = a + e;
-                if (nz && a != 0 && k > 0) {
-                    k = min(k, 127);
-                    const int mag = 1 << (k >> 3);
-                    atomicAdd(acc_row + (k & 7), ((xab >> 7) ^ neg) ? -mag : mag);
-                }
-            }
+        while (m) {
+            const int bi = (__ffs((int)m) - 1) >> 3;
+            m &= m - 1u;
+            const int rp = 4 * (kc & 1) + half + 2 * (bi >> 1);
+            const int h = bi & 1;
+            if (((w >> (16 * h + 7 - rp)) & 1u) == 0u)
+                continue;
+            const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
+            const uint32_t xab = (raw >> (8 * bi)) & 0xffu;
+            const int a = (int)(xab & 0x7fu);
+            const bool minus = ((xab >> 7) ^ neg) != 0u;
+            const int v = 1 << (a >> 3);
+            atomicAdd(gcorr + (a & 7), minus ? v : -v);
+            if (a + e > 127)
+                clamp += minus ? -(1 << 15) : (1 << 15);
         }
     }
+    return clamp;
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -127,6 +140,8 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     __shared__ uint2 vfrag[kChunkGroups][8][32];   // V fragments (b0, b1) per group, chunk, lane
     __shared__ unsigned gmin[kChunkGroups], gmax[kChunkGroups];
     __shared__ int acc[kRows][8];                  // int32 phase partials of this CTA's groups
+    __shared__ int stage[kRows + kMaxCluster][8];  // partials of the rows this CTA owns, per source CTA
+    __shared__ int gcorr[kWarps][16][8];           // class-sum corrections of clamped lanes, per warp row
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -138,8 +153,10 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     const int g_begin = rank * gpc;
     const int g_end = min(G, g_begin + gpc);
 
-    for (int i = tid; i < kRows * 8; i += blockDim.x)
+    for (int i = tid; i < kRows * 8; i += blockDim.x) {
         (&acc[0][0])[i] = 0;
+        (&gcorr[0][0][0])[i] = 0;
+    }
 
     const bool active = rb * 16 < N;   // warp-uniform
     for (int c0 = g_begin; c0 < g_end; c0 += kChunkGroups) {
@@ -198,64 +215,96 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                     break;
                 const int grp = c0 + gl;
                 const uint32_t w4[4] = {wv[gl].x, wv[gl].y, wv[gl].z, wv[gl].w};
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                // two independent accumulation chains (even and odd chunks);
+                // each partial is an integer of magnitude below 2^23, so the
+                // fp32 sums and their final sum are exact
+                float d[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int kc = 0; kc < 8; kc++) {
+                for (int kc = 0; kc < 8; kc += 2) {
                     const uint32_t w = w4[kc >> 1];
-                    const uint2 b = vfrag[gl][kc][lane];
-                    if (kc & 1)
-                        mma_bf16_16816(d, frag_pair<4>(w), frag_pair<5>(w), frag_pair<6>(w), frag_pair<7>(w), b.x, b.y);
-                    else
-                        mma_bf16_16816(d, frag_pair<0>(w), frag_pair<1>(w), frag_pair<2>(w), frag_pair<3>(w), b.x, b.y);
+                    const uint2 b0 = vfrag[gl][kc][lane], b1 = vfrag[gl][kc + 1][lane];
+                    mma_bf16_16816(d, frag_pair<0>(w), frag_pair<1>(w), frag_pair<2>(w), frag_pair<3>(w), b0.x, b0.y);
+                    mma_bf16_16816(d1, frag_pair<4>(w), frag_pair<5>(w), frag_pair<6>(w), frag_pair<7>(w), b1.x, b1.y);
                 }
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    d[i] += d1[i];
                 const int lo = (int)gmin[gl], hi = (int)gmax[gl];
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
                     const int e = ec[gl][half];
                     int *acc_row = acc[warp * 16 + gq + 8 * half];
+                    // quad-uniform: the four threads of a quad hold the same row
                     const bool clamp_free = lo > 127 || (lo + e >= 1 && hi + e <= 127);
-                    if (clamp_free) {
+                    int clamp = 0;
+                    if (!clamp_free) {
+                        int *gc = gcorr[warp][gq + 8 * half];
+                        const unsigned qmask = 0xfu << (lane & ~3);
+                        clamp = clamp_lanes(w4, half, tq, e, xa + (size_t)grp * TG_GROUP, gc);
+                        __syncwarp(qmask);
+                        d[2 * half] += (float)gc[2 * tq];
+                        d[2 * half + 1] += (float)gc[2 * tq + 1];
+                        gc[2 * tq] = 0;
+                        gc[2 * tq + 1] = 0;
+                        clamp += __shfl_xor_sync(qmask, clamp, 1);
+                        clamp += __shfl_xor_sync(qmask, clamp, 2);
+                    }
 #pragma unroll
-                        for (int j = 0; j < 2; j++) {
-                            const int q = 2 * tq + j;
-                            const int v = __float2int_rn(d[2 * half + j]);
-                            const int sidx = q + (e & 7);
-                            const int sh = (e >> 3) + (sidx >> 3);
-                            acc_row[sidx & 7] += sh >= 0 ? (v << sh) : (v >> -sh);
-                        }
-                    } else {
-                        route_lanes(w4, half, tq, e, xa + (size_t)grp * TG_GROUP, acc_row);
+                    for (int j = 0; j < 2; j++) {
+                        const int q = 2 * tq + j;
+                        const int v = __float2int_rn(d[2 * half + j]);
+                        const int sidx = q + (e & 7);
+                        const int sh = max(-31, min(31, (e >> 3) + (sidx >> 3)));
+                        int add = sh >= 0 ? (v << sh) : (v >> -sh);
+                        if ((sidx & 7) == 7)
+                            add += clamp;
+                        acc_row[sidx & 7] += add;
                     }
                 }
                 __syncwarp();
             }
         }
     }
+    // Cluster reduction: CTA `dst` of the cluster owns rows [dst * slice,
+    // (dst + 1) * slice) of the 128; every CTA stores its partials of those rows
+    // into the owner's staging area, one barrier makes them visible, and each
+    // owner sums its slice in rank order.
     __syncthreads();
-    cluster.sync();
-    if (rank == 0 && tid < kRows) {
-        const int row = blockIdx.x * kRows + tid;
-        int64_t a8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int r = 0; r < csize; r++) {
-            const int *remote = cluster.map_shared_rank(&acc[0][0], r);
-#pragma unroll
-            for (int p = 0; p < 8; p++)
-                a8[p] += remote[tid * 8 + p];
-        }
-        if (row < N) {
-#pragma unroll
-            for (int p = 0; p < 8; p++)
-                A[(size_t)row * 8 + p] = a8[p];
-            if (S) {
-                double sum = 0.0;
-#pragma unroll
-                for (int p = 0; p < 8; p++)
-                    sum = __dadd_rn(sum, __dmul_rn((double)a8[p], F.f[p]));
-                S[row] = __dmul_rn(sum, 0x1p-9);
-            }
-        }
+    const int slice = (kRows + csize - 1) / csize;
+    for (int item = tid; item < kRows * 8; item += blockDim.x) {
+        const int rl = item >> 3, p = item & 7;
+        const int dst = rl / slice;
+        int *remote = cluster.map_shared_rank(&stage[0][0], dst);
+        remote[((rank * slice) + (rl - dst * slice)) * 8 + p] = acc[rl][p];
     }
     cluster.sync();
+    for (int b = 0; b < slice * 8; b += blockDim.x) {   // uniform over the block: shuffles below see full warps
+        const int item = b + tid;
+        const int i = item >> 3, p = item & 7;
+        const int rl = rank * slice + i;
+        const int row = blockIdx.x * kRows + rl;
+        const bool valid = item < slice * 8 && rl < kRows && row < N;
+        int64_t a = 0;
+        if (valid)
+            for (int src = 0; src < csize; src++)
+                a += stage[src * slice + i][p];
+        if (valid)
+            A[(size_t)row * 8 + p] = a;
+        if (S) {
+            // S in the order p = 0..7: lane p == 0 of each 8-lane row gathers the products
+            double fp = F.f[0];
+#pragma unroll
+            for (int pp = 1; pp < 8; pp++)
+                fp = p == pp ? F.f[pp] : fp;   // selects keep F in parameter space
+            const double prod = __dmul_rn((double)a, fp);
+            double sum = 0.0;
+#pragma unroll
+            for (int pp = 0; pp < 8; pp++)
+                sum = __dadd_rn(sum, __shfl_sync(0xffffffffu, prod, (lane & ~7) | pp));
+            if (valid && p == 0)
+                S[row] = __dmul_rn(sum, 0x1p-9);
+        }
+    }
 }
 
 }  // namespace
