@@ -81,3 +81,26 @@ def test_only_exact_ternary_rows():
     planes = w["planes"].copy()
     planes[1:] = 0
     check(planes, w["s"], w["x"], 64)
+
+
+def test_row_shards_merge_to_global_topk():
+    """Vocabulary split into three independently packed row shards: each shard's
+    two-stage top-k on the GPU, merged on the host, equals the global top-k."""
+    import bit_decode_gemv_gb300 as tg
+    from bit_decode_gemv_gb300.shard import merge_topk, shard_rows
+    from gpu_helpers import lmhead, pack_to_device
+    w = W.lm_head(seed=21, N=6000, K=512)
+    k = 64
+    logits_ref = oracle.lmhead_logits(w["planes"], w["s"], w["x"])
+    ids, scores = [], []
+    for r in range(3):
+        a, b = shard_rows(w["planes"].shape[1], 3, r)
+        wd, L = pack_to_device(tg.TG_PLANES8, np.ascontiguousarray(w["planes"][:, a:b]), w["s"][a:b])
+        out = lmhead(wd, L, w["x"], k, False)
+        ids.append(out["ids"].astype(np.int64) + a)
+        scores.append(out["scores"])
+    got_ids, got_scores = merge_topk(ids, scores, k)
+    ref_ids, ref_scores = oracle.topk(logits_ref, k)
+    np.testing.assert_array_equal(got_ids, ref_ids)
+    np.testing.assert_array_equal(got_scores, ref_scores)
+    assert got_ids[0] == oracle.argmax(logits_ref)
