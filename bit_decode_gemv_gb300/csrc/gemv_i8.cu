@@ -160,6 +160,8 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
 // ---------------------------------------------------------------------------
 constexpr int kMT = 16;   // tokens per warp
 constexpr int kKC = 4;    // groups per shared-memory chunk
+// From this many tokens on, the tensor-core kernel (gemv_i8_mma.cu) runs.
+constexpr int kMmaMinTokens = 2;
 
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
@@ -317,6 +319,8 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
             e = launch_m1<4>(masks, scales, x, y, N, G, tiles, pdl, s);
         if (e != cudaSuccess)
             return TG_ERR_CUDA;
+    } else if (M >= kMmaMinTokens) {
+        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, s);
     } else {
         const int warps = (int)((M + kMT - 1) / kMT);
         switch (warps) {

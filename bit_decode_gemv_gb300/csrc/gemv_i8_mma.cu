@@ -1,0 +1,500 @@
+// gemv_i8_mma.cu -- small-batch ternary GEMM (M = 2..64 tokens) on the
+// fifth-generation tensor cores (integer_engine.md §4.2 with §4.4, batched):
+//
+//   y[m][r] = sum_g d[r][g] * P[m][r][g],   P[m][r][g] = sum_{i in g} t[r][i] * x[m][i]
+//
+// Exactness. t is -1/0/+1 and x an int8, both exact fp16 values. The tensor
+// core sums one group at a time in fp32 into an accumulator that starts at
+// 1.5 * 2^23 (the D buffer is filled with that value before the group's first
+// step); a group's sum has |P| <= 128 * 128 = 2^14, so every partial sum is an
+// integer in (2^23, 2^24), where consecutive fp32 values are exactly 1 apart:
+// nothing is rounded and the accumulator's bit pattern is 0x4B400000 + P. The
+// epilogue multiplies that bit pattern by d[r][g] into a wrapping 64-bit
+// accumulator per token and at the end subtracts 0x4B400000 * sum_g d[r][g];
+// the result is exact modulo 2^64 and therefore exact, since y fits in int64
+// (checked on the host).
+//
+// Mapping. A CTA owns 128 rows (four 32-row mask tiles) for all groups and all
+// tokens. 16 compute warps and one MMA warp hand work to each other through
+// mbarrier rings, with no CTA-wide barrier inside the group loop.
+//   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
+//     rows of mask tile w%4) and handles part p = w/4. In its iteration for
+//     group g it first reads back group g-2's D buffer for tokens
+//     16p..16p+15, accumulates it, and refills that buffer with the offset for
+//     group g+2; then expands its 32 weights of group g (group lanes
+//     32p..32p+31, from the mask ring) to fp16, one byte permute per two
+//     weights, into A slot g%3 in tensor memory (row = lane, K along the
+//     columns), converts two 8-byte activation chunks (loaded two groups
+//     ahead) into B slot g%3 in shared memory, in the canonical K-major layout
+//     of 8-row x 16-byte core matrices, and arrives on the slot's "full"
+//     barrier.
+//   - The MMA warp, when A/B slot g%3 is full and D buffer g%4 has been
+//     refilled, issues the eight K=16 steps of group g (one thread) and
+//     commits them to the slot's "empty" and the buffer's "full" barriers; it
+//     then bulk-copies (TMA) the mask bytes of group g+8 into the ring stage
+//     group g used, which every compute warp has read by then.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "tg.h"
+#include "tg_internal.h"
+
+TGI_DEFINE_DEVICE_ERROR(gemv_mma_take_device_error)
+
+namespace {
+
+constexpr int kComputeWarps = 16;
+constexpr int kThreads = (kComputeWarps + 1) * 32;   // + the MMA warp
+constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
+constexpr int kMaxN = 64;                 // tokens, the MMA's N at most
+constexpr int kStages = 8;                // mask ring stages
+constexpr int kSlots = 3;                 // A/B slots
+constexpr int kDBufs = 4;                 // D buffers
+constexpr int kLag = 2;                   // the epilogue of group g runs after the inputs of group g + kLag
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColA = 0;             // A slots: 64 columns each (128 fp16 of K per row)
+constexpr uint32_t kColD = 64 * kSlots;   // D buffers: kMaxN columns each
+static_assert(kColD + kDBufs * kMaxN <= kTmemCols, "tensor memory plan");
+static_assert(kMaxN == 64, "each compute warp reads and refills 16 D columns");
+constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^23
+
+// Shared-memory plan (dynamic), byte offsets.
+constexpr int kKStepBytes = (kMaxN / 8) * 256;         // one K=16 step of B: token octets x 256 B
+constexpr int kBBytes = 8 * kKStepBytes;               // one group of B
+constexpr int kOffB = 0;                               // kSlots B slots
+constexpr int kOffStages = kOffB + kSlots * kBBytes;
+constexpr int kStageBytes = 4096;                      // masks of 4 tiles
+// mbarriers: mask stage full, A/B slot full/empty, D buffer full/empty
+constexpr int kBarMFull = 0, kBarABFull = kStages, kBarABEmpty = kStages + kSlots;
+constexpr int kBarDFull = kStages + 2 * kSlots, kBarDEmpty = kBarDFull + kDBufs, kNumBars = kBarDEmpty + kDBufs;
+constexpr int kOffBar = kOffStages + kStages * kStageBytes;
+constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+constexpr int kSmemBytes = kOffSlot + 16;
+static_assert(kStageBytes % 16 == 0 && kOffStages % 16 == 0, "bulk copies need 16-byte alignment");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Shared-memory matrix descriptor, K-major without swizzle: core matrices of
+// 8 rows x 16 bytes stored as 128 contiguous bytes, K-adjacent core matrices
+// 128 bytes apart (leading byte offset), 8-row groups 256 bytes apart (stride
+// byte offset); bit 46 is the descriptor version of this MMA generation.
+// The same strides serve every operand tile here.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) |
+           ((uint64_t)(256u >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: fp16 A and B, both K-major, fp32 D,
+// M = 128, N = n.
+__device__ __forceinline__ uint32_t instr_desc(uint32_t n)
+{
+    return (1u << 4) | ((n >> 3) << 17) | ((uint32_t)(kRowsPerCta >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_a_tmem(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 16 columns: thread i writes its v[0..15] into lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// 32 lanes x 16 columns: thread i reads lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk (TMA) copy global -> shared, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Wait for phase `parity` of an mbarrier: one non-blocking test, then
+// suspending waits. Gives up (returns false) after about two seconds of SM
+// clock, or once *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done)
+        return true;
+    const long long start = clock64();
+    while (true) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+        if (*abort || clock64() - start > (4ll << 30))
+            return false;
+    }
+}
+
+// fp16 (+1, -1, 0) of weight codes f = W_nonzero | W_negative << 1 held in
+// nibbles 1 and 3 of the selector: byte 0 of the table is 0x00 (the low byte
+// of every value, and the high byte for f = 0), byte 1 is 0x3C (+1: 0x3C00),
+// byte 3 is 0xBC (-1: 0xBC00).
+__device__ __forceinline__ uint32_t fp16_pair(uint32_t sel) { return __byte_perm(0xBC003C00u, 0u, sel); }
+
+// Eight int8 activations -> eight exact fp16 values: the bytes x ^ 0x80 =
+// x + 128 sit under the exponent byte 0x64 (fp16 0x64bb is 1024 + bb exactly),
+// then 1152 is subtracted (exact: the result is the integer x).
+__device__ __forceinline__ uint32_t fp16x2_sub1152(uint32_t v)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64806480u));
+    return r;
+}
+
+__device__ __forceinline__ uint4 fp16_of_int8x8(uint2 v)
+{
+    const uint32_t lo = v.x ^ 0x80808080u, hi = v.y ^ 0x80808080u;
+    return make_uint4(fp16x2_sub1152(__byte_perm(lo, 0x64646464u, 0x5140)),
+                      fp16x2_sub1152(__byte_perm(lo, 0x64646464u, 0x7362)),
+                      fp16x2_sub1152(__byte_perm(hi, 0x64646464u, 0x5140)),
+                      fp16x2_sub1152(__byte_perm(hi, 0x64646464u, 0x7362)));
+}
+
+// acc + (int64)a * b, wrapping modulo 2^64.
+__device__ __forceinline__ uint64_t mad_wide(uint32_t a, int32_t b, uint64_t acc)
+{
+    uint64_t r;
+    asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(acc));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Expand one mask word (16 weights, lanes 16u + 4j + b in bits 8b + 2j, 8b + 2j + 1)
+// into 8 fp16 pairs: out[2j] holds lanes 4j, 4j + 1 and out[2j + 1] lanes 4j + 2, 4j + 3.
+__device__ __forceinline__ void expand_word(uint32_t w, uint32_t *out)
+{
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const uint32_t m = w & (0x03030303u << (2 * j));
+        const uint32_t s01 = j < 2 ? m << (4 - 2 * j) : m >> (2 * j - 4);   // codes of bytes 0, 1 -> nibbles 1, 3
+        out[2 * j] = fp16_pair(s01);
+        out[2 * j + 1] = fp16_pair(m >> (12 + 2 * j));                    // bytes 2, 3 -> nibbles 1, 3
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__restrict__ scales,
+                   const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int tiles, int M)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ volatile int abort_flag;   // set when a bounded wait gave up
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int K = G * TG_GROUP;
+    const uint32_t nmma = (uint32_t)((M + 15) & ~15);
+    const int tiles_here = min(4, tiles - (int)blockIdx.x * 4);
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + kOffBar;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    auto *slot = reinterpret_cast<volatile uint32_t *>(smem + kOffSlot);
+
+    // --- set-up: zero the B slots (tokens M.. stay zero), barriers, TMEM
+    for (int i = tid; i < kOffStages / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < kStages; i++)
+            mbar_init(bar(kBarMFull + i), 1);
+        for (int i = 0; i < kSlots; i++) {
+            mbar_init(bar(kBarABFull + i), kComputeWarps);
+            mbar_init(bar(kBarABEmpty + i), 1);
+        }
+        for (int i = 0; i < kDBufs; i++) {
+            mbar_init(bar(kBarDFull + i), 1);
+            mbar_init(bar(kBarDEmpty + i), kComputeWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sbase + kOffSlot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *slot;
+
+    // A bounded wait; once any thread has given up, the others stop waiting too.
+    auto wait = [&](int i, uint32_t parity) {
+        if (!mbar_wait(bar(i), parity, &abort_flag) && !abort_flag) {
+            atomicExch(&tgi_device_error_word, 1);
+            abort_flag = 1;
+        }
+    };
+
+    if (warp == kComputeWarps) {
+        // ---------------- MMA warp (also the mask copier) ----------------
+        const uint32_t tx = (uint32_t)tiles_here * 1024u;
+        auto copy_masks = [&](int g) {   // mask bytes of group g (four tiles) -> stage g % kStages
+            const int st = g % kStages;
+            if (lane == 0)
+                mbar_expect_tx(bar(kBarMFull + st), tx);
+            __syncwarp();
+            if (lane < tiles_here)
+                bulk_copy(sbase + kOffStages + st * kStageBytes + lane * 1024,
+                          masks + ((size_t)(blockIdx.x * 4 + lane) * G + g) * 1024, 1024, bar(kBarMFull + st));
+            __syncwarp();
+        };
+        for (int g = 0; g < min(G, kStages); g++)
+            copy_masks(g);
+        const uint32_t idesc = instr_desc(nmma);
+        for (int g = 0; g < G; g++) {
+            const int sl = g % kSlots, db = g % kDBufs;
+            if (lane == 0) {
+                wait(kBarABFull + sl, (uint32_t)(g / kSlots) & 1u);
+                wait(kBarDEmpty + db, (uint32_t)(g / kDBufs) & 1u);   // refilled with the offset
+                if (!abort_flag) {
+                    fence_after_sync();
+                    const uint32_t dt = tmem + kColD + (uint32_t)(kMaxN * db);
+                    const uint32_t Bs = sbase + kOffB + sl * kBBytes;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ks++)
+                        mma_a_tmem(dt, tmem + kColA + 64u * (uint32_t)sl + 8u * ks, smem_desc(Bs + ks * kKStepBytes),
+                                   idesc, 1u);
+                    mma_commit(bar(kBarABEmpty + sl));
+                    mma_commit(bar(kBarDFull + db));
+                }
+            }
+            __syncwarp();
+            if (__shfl_sync(0xffffffffu, abort_flag, 0))
+                break;
+            if (g + kStages < G)   // every compute warp read stage g % kStages before arriving on "full"
+                copy_masks(g + kStages);
+        }
+    } else {
+        // ---------------- compute warps ----------------
+        const int q = warp & 3, p = warp >> 2;
+        const int tile = blockIdx.x * 4 + q;
+        const bool tile_ok = tile < tiles;
+        const int row = tile * tgi::kTileRows + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const bool epi = 16 * p < M;   // warp-uniform: this warp's tokens exist
+        const int32_t *dsrc = scales + (size_t)tile * G * tgi::kTileRows + lane;   // + g * 32
+
+        // activation chunks: token xn, chunks xc0 and xc0 + 4 of each group
+        const int xn = (warp & 7) * 8 + (lane & 7);
+        const int xc0 = 8 * (warp >> 3) + (lane >> 3);
+        const bool x_ok = xn < M;
+        const int8_t *xrow = x + (size_t)xn * K + 8 * xc0;
+        uint2 xr[2][2];
+        int dr[2] = {0, 0};
+        auto prefetch = [&](int bb, int g) {
+            if (g < G) {
+                if (x_ok) {
+                    xr[bb][0] = __ldg(reinterpret_cast<const uint2 *>(xrow + (size_t)g * TG_GROUP));
+                    xr[bb][1] = __ldg(reinterpret_cast<const uint2 *>(xrow + (size_t)g * TG_GROUP + 32));
+                }
+                if (tile_ok)
+                    dr[bb] = __ldg(dsrc + (size_t)g * tgi::kTileRows);
+            }
+        };
+        prefetch(0, 0);
+        prefetch(1, 1);
+
+        uint32_t offs[16];   // the offset 1.5 * 2^23 in every accumulator column
+#pragma unroll
+        for (int j = 0; j < 16; j++)
+            offs[j] = kOffsetBits;
+        // D buffers of groups 0..kDBufs-1 start at the offset
+#pragma unroll 1
+        for (int db = 0; db < kDBufs; db++)
+            tmem_st16(tmem + lane_off + kColD + (uint32_t)(kMaxN * db) + 16u * (uint32_t)p, offs);
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0)
+            for (int db = 0; db < kDBufs; db++)
+                mbar_arrive(bar(kBarDEmpty + db));
+
+        uint64_t acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++)
+            acc[j] = 0;
+        uint64_t dsum = 0;
+        int d_lag[2] = {0, 0};   // scale of group g, kept for its epilogue kLag groups later
+
+        // read back group gp's D buffer, accumulate, and refill it with the offset for group gp + kDBufs
+        auto epilogue = [&](int gp, int dgp, bool refill) {
+            const int db = gp % kDBufs;
+            wait(kBarDFull + db, (uint32_t)(gp / kDBufs) & 1u);
+            fence_after_sync();
+            const uint32_t dcol = tmem + lane_off + kColD + (uint32_t)(kMaxN * db) + 16u * (uint32_t)p;
+            uint32_t v[16];
+            if (epi) {
+                tmem_ld16(dcol, v);
+                tmem_wait_ld();
+            }
+            if (refill)
+                tmem_st16(dcol, offs);
+            if (epi) {
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                    acc[j] = mad_wide(v[j], dgp, acc[j]);
+            }
+        };
+
+        static_assert(kLag == 2, "the scale history below keeps two groups");
+#pragma unroll 1
+        for (int g0 = 0; g0 < G; g0 += 2) {
+#pragma unroll
+            for (int bb = 0; bb < 2; bb++) {   // g & 1: register buffer of the prefetched inputs, static
+                const int g = g0 + bb;
+                if (g >= G)
+                    break;
+                const int sl = g % kSlots, st = g % kStages;
+                const bool refill = g >= kLag && g - kLag + kDBufs < G;
+                if (g >= kLag)
+                    epilogue(g - kLag, d_lag[bb], refill);   // group g - 2 has the same parity as g
+                if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
+                    wait(kBarABEmpty + sl, (uint32_t)(g / kSlots - 1) & 1u);
+                wait(kBarMFull + st, (uint32_t)(g / kStages) & 1u);
+                const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(smem + kOffStages + st * kStageBytes +
+                                                                            q * 1024 + (p >> 1) * 512 + lane * 16 +
+                                                                            (p & 1) * 8)
+                                         : make_uint2(0, 0);
+                {
+                    // words 2(p%2), 2(p%2)+1 of half p/2: group lanes 32p..32p+31 -> columns 16p..16p+15
+                    uint32_t a[16];
+                    expand_word(mw.x, a);
+                    expand_word(mw.y, a + 8);
+                    tmem_st16(tmem + lane_off + kColA + 64u * (uint32_t)sl + 16u * (uint32_t)p, a);
+                }
+                if (x_ok) {
+                    unsigned char *B = smem + kOffB + sl * kBBytes;
+#pragma unroll
+                    for (int it = 0; it < 2; it++) {
+                        const int c = xc0 + 4 * it;   // chunk: K elements 8c..8c+7 of the group
+                        *reinterpret_cast<uint4 *>(B + (c >> 1) * kKStepBytes + (xn >> 3) * 256 + (c & 1) * 128 +
+                                                   (xn & 7) * 16) = fp16_of_int8x8(xr[bb][it]);
+                    }
+                }
+                const int dg = dr[bb];
+                dsum += (uint64_t)(int64_t)dg;
+                prefetch(bb, g + 2);
+                tmem_wait_st();   // A of group g and the refilled D buffer
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(kBarABFull + sl));
+                    if (refill)
+                        mbar_arrive(bar(kBarDEmpty + (g - kLag) % kDBufs));
+                }
+                d_lag[bb] = dg;
+            }
+        }
+        for (int gp = max(0, G - kLag); gp < G; gp++)
+            epilogue(gp, (gp & 1) ? d_lag[1] : d_lag[0], false);
+
+        // y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64)
+        if (epi && tile_ok && row < N) {
+            const uint64_t corr = (uint64_t)kOffsetBits * dsum;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int m = 16 * p + j;
+                if (m < M)
+                    y[(size_t)m * N + row] = (int64_t)(acc[j] - corr);
+            }
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+}  // namespace
+
+namespace tgi {
+
+int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
+                int tiles, int M, cudaStream_t s)
+{
+    static bool attr_set = false;   // set once per process; idempotent if raced
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemv_i8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
+            return TG_ERR_CUDA;
+        attr_set = true;
+    }
+    const int grid = (tiles + 3) / 4;
+    gemv_i8_mma_kernel<<<grid, kThreads, kSmemBytes, s>>>(reinterpret_cast<const unsigned char *>(masks), scales,
+                                                         x, y, N, G, tiles, M);
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace tgi

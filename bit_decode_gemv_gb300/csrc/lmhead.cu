@@ -728,8 +728,8 @@ extern "C" int tg_device_error(void *stream, int32_t *code)
     if (!code)
         return TG_ERR_ARG;
     int worst = TG_OK;
-    const int r[3] = {tgi::gemv_take_device_error(stream), tgi::lns8_take_device_error(stream),
-                      tgi::lmhead_take_device_error(stream)};
+    const int r[4] = {tgi::gemv_take_device_error(stream), tgi::gemv_mma_take_device_error(stream),
+                      tgi::lns8_take_device_error(stream), tgi::lmhead_take_device_error(stream)};
     for (int v : r) {
         if (v == TG_ERR_CUDA)
             return TG_ERR_CUDA;

@@ -4,6 +4,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 #include "tg.h"
 
 namespace tgi {
@@ -16,7 +18,13 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 // Per translation unit: read-and-clear of that unit's device error word.
 // Each returns 0 or TG_ERR_DEVICE, or TG_ERR_CUDA if the query failed.
 int gemv_take_device_error(void *stream);
+int gemv_mma_take_device_error(void *stream);
 int lns8_take_device_error(void *stream);
 int lmhead_take_device_error(void *stream);
+
+// Small-batch ternary GEMM on the tensor cores (2 <= M <= 64); arguments as
+// checked by tg_gemv_i8. Returns a tg_status.
+int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
+                int tiles, int M, cudaStream_t s);
 
 }  // namespace tgi

@@ -137,3 +137,21 @@ def test_const_weights_back_to_back(N, K):
         for i, w in enumerate(cases):
             xi = xs[(i + rep) % 4].cpu().numpy()
             np.testing.assert_array_equal(outs[rep * 4 + i].cpu().numpy(), oracle.gemv_i8(w["t"], w["d"], xi))
+
+
+@pytest.mark.parametrize("M", [2, 31, 64])
+def test_extreme_values_batched(M):
+    """Largest group sums |P| = 2^14 and int32-extreme scales with several tokens."""
+    N, K = 300, 1024
+    rng = np.random.default_rng(5 + M)
+    t = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    t[:50] = -1
+    t[50:100] = 1
+    d = rng.integers(np.iinfo(np.int32).min, np.iinfo(np.int32).max, size=(N, K // 128),
+                     dtype=np.int64).astype(np.int32)
+    d[::3] = np.iinfo(np.int32).max
+    d[1::3] = np.iinfo(np.int32).min
+    x = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    x[0] = -128
+    x[-1] = 127
+    check(dict(t=t, d=d, x=x))
