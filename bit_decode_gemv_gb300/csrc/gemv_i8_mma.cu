@@ -15,24 +15,26 @@
 // (checked on the host).
 //
 // Mapping. A CTA owns 128 rows (four 32-row mask tiles) for all groups and all
-// tokens. 16 compute warps and one MMA warp hand work to each other through
+// tokens. 8 compute warps, two MMA warps and a copy warp hand work to each other through
 // mbarrier rings, with no CTA-wide barrier inside the group loop.
 //   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
-//     rows of mask tile w%4) and handles part p = w/4. In its iteration for
+//     rows of mask tile w%4) and handles half h = w/4. In its iteration for
 //     group g it first reads back group g-2's D buffer for tokens
-//     16p..16p+15, accumulates it, and refills that buffer with the offset for
-//     group g+2; then expands its 32 weights of group g (group lanes
-//     32p..32p+31, from the mask ring) to fp16, one byte permute per two
+//     32h..32h+31, accumulates it, and refills that buffer with the offset for
+//     group g+2; then expands its 64 weights of group g (group lanes
+//     64h..64h+63, from the mask ring) to fp16, one byte permute per two
 //     weights, into A slot g%3 in tensor memory (row = lane, K along the
-//     columns), converts two 8-byte activation chunks (loaded two groups
+//     columns), converts four 8-byte activation chunks (loaded two groups
 //     ahead) into B slot g%3 in shared memory, in the canonical K-major layout
 //     of 8-row x 16-byte core matrices, and arrives on the slot's "full"
 //     barrier.
-//   - The MMA warp, when A/B slot g%3 is full and D buffer g%4 has been
-//     refilled, issues the eight K=16 steps of group g (one thread) and
-//     commits them to the slot's "empty" and the buffer's "full" barriers; it
-//     then bulk-copies (TMA) the mask bytes of group g+8 into the ring stage
-//     group g used, which every compute warp has read by then.
+//   - Two MMA warps take the even and the odd groups. When A/B slot g%3 is full
+//     and D buffer g%4 has been refilled, one thread issues the eight K=16
+//     steps of group g and commits them to the slot's "empty" and the buffer's
+//     "full" barriers. (One thread issues an MMA only every ~70 cycles, so two
+//     issuers keep the tensor core busier.)
+//   - A copy warp bulk-copies (TMA) the mask bytes of group g+8 into the ring
+//     stage group g used, once every compute warp has read it.
 
 #include <cuda_runtime.h>
 
@@ -46,8 +48,9 @@ TGI_DEFINE_DEVICE_ERROR(gemv_mma_take_device_error)
 
 namespace {
 
-constexpr int kComputeWarps = 16;
-constexpr int kThreads = (kComputeWarps + 1) * 32;   // + the MMA warp
+constexpr int kComputeWarps = 8;
+constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd groups)
+constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
 constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
 constexpr int kMaxN = 64;                 // tokens, the MMA's N at most
 constexpr int kStages = 8;                // mask ring stages
@@ -58,7 +61,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;             // A slots: 64 columns each (128 fp16 of K per row)
 constexpr uint32_t kColD = 64 * kSlots;   // D buffers: kMaxN columns each
 static_assert(kColD + kDBufs * kMaxN <= kTmemCols, "tensor memory plan");
-static_assert(kMaxN == 64, "each compute warp reads and refills 16 D columns");
+static_assert(kMaxN == 64, "each compute warp reads and refills 32 D columns");
 constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^23
 
 // Shared-memory plan (dynamic), byte offsets.
@@ -115,26 +118,30 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 lanes x 16 columns: thread i writes its v[0..15] into lane (taddr.lane + i).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+// 32 lanes x 32 columns: thread i writes its v[0..31] into lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
 {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15, %16};"
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
         ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 
-// 32 lanes x 16 columns: thread i reads lane (taddr.lane + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+// 32 lanes x 32 columns: thread i reads lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15])
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr)
         : "memory");
 }
@@ -294,10 +301,10 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
         }
     };
 
-    if (warp == kComputeWarps) {
-        // ---------------- MMA warp (also the mask copier) ----------------
+    if (warp == kComputeWarps + kMmaWarps) {
+        // ---------------- copy warp: mask bytes of group g -> stage g % kStages ----------------
         const uint32_t tx = (uint32_t)tiles_here * 1024u;
-        auto copy_masks = [&](int g) {   // mask bytes of group g (four tiles) -> stage g % kStages
+        auto copy_masks = [&](int g) {
             const int st = g % kStages;
             if (lane == 0)
                 mbar_expect_tx(bar(kBarMFull + st), tx);
@@ -309,68 +316,80 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
         };
         for (int g = 0; g < min(G, kStages); g++)
             copy_masks(g);
-        const uint32_t idesc = instr_desc(nmma);
-        for (int g = 0; g < G; g++) {
-            const int sl = g % kSlots, db = g % kDBufs;
-            if (lane == 0) {
-                wait(kBarABFull + sl, (uint32_t)(g / kSlots) & 1u);
-                wait(kBarDEmpty + db, (uint32_t)(g / kDBufs) & 1u);   // refilled with the offset
-                if (!abort_flag) {
-                    fence_after_sync();
-                    const uint32_t dt = tmem + kColD + (uint32_t)(kMaxN * db);
-                    const uint32_t Bs = sbase + kOffB + sl * kBBytes;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ks++)
-                        mma_a_tmem(dt, tmem + kColA + 64u * (uint32_t)sl + 8u * ks, smem_desc(Bs + ks * kKStepBytes),
-                                   idesc, 1u);
-                    mma_commit(bar(kBarABEmpty + sl));
-                    mma_commit(bar(kBarDFull + db));
-                }
-            }
+        for (int g = 0; g + kStages < G; g++) {
+            // every compute warp read stage g % kStages before arriving on "full" of group g
+            if (lane == 0)
+                wait(kBarABFull + g % kSlots, (uint32_t)(g / kSlots) & 1u);
             __syncwarp();
             if (__shfl_sync(0xffffffffu, abort_flag, 0))
                 break;
-            if (g + kStages < G)   // every compute warp read stage g % kStages before arriving on "full"
-                copy_masks(g + kStages);
+            copy_masks(g + kStages);
         }
+    } else if (warp >= kComputeWarps) {
+        // ---------------- MMA warps: groups g = (warp - kComputeWarps) mod 2 ----------------
+        const uint32_t idesc = instr_desc(nmma);
+        if (lane == 0) {
+            for (int g = warp - kComputeWarps; g < G && !abort_flag; g += kMmaWarps) {
+                const int sl = g % kSlots, db = g % kDBufs;
+                wait(kBarABFull + sl, (uint32_t)(g / kSlots) & 1u);
+                wait(kBarDEmpty + db, (uint32_t)(g / kDBufs) & 1u);   // refilled with the offset
+                if (abort_flag)
+                    break;
+                fence_after_sync();
+                const uint32_t dt = tmem + kColD + (uint32_t)(kMaxN * db);
+                const uint32_t Bs = sbase + kOffB + sl * kBBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++)
+                    mma_a_tmem(dt, tmem + kColA + 64u * (uint32_t)sl + 8u * ks, smem_desc(Bs + ks * kKStepBytes),
+                               idesc, 1u);
+                mma_commit(bar(kBarABEmpty + sl));
+                mma_commit(bar(kBarDFull + db));
+            }
+        }
+        __syncwarp();
     } else {
         // ---------------- compute warps ----------------
-        const int q = warp & 3, p = warp >> 2;
+        const int q = warp & 3, h = warp >> 2;
         const int tile = blockIdx.x * 4 + q;
         const bool tile_ok = tile < tiles;
         const int row = tile * tgi::kTileRows + lane;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const bool epi = 16 * p < M;   // warp-uniform: this warp's tokens exist
-        const int32_t *dsrc = scales + (size_t)tile * G * tgi::kTileRows + lane;   // + g * 32
+        const bool epi = 32 * h < M;   // warp-uniform: this warp's tokens exist
 
-        // activation chunks: token xn, chunks xc0 and xc0 + 4 of each group
-        const int xn = (warp & 7) * 8 + (lane & 7);
-        const int xc0 = 8 * (warp >> 3) + (lane >> 3);
+        // activation chunks: token xn, chunks 4c4..4c4+3 (K elements 32c4..32c4+31) of each group
+        const int xn = warp * 8 + (lane & 7);
+        const int c4 = lane >> 3;
         const bool x_ok = xn < M;
-        const int8_t *xrow = x + (size_t)xn * K + 8 * xc0;
-        uint2 xr[2][2];
+        const int8_t *xp = x + (size_t)xn * K + 32 * c4;                       // advances by 128 per group
+        const int32_t *dp = scales + (size_t)tile * G * tgi::kTileRows + lane;   // advances by 32 per group
+        uint4 xr[2][2];
         int dr[2] = {0, 0};
-        auto prefetch = [&](int bb, int g) {
-            if (g < G) {
+        int pf_left = G;   // groups not yet prefetched
+        auto prefetch = [&](int bb) {
+            if (pf_left > 0) {
                 if (x_ok) {
-                    xr[bb][0] = __ldg(reinterpret_cast<const uint2 *>(xrow + (size_t)g * TG_GROUP));
-                    xr[bb][1] = __ldg(reinterpret_cast<const uint2 *>(xrow + (size_t)g * TG_GROUP + 32));
+                    xr[bb][0] = __ldg(reinterpret_cast<const uint4 *>(xp));
+                    xr[bb][1] = __ldg(reinterpret_cast<const uint4 *>(xp) + 1);
                 }
                 if (tile_ok)
-                    dr[bb] = __ldg(dsrc + (size_t)g * tgi::kTileRows);
+                    dr[bb] = __ldg(dp);
+                xp += TG_GROUP;
+                dp += tgi::kTileRows;
+                pf_left--;
             }
         };
-        prefetch(0, 0);
-        prefetch(1, 1);
+        prefetch(0);
+        prefetch(1);
 
-        uint32_t offs[16];   // the offset 1.5 * 2^23 in every accumulator column
+        uint32_t offs[32];   // the offset 1.5 * 2^23 in every accumulator column
 #pragma unroll
-        for (int j = 0; j < 16; j++)
+        for (int j = 0; j < 32; j++)
             offs[j] = kOffsetBits;
         // D buffers of groups 0..kDBufs-1 start at the offset
+        const uint32_t dbase = tmem + lane_off + kColD + 32u * (uint32_t)h;
 #pragma unroll 1
         for (int db = 0; db < kDBufs; db++)
-            tmem_st16(tmem + lane_off + kColD + (uint32_t)(kMaxN * db) + 16u * (uint32_t)p, offs);
+            tmem_st32(dbase + (uint32_t)(kMaxN * db), offs);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
@@ -378,30 +397,44 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
             for (int db = 0; db < kDBufs; db++)
                 mbar_arrive(bar(kBarDEmpty + db));
 
-        uint64_t acc[16];
+        uint64_t acc[32];
 #pragma unroll
-        for (int j = 0; j < 16; j++)
+        for (int j = 0; j < 32; j++)
             acc[j] = 0;
         uint64_t dsum = 0;
         int d_lag[2] = {0, 0};   // scale of group g, kept for its epilogue kLag groups later
 
-        // read back group gp's D buffer, accumulate, and refill it with the offset for group gp + kDBufs
-        auto epilogue = [&](int gp, int dgp, bool refill) {
-            const int db = gp % kDBufs;
-            wait(kBarDFull + db, (uint32_t)(gp / kDBufs) & 1u);
+        // ring positions of group g, advanced by counters
+        int sl = 0, st = 0;              // A/B slot, mask stage
+        uint32_t sl_par = 0, st_par = 0;  // phase parities of those uses
+        int db_e = 0;                    // D buffer of group g - kLag
+        uint32_t db_par = 0;
+        const unsigned char *mrow = smem + kOffStages + q * 1024 + h * 512 + lane * 16;
+        const uint32_t abase = tmem + lane_off + kColA + 32u * (uint32_t)h;
+        unsigned char *bdst = smem + kOffB + warp * 256 + (lane & 7) * 16;   // + slot, + chunk position
+
+        // read back group gp's D buffer (db_e), accumulate, and refill it with the offset
+        auto epilogue = [&](int dgp, bool refill) {
+            wait(kBarDFull + db_e, db_par);
             fence_after_sync();
-            const uint32_t dcol = tmem + lane_off + kColD + (uint32_t)(kMaxN * db) + 16u * (uint32_t)p;
-            uint32_t v[16];
+            const uint32_t dcol = dbase + (uint32_t)(kMaxN * db_e);
             if (epi) {
-                tmem_ld16(dcol, v);
+                uint32_t v[32];
+                tmem_ld32(dcol, v);
                 tmem_wait_ld();
-            }
-            if (refill)
-                tmem_st16(dcol, offs);
-            if (epi) {
+                if (refill)
+                    tmem_st32(dcol, offs);
 #pragma unroll
-                for (int j = 0; j < 16; j++)
+                for (int j = 0; j < 32; j++)
                     acc[j] = mad_wide(v[j], dgp, acc[j]);
+            } else if (refill) {
+                tmem_st32(dcol, offs);
+            }
+        };
+        auto next_db = [&]() {
+            if (++db_e == kDBufs) {
+                db_e = 0;
+                db_par ^= 1u;
             }
         };
 
@@ -413,36 +446,36 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
                 const int g = g0 + bb;
                 if (g >= G)
                     break;
-                const int sl = g % kSlots, st = g % kStages;
                 const bool refill = g >= kLag && g - kLag + kDBufs < G;
                 if (g >= kLag)
-                    epilogue(g - kLag, d_lag[bb], refill);   // group g - 2 has the same parity as g
+                    epilogue(d_lag[bb], refill);   // group g - 2 has the same parity as g
                 if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
-                    wait(kBarABEmpty + sl, (uint32_t)(g / kSlots - 1) & 1u);
-                wait(kBarMFull + st, (uint32_t)(g / kStages) & 1u);
-                const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(smem + kOffStages + st * kStageBytes +
-                                                                            q * 1024 + (p >> 1) * 512 + lane * 16 +
-                                                                            (p & 1) * 8)
-                                         : make_uint2(0, 0);
+                    wait(kBarABEmpty + sl, sl_par ^ 1u);
+                wait(kBarMFull + st, st_par);
+                const uint4 mw = tile_ok ? *reinterpret_cast<const uint4 *>(mrow + st * kStageBytes)
+                                         : make_uint4(0, 0, 0, 0);
                 {
-                    // words 2(p%2), 2(p%2)+1 of half p/2: group lanes 32p..32p+31 -> columns 16p..16p+15
-                    uint32_t a[16];
+                    // half h of the group: lanes 64h..64h+63 -> columns 32h..32h+31
+                    uint32_t a[32];
                     expand_word(mw.x, a);
                     expand_word(mw.y, a + 8);
-                    tmem_st16(tmem + lane_off + kColA + 64u * (uint32_t)sl + 16u * (uint32_t)p, a);
+                    expand_word(mw.z, a + 16);
+                    expand_word(mw.w, a + 24);
+                    tmem_st32(abase + 64u * (uint32_t)sl, a);
                 }
                 if (x_ok) {
-                    unsigned char *B = smem + kOffB + sl * kBBytes;
+                    unsigned char *B = bdst + sl * kBBytes;
+                    const uint2 ch[4] = {make_uint2(xr[bb][0].x, xr[bb][0].y), make_uint2(xr[bb][0].z, xr[bb][0].w),
+                                         make_uint2(xr[bb][1].x, xr[bb][1].y), make_uint2(xr[bb][1].z, xr[bb][1].w)};
 #pragma unroll
-                    for (int it = 0; it < 2; it++) {
-                        const int c = xc0 + 4 * it;   // chunk: K elements 8c..8c+7 of the group
-                        *reinterpret_cast<uint4 *>(B + (c >> 1) * kKStepBytes + (xn >> 3) * 256 + (c & 1) * 128 +
-                                                   (xn & 7) * 16) = fp16_of_int8x8(xr[bb][it]);
+                    for (int it = 0; it < 4; it++) {
+                        const int c = 4 * c4 + it;   // chunk: K elements 8c..8c+7 of the group
+                        *reinterpret_cast<uint4 *>(B + (c >> 1) * kKStepBytes + (c & 1) * 128) = fp16_of_int8x8(ch[it]);
                     }
                 }
                 const int dg = dr[bb];
                 dsum += (uint64_t)(int64_t)dg;
-                prefetch(bb, g + 2);
+                prefetch(bb);
                 tmem_wait_st();   // A of group g and the refilled D buffer
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 fence_before_sync();
@@ -450,20 +483,32 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
                 if (lane == 0) {
                     mbar_arrive(bar(kBarABFull + sl));
                     if (refill)
-                        mbar_arrive(bar(kBarDEmpty + (g - kLag) % kDBufs));
+                        mbar_arrive(bar(kBarDEmpty + db_e));
                 }
+                if (g >= kLag)
+                    next_db();
                 d_lag[bb] = dg;
+                if (++sl == kSlots) {
+                    sl = 0;
+                    sl_par ^= 1u;
+                }
+                if (++st == kStages) {
+                    st = 0;
+                    st_par ^= 1u;
+                }
             }
         }
-        for (int gp = max(0, G - kLag); gp < G; gp++)
-            epilogue(gp, (gp & 1) ? d_lag[1] : d_lag[0], false);
+        for (int gp = max(0, G - kLag); gp < G; gp++) {
+            epilogue((gp & 1) ? d_lag[1] : d_lag[0], false);
+            next_db();
+        }
 
         // y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64)
         if (epi && tile_ok && row < N) {
             const uint64_t corr = (uint64_t)kOffsetBits * dsum;
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int m = 16 * p + j;
+            for (int j = 0; j < 32; j++) {
+                const int m = 32 * h + j;
                 if (m < M)
                     y[(size_t)m * N + row] = (int64_t)(acc[j] - corr);
             }
