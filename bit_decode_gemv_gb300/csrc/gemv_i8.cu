@@ -19,6 +19,9 @@
 // subtracted (the block-total reuse of integer_engine.md §4.1, computed once
 // per group and shared by every row). Cost: one LOP3 and one dp4a per four
 // weights, plus one broadcast 16-byte shared-memory load per sixteen.
+//
+// This file holds the batch-1 kernel (M = 1) and the entry point; every M > 1
+// runs the tensor-core kernel of gemv_i8_mma.cu.
 
 #include <cuda_runtime.h>
 
@@ -151,104 +154,8 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     }
 }
 
-// ---------------------------------------------------------------------------
-// Small batch (M tokens). One CTA per tile of 32 rows; warp w owns tokens
-// 16w .. 16w + 15 and lane l row 32T + l. K is walked in chunks of KC groups:
-// the chunk's activations for every token go to shared memory, then each
-// thread decodes its row's mask words once per group and reuses them for all
-// of its tokens.
-// ---------------------------------------------------------------------------
-constexpr int kMT = 16;   // tokens per warp
-constexpr int kKC = 4;    // groups per shared-memory chunk
-// From this many tokens on, the tensor-core kernel (gemv_i8_mma.cu) runs.
+// From this many tokens on, tg_gemv_i8 runs the tensor-core kernel (gemv_i8_mma.cu).
 constexpr int kMmaMinTokens = 2;
-
-template <int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
-gemv_i8_mb_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
-                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int M)
-{
-    __shared__ __align__(16) int8_t xs[WARPS * kMT][kKC * 128];
-    __shared__ int tsum[WARPS * kMT][kKC];
-
-    const int tile = blockIdx.x;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int K = G * 128;
-    const int mbase = warp * kMT;
-    const uint4 *tmask = masks + (size_t)tile * G * 64;
-    const int32_t *tscale = scales + (size_t)tile * G * kTileRows;
-
-    int64_t acc[kMT];
-#pragma unroll
-    for (int m = 0; m < kMT; m++)
-        acc[m] = 0;
-
-    for (int c0 = 0; c0 < G; c0 += kKC) {
-        const int cg = min(kKC, G - c0);
-        __syncthreads();
-        // stage x[m][c0*128 .. (c0+cg)*128) for every token
-        const int vec_per_tok = cg * 8;   // uint4 per token
-        for (int i = threadIdx.x; i < M * vec_per_tok; i += WARPS * 32) {
-            const int m = i / vec_per_tok, v = i % vec_per_tok;
-            reinterpret_cast<uint4 *>(xs[m])[v] =
-                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * K + c0 * 128) + v);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < M * cg; i += WARPS * 32) {
-            const int m = i / cg, g = i % cg;
-            int s = 0;
-            for (int b = 0; b < 32; b++)
-                s += tgi::byte_sum_s8(reinterpret_cast<const uint32_t *>(xs[m] + g * 128)[b]);
-            tsum[m][g] = s;
-        }
-        __syncthreads();
-
-        for (int gl = 0; gl < cg; gl++) {
-            const int g = c0 + gl;
-            const uint4 q0 = __ldg(tmask + g * 64 + lane);
-            const uint4 q1 = __ldg(tmask + g * 64 + 32 + lane);
-            const int64_t d = __ldg(tscale + g * kTileRows + lane);
-            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-            uint32_t c[4][8];
-#pragma unroll
-            for (int u = 0; u < 8; u++) {
-                c[0][u] = (w[u] & 0x03030303u) ^ 0x02020202u;
-                c[1][u] = (w[u] & 0x0C0C0C0Cu) ^ 0x08080808u;
-                c[2][u] = (w[u] & 0x30303030u) ^ 0x20202020u;
-                c[3][u] = (w[u] & 0xC0C0C0C0u) ^ 0x80808080u;
-            }
-#pragma unroll
-            for (int mm = 0; mm < kMT; mm++) {
-                const int m = mbase + mm;
-                if (m < M) {
-                    const int8_t *xg = xs[m] + gl * 128;
-                    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-#pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xg + 16 * u);
-                        a0 = dp4a_us(c[0][u], xv.x, a0);
-                        a1 = dp4a_us(c[1][u], xv.y, a1);
-                        a2 = dp4a_us(c[2][u], xv.z, a2);
-                        a3 = dp4a_us(c[3][u], xv.w, a3);
-                    }
-                    const int P = a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6) - 2 * tsum[m][gl];
-                    acc[mm] += d * (int64_t)P;
-                }
-            }
-        }
-    }
-
-    const int row = tile * kTileRows + lane;
-    if (row < N) {
-#pragma unroll
-        for (int mm = 0; mm < kMT; mm++) {
-            const int m = mbase + mm;
-            if (m < M)
-                y[(size_t)m * N + row] = acc[mm];
-        }
-    }
-}
 
 size_t m1_smem_bytes(int G, int warps) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + warps * 32 * 8; }
 
@@ -319,16 +226,9 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
             e = launch_m1<4>(masks, scales, x, y, N, G, tiles, pdl, s);
         if (e != cudaSuccess)
             return TG_ERR_CUDA;
-    } else if (M >= kMmaMinTokens) {
-        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, s);
     } else {
-        const int warps = (int)((M + kMT - 1) / kMT);
-        switch (warps) {
-        case 1: gemv_i8_mb_kernel<1><<<tiles, 32, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
-        case 2: gemv_i8_mb_kernel<2><<<tiles, 64, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
-        case 3: gemv_i8_mb_kernel<3><<<tiles, 96, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
-        default: gemv_i8_mb_kernel<4><<<tiles, 128, 0, s>>>(masks, scales, x, y, N, G, (int)M); break;
-        }
+        static_assert(kMmaMinTokens == 2, "every M > 1 takes the tensor-core kernel");
+        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, s);
     }
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
