@@ -24,21 +24,27 @@
 //     group g+2; then expands its 64 weights of group g (group lanes
 //     64h..64h+63, from the mask ring) to fp16, one byte permute per two
 //     weights, into A slot g%3 in tensor memory (row = lane, K along the
-//     columns), converts four 8-byte activation chunks (loaded two groups
-//     ahead) into B slot g%3 in shared memory, in the canonical K-major layout
-//     of 8-row x 16-byte core matrices, and arrives on the slot's "full"
-//     barrier.
+//     columns), converts four 8-byte activation chunks (from the input ring)
+//     into B slot g%3 in shared memory, in the canonical K-major layout of
+//     8-row x 16-byte core matrices, and arrives on the slot's "full" barrier.
+//     The compute warps issue no global loads at all.
 //   - Two MMA warps take the even and the odd groups. When A/B slot g%3 is full
 //     and D buffer g%4 has been refilled, one thread issues the eight K=16
 //     steps of group g and commits them to the slot's "empty" and the buffer's
 //     "full" barriers. (One thread issues an MMA only every ~70 cycles, so two
 //     issuers keep the tensor core busier.)
-//   - A copy warp bulk-copies (TMA) the mask bytes of group g+8 into the ring
-//     stage group g used, once every compute warp has read it.
+//   - A copy warp fills a 6-deep ring of input stages with bulk and tensor
+//     (TMA) copies: per group the mask bytes and scales of the four tiles and
+//     the 64 x 128 activation box (128-byte swizzle, so the compute warps'
+//     16-byte reads of eight token rows hit eight different bank groups); it
+//     refills the stage of group g with group g+6 once every compute warp has
+//     read it.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "tg.h"
@@ -53,7 +59,7 @@ constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even a
 constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
 constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
 constexpr int kMaxN = 64;                 // tokens, the MMA's N at most
-constexpr int kStages = 8;                // mask ring stages
+constexpr int kStages = 6;                // input ring stages (masks, scales, activations of one group)
 constexpr int kSlots = 3;                 // A/B slots
 constexpr int kDBufs = 4;                 // D buffers
 constexpr int kLag = 2;                   // the epilogue of group g runs after the inputs of group g + kLag
@@ -68,15 +74,19 @@ constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^2
 constexpr int kKStepBytes = (kMaxN / 8) * 256;         // one K=16 step of B: token octets x 256 B
 constexpr int kBBytes = 8 * kKStepBytes;               // one group of B
 constexpr int kOffB = 0;                               // kSlots B slots
-constexpr int kOffStages = kOffB + kSlots * kBBytes;
-constexpr int kStageBytes = 4096;                      // masks of 4 tiles
-// mbarriers: mask stage full, A/B slot full/empty, D buffer full/empty
+constexpr int kOffStages = kOffB + kSlots * kBBytes;   // 1024-aligned: the activation box is swizzled
+constexpr int kStageMask = 0;                          // masks of 4 tiles, 1 KB each
+constexpr int kStageScale = 4096;                      // scales of 4 tiles, 128 B each
+constexpr int kStageX = 5120;                          // activations: 64 tokens x 128 B, 128-byte swizzle
+constexpr int kStageBytes = kStageX + kMaxN * TG_GROUP;
+// mbarriers: input stage full, A/B slot full/empty, D buffer full/empty
 constexpr int kBarMFull = 0, kBarABFull = kStages, kBarABEmpty = kStages + kSlots;
 constexpr int kBarDFull = kStages + 2 * kSlots, kBarDEmpty = kBarDFull + kDBufs, kNumBars = kBarDEmpty + kDBufs;
 constexpr int kOffBar = kOffStages + kStages * kStageBytes;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
-constexpr int kSmemBytes = kOffSlot + 16;
-static_assert(kStageBytes % 16 == 0 && kOffStages % 16 == 0, "bulk copies need 16-byte alignment");
+constexpr int kSmemBytes = kOffSlot + 16 + 1024;   // + slack to align the base to 1024 bytes
+static_assert(kStageBytes % 1024 == 0 && kOffStages % 1024 == 0 && kStageX % 1024 == 0,
+              "bulk copies need 16-byte and the swizzled activation box 1024-byte alignment");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -168,6 +178,16 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
+// 2D tensor (TMA) copy of the box at (x0, y0) of the tensor map into shared
+// memory, completing its bytes on the mbarrier.
+__device__ __forceinline__ void tensor_copy_2d(uint32_t dst, const CUtensorMap *map, int x0, int y0, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x0), "r"(y0), "r"(bar)
+        : "memory");
+}
+
 // Wait for phase `parity` of an mbarrier: one non-blocking test, then
 // suspending waits. Gives up (returns false) after about two seconds of SM
 // clock, or once *abort is set.
@@ -249,14 +269,15 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t *out)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__restrict__ scales,
-                   const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int tiles, int M)
+gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char *__restrict__ scales,
+                   const __grid_constant__ CUtensorMap xmap, int64_t *__restrict__ y, int N, int G, int tiles,
+                   int M)
 {
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ volatile int abort_flag;   // set when a bounded wait gave up
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int K = G * TG_GROUP;
     const uint32_t nmma = (uint32_t)((M + 15) & ~15);
     const int tiles_here = min(4, tiles - (int)blockIdx.x * 4);
 
@@ -302,20 +323,27 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
     };
 
     if (warp == kComputeWarps + kMmaWarps) {
-        // ---------------- copy warp: mask bytes of group g -> stage g % kStages ----------------
-        const uint32_t tx = (uint32_t)tiles_here * 1024u;
-        auto copy_masks = [&](int g) {
+        // ---------------- copy warp: inputs of group g -> stage g % kStages ----------------
+        const uint32_t tx = (uint32_t)tiles_here * (1024u + 128u) + (uint32_t)(kMaxN * TG_GROUP);
+        auto copy_inputs = [&](int g) {
             const int st = g % kStages;
+            const uint32_t sdst = sbase + kOffStages + st * kStageBytes;
+            const uint32_t b = bar(kBarMFull + st);
             if (lane == 0)
-                mbar_expect_tx(bar(kBarMFull + st), tx);
+                mbar_expect_tx(b, tx);
             __syncwarp();
-            if (lane < tiles_here)
-                bulk_copy(sbase + kOffStages + st * kStageBytes + lane * 1024,
-                          masks + ((size_t)(blockIdx.x * 4 + lane) * G + g) * 1024, 1024, bar(kBarMFull + st));
+            if (lane < tiles_here) {
+                const size_t unit = (size_t)(blockIdx.x * 4 + lane) * G + g;
+                bulk_copy(sdst + kStageMask + lane * 1024, masks + unit * 1024, 1024, b);
+                bulk_copy(sdst + kStageScale + lane * 128, scales + unit * 128, 128, b);
+            } else if (lane == 31) {
+                // 64 token rows x 128 bytes of group g (rows from M on read as zero)
+                tensor_copy_2d(sdst + kStageX, &xmap, g * TG_GROUP, 0, b);
+            }
             __syncwarp();
         };
         for (int g = 0; g < min(G, kStages); g++)
-            copy_masks(g);
+            copy_inputs(g);
         for (int g = 0; g + kStages < G; g++) {
             // every compute warp read stage g % kStages before arriving on "full" of group g
             if (lane == 0)
@@ -323,7 +351,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
             __syncwarp();
             if (__shfl_sync(0xffffffffu, abort_flag, 0))
                 break;
-            copy_masks(g + kStages);
+            copy_inputs(g + kStages);
         }
     } else if (warp >= kComputeWarps) {
         // ---------------- MMA warps: groups g = (warp - kComputeWarps) mod 2 ----------------
@@ -356,30 +384,13 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const bool epi = 32 * h < M;   // warp-uniform: this warp's tokens exist
 
-        // activation chunks: token xn, chunks 4c4..4c4+3 (K elements 32c4..32c4+31) of each group
+        // activation chunks: token xn, 16-byte chunks 2c4, 2c4 + 1 (K elements 32c4..32c4+31) of
+        // each group, read from the stage's swizzled box (chunk j of row n sits at chunk j ^ (n & 7))
         const int xn = warp * 8 + (lane & 7);
         const int c4 = lane >> 3;
         const bool x_ok = xn < M;
-        const int8_t *xp = x + (size_t)xn * K + 32 * c4;                       // advances by 128 per group
-        const int32_t *dp = scales + (size_t)tile * G * tgi::kTileRows + lane;   // advances by 32 per group
-        uint4 xr[2][2];
-        int dr[2] = {0, 0};
-        int pf_left = G;   // groups not yet prefetched
-        auto prefetch = [&](int bb) {
-            if (pf_left > 0) {
-                if (x_ok) {
-                    xr[bb][0] = __ldg(reinterpret_cast<const uint4 *>(xp));
-                    xr[bb][1] = __ldg(reinterpret_cast<const uint4 *>(xp) + 1);
-                }
-                if (tile_ok)
-                    dr[bb] = __ldg(dp);
-                xp += TG_GROUP;
-                dp += tgi::kTileRows;
-                pf_left--;
-            }
-        };
-        prefetch(0);
-        prefetch(1);
+        const int xoff0 = kStageX + xn * TG_GROUP + (((2 * c4) ^ (xn & 7)) << 4);
+        const int xoff1 = kStageX + xn * TG_GROUP + (((2 * c4 + 1) ^ (xn & 7)) << 4);
 
         uint32_t offs[32];   // the offset 1.5 * 2^23 in every accumulator column
 #pragma unroll
@@ -409,7 +420,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
         uint32_t sl_par = 0, st_par = 0;  // phase parities of those uses
         int db_e = 0;                    // D buffer of group g - kLag
         uint32_t db_par = 0;
-        const unsigned char *mrow = smem + kOffStages + q * 1024 + h * 512 + lane * 16;
+        const unsigned char *mrow = smem + kOffStages + kStageMask + q * 1024 + h * 512 + lane * 16;
+        const unsigned char *srow = smem + kOffStages + kStageScale + q * 128 + lane * 4;
+        const unsigned char *xrow = smem + kOffStages;
         const uint32_t abase = tmem + lane_off + kColA + 32u * (uint32_t)h;
         unsigned char *bdst = smem + kOffB + warp * 256 + (lane & 7) * 16;   // + slot, + chunk position
 
@@ -442,7 +455,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
 #pragma unroll 1
         for (int g0 = 0; g0 < G; g0 += 2) {
 #pragma unroll
-            for (int bb = 0; bb < 2; bb++) {   // g & 1: register buffer of the prefetched inputs, static
+            for (int bb = 0; bb < 2; bb++) {   // g & 1: which scale history register, static
                 const int g = g0 + bb;
                 if (g >= G)
                     break;
@@ -465,17 +478,18 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const int32_t *__res
                 }
                 if (x_ok) {
                     unsigned char *B = bdst + sl * kBBytes;
-                    const uint2 ch[4] = {make_uint2(xr[bb][0].x, xr[bb][0].y), make_uint2(xr[bb][0].z, xr[bb][0].w),
-                                         make_uint2(xr[bb][1].x, xr[bb][1].y), make_uint2(xr[bb][1].z, xr[bb][1].w)};
+                    const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes + xoff0);
+                    const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes + xoff1);
+                    const uint2 ch[4] = {make_uint2(x0.x, x0.y), make_uint2(x0.z, x0.w), make_uint2(x1.x, x1.y),
+                                         make_uint2(x1.z, x1.w)};
 #pragma unroll
                     for (int it = 0; it < 4; it++) {
                         const int c = 4 * c4 + it;   // chunk: K elements 8c..8c+7 of the group
                         *reinterpret_cast<uint4 *>(B + (c >> 1) * kKStepBytes + (c & 1) * 128) = fp16_of_int8x8(ch[it]);
                     }
                 }
-                const int dg = dr[bb];
+                const int dg = tile_ok ? *reinterpret_cast<const int *>(srow + st * kStageBytes) : 0;
                 dsum += (uint64_t)(int64_t)dg;
-                prefetch(bb);
                 tmem_wait_st();   // A of group g and the refilled D buffer
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 fence_before_sync();
@@ -529,16 +543,45 @@ namespace tgi {
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
                 int tiles, int M, cudaStream_t s)
 {
-    static bool attr_set = false;   // set once per process; idempotent if raced
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv_i8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-            return TG_ERR_CUDA;
-        attr_set = true;
+    // cuTensorMapEncodeTiled from the driver, looked up once
+    using encode_fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static std::mutex mu;
+    static encode_fn encode = nullptr;
+    static bool attr_set = false;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return TG_ERR_CUDA;
+            encode = reinterpret_cast<encode_fn>(fn);
+        }
+        if (!attr_set) {
+            if (cudaFuncSetAttribute(gemv_i8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+                cudaSuccess)
+                return TG_ERR_CUDA;
+            attr_set = true;
+        }
     }
+    // x as a 2D tensor [M rows][K bytes]; boxes of 64 rows x 128 bytes, 128-byte swizzle
+    CUtensorMap xmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)G * TG_GROUP, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)G * TG_GROUP};
+    const cuuint32_t box[2] = {TG_GROUP, kMaxN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return TG_ERR_CUDA;
     const int grid = (tiles + 3) / 4;
-    gemv_i8_mma_kernel<<<grid, kThreads, kSmemBytes, s>>>(reinterpret_cast<const unsigned char *>(masks), scales,
-                                                         x, y, N, G, tiles, M);
+    gemv_i8_mma_kernel<<<grid, kThreads, kSmemBytes, s>>>(reinterpret_cast<const unsigned char *>(masks),
+                                                         reinterpret_cast<const unsigned char *>(scales), xmap, y,
+                                                         N, G, tiles, M);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
