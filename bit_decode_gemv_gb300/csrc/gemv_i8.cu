@@ -230,7 +230,7 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
             return TG_ERR_CUDA;
     } else {
         static_assert(kMmaMinTokens == 2, "every M > 1 takes the tensor-core kernel");
-        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, s);
+        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale, s);
     }
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

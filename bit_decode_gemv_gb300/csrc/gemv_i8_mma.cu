@@ -15,16 +15,16 @@
 // (checked on the host).
 //
 // Mapping. A CTA owns 128 rows (four 32-row mask tiles) for all groups and all
-// tokens. 8 compute warps, two MMA warps and a copy warp hand work to each other through
+// tokens. 16 compute warps, two MMA warps and a copy warp hand work to each other through
 // mbarrier rings, with no CTA-wide barrier inside the group loop.
 //   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
-//     rows of mask tile w%4) and handles half h = w/4. In its iteration for
+//     rows of mask tile w%4) and handles part p = w/4. In its iteration for
 //     group g it first reads back group g-2's D buffer for tokens
-//     32h..32h+31, accumulates it, and refills that buffer with the offset for
-//     group g+2; then expands its 64 weights of group g (group lanes
-//     64h..64h+63, from the mask ring) to fp16, one byte permute per two
+//     16p..16p+15, accumulates it, and refills that buffer with the offset for
+//     group g+2; then expands its 32 weights of group g (group lanes
+//     32p..32p+31, from the input ring) to fp16, one byte permute per two
 //     weights, into A slot g%3 in tensor memory (row = lane, K along the
-//     columns), converts four 8-byte activation chunks (from the input ring)
+//     columns), converts two 8-byte activation chunks (from the input ring)
 //     into B slot g%3 in shared memory, in the canonical K-major layout of
 //     8-row x 16-byte core matrices, and arrives on the slot's "full" barrier.
 //     The compute warps issue no global loads at all.
@@ -38,7 +38,7 @@
 //     the 64 x 128 activation box (128-byte swizzle, so the compute warps'
 //     16-byte reads of eight token rows hit eight different bank groups); it
 //     refills the stage of group g with group g+6 once every compute warp has
-//     read it.
+//     arrived on that stage's "empty" barrier.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -54,7 +54,7 @@ TGI_DEFINE_DEVICE_ERROR(gemv_mma_take_device_error)
 
 namespace {
 
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 16;   // 4 row quarters x 4 parts (32 weights and 16 tokens each)
 constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd groups)
 constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
 constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
@@ -79,10 +79,13 @@ constexpr int kStageMask = 0;                          // masks of 4 tiles, 1 KB
 constexpr int kStageScale = 4096;                      // scales of 4 tiles, 128 B each
 constexpr int kStageX = 5120;                          // activations: 64 tokens x 128 B, 128-byte swizzle
 constexpr int kStageBytes = kStageX + kMaxN * TG_GROUP;
-// mbarriers: input stage full, A/B slot full/empty, D buffer full/empty
-constexpr int kBarMFull = 0, kBarABFull = kStages, kBarABEmpty = kStages + kSlots;
-constexpr int kBarDFull = kStages + 2 * kSlots, kBarDEmpty = kBarDFull + kDBufs, kNumBars = kBarDEmpty + kDBufs;
-constexpr int kOffBar = kOffStages + kStages * kStageBytes;
+// mbarriers: input stage full/empty, A/B slot full/empty, D buffer full/empty. Every
+// waiter of a barrier is also needed for that barrier's next phase to complete, so no
+// waiter can see a phase completed twice over (which would make it wait forever).
+constexpr int kBarMFull = 0, kBarMEmpty = kStages, kBarABFull = 2 * kStages, kBarABEmpty = 2 * kStages + kSlots;
+constexpr int kBarDFull = 2 * kStages + 2 * kSlots, kBarDEmpty = kBarDFull + kDBufs, kNumBars = kBarDEmpty + kDBufs;
+constexpr int kOffAcc = kOffStages + kStages * kStageBytes;   // int64 accumulators [token][row]
+constexpr int kOffBar = kOffAcc + kMaxN * kRowsPerCta * 8;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;   // + slack to align the base to 1024 bytes
 static_assert(kStageBytes % 1024 == 0 && kOffStages % 1024 == 0 && kStageX % 1024 == 0,
@@ -128,30 +131,36 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 lanes x 32 columns: thread i writes its v[0..31] into lane (taddr.lane + i).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+// 32 lanes x 16 columns: thread i writes its v[0..15] into lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
 {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16};"
         ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
-// 32 lanes x 32 columns: thread i reads lane (taddr.lane + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+// 32 lanes x 16 columns, every column of thread i's lane set to v.
+__device__ __forceinline__ void tmem_st16_same(uint32_t taddr, uint32_t v)
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
+        "%1, %1};"
+        ::"r"(taddr), "r"(v)
+        : "memory");
+}
+
+// 32 lanes x 16 columns: thread i reads lane (taddr.lane + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15}, [%16];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          "=r"(v[15])
         : "r"(taddr)
         : "memory");
 }
@@ -268,6 +277,15 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t *out)
     }
 }
 
+// kNarrow: every |d| <= kNarrowMaxScale, so kBlock groups of exact P * d sum
+// below 2^31 in magnitude: the fold is one wrapping 32-bit multiply-add per
+// value and a 64-bit flush every kBlock groups. Otherwise one 64-bit wide
+// multiply-add per value.
+constexpr int kBlock = 4;
+constexpr int64_t kNarrowMaxScale = 32767;   // 4 * 2^14 * 32767 < 2^31
+static_assert((int64_t)kBlock * 16384 * kNarrowMaxScale < ((int64_t)1 << 31), "narrow fold bound");
+
+template <bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char *__restrict__ scales,
                    const __grid_constant__ CUtensorMap xmap, int64_t *__restrict__ y, int N, int G, int tiles,
@@ -286,13 +304,17 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     auto *slot = reinterpret_cast<volatile uint32_t *>(smem + kOffSlot);
 
-    // --- set-up: zero the B slots (tokens M.. stay zero), barriers, TMEM
+    // --- set-up: zero the B slots (tokens M.. stay zero) and the accumulators, barriers, TMEM
     for (int i = tid; i < kOffStages / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < kMaxN * kRowsPerCta * 8 / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + kOffAcc)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         abort_flag = 0;
-        for (int i = 0; i < kStages; i++)
+        for (int i = 0; i < kStages; i++) {
             mbar_init(bar(kBarMFull + i), 1);
+            mbar_init(bar(kBarMEmpty + i), kComputeWarps);
+        }
         for (int i = 0; i < kSlots; i++) {
             mbar_init(bar(kBarABFull + i), kComputeWarps);
             mbar_init(bar(kBarABEmpty + i), 1);
@@ -345,9 +367,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         for (int g = 0; g < min(G, kStages); g++)
             copy_inputs(g);
         for (int g = 0; g + kStages < G; g++) {
-            // every compute warp read stage g % kStages before arriving on "full" of group g
+            // every compute warp has read stage g % kStages
             if (lane == 0)
-                wait(kBarABFull + g % kSlots, (uint32_t)(g / kSlots) & 1u);
+                wait(kBarMEmpty + g % kStages, (uint32_t)(g / kStages) & 1u);
             __syncwarp();
             if (__shfl_sync(0xffffffffu, abort_flag, 0))
                 break;
@@ -377,30 +399,27 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         __syncwarp();
     } else {
         // ---------------- compute warps ----------------
-        const int q = warp & 3, h = warp >> 2;
+        const int q = warp & 3, p = warp >> 2;
         const int tile = blockIdx.x * 4 + q;
         const bool tile_ok = tile < tiles;
         const int row = tile * tgi::kTileRows + lane;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const bool epi = 32 * h < M;   // warp-uniform: this warp's tokens exist
+        const bool epi = 16 * p < M;   // warp-uniform: this warp's tokens exist
+        // int64 accumulators of tokens 16p + j (j = 0..15) for this row: [token][row] layout, + 128 j
+        int64_t *accs = reinterpret_cast<int64_t *>(smem + kOffAcc) + 16 * p * kRowsPerCta + 32 * q + lane;
 
-        // activation chunks: token xn, 16-byte chunks 2c4, 2c4 + 1 (K elements 32c4..32c4+31) of
-        // each group, read from the stage's swizzled box (chunk j of row n sits at chunk j ^ (n & 7))
-        const int xn = warp * 8 + (lane & 7);
-        const int c4 = lane >> 3;
+        // activation chunk: token xn, 16-byte chunk j16 (K elements 16 j16 .. 16 j16 + 15) of each
+        // group, read from the stage's swizzled box (chunk j of row n sits at chunk j ^ (n & 7))
+        const int xn = (warp & 7) * 8 + (lane & 7);
+        const int j16 = 4 * (warp >> 3) + (lane >> 3);
         const bool x_ok = xn < M;
-        const int xoff0 = kStageX + xn * TG_GROUP + (((2 * c4) ^ (xn & 7)) << 4);
-        const int xoff1 = kStageX + xn * TG_GROUP + (((2 * c4 + 1) ^ (xn & 7)) << 4);
+        const int xoff = kStageX + xn * TG_GROUP + ((j16 ^ (xn & 7)) << 4);
 
-        uint32_t offs[32];   // the offset 1.5 * 2^23 in every accumulator column
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-            offs[j] = kOffsetBits;
-        // D buffers of groups 0..kDBufs-1 start at the offset
-        const uint32_t dbase = tmem + lane_off + kColD + 32u * (uint32_t)h;
+        // D buffers of groups 0..kDBufs-1 start at the offset 1.5 * 2^23
+        const uint32_t dbase = tmem + lane_off + kColD + 16u * (uint32_t)p;
 #pragma unroll 1
         for (int db = 0; db < kDBufs; db++)
-            tmem_st32(dbase + (uint32_t)(kMaxN * db), offs);
+            tmem_st16_same(dbase + (uint32_t)(kMaxN * db), kOffsetBits);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
@@ -408,23 +427,40 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             for (int db = 0; db < kDBufs; db++)
                 mbar_arrive(bar(kBarDEmpty + db));
 
-        uint64_t acc[32];
+        uint32_t acc32[16];    // narrow fold: the current block of groups, wrapping
 #pragma unroll
-        for (int j = 0; j < 32; j++)
-            acc[j] = 0;
-        uint64_t dsum = 0;
+        for (int j = 0; j < 16; j++)
+            acc32[j] = 0;
+        uint64_t dsum = 0;     // wide fold: sum_g d, for the offset correction
+        uint32_t dblk = 0;     // narrow fold: sum of the block's d (wrapping)
+        int nblk = 0;
+        // narrow fold: the block's exact sum of P * d is acc32 - 0x4B400000 * dblk modulo 2^32,
+        // and its magnitude is below 2^31, so the int32 reading of that difference is exact
+        auto flush = [&]() {
+            const uint32_t c = kOffsetBits * dblk;
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                accs[128 * j] += (int64_t)(int32_t)(acc32[j] - c);
+                acc32[j] = 0;
+            }
+            dblk = 0;
+            nblk = 0;
+        };
         int d_lag[2] = {0, 0};   // scale of group g, kept for its epilogue kLag groups later
 
         // ring positions of group g, advanced by counters
-        int sl = 0, st = 0;              // A/B slot, mask stage
+        int sl = 0, st = 0;              // A/B slot, input stage
         uint32_t sl_par = 0, st_par = 0;  // phase parities of those uses
         int db_e = 0;                    // D buffer of group g - kLag
         uint32_t db_par = 0;
-        const unsigned char *mrow = smem + kOffStages + kStageMask + q * 1024 + h * 512 + lane * 16;
+        // this thread's 32 weights: group lanes 32p..32p+31 = words 2(p%2), 2(p%2)+1 of half p/2
+        const unsigned char *mrow = smem + kOffStages + kStageMask + q * 1024 + (p >> 1) * 512 + lane * 16 +
+                                    (p & 1) * 8;
         const unsigned char *srow = smem + kOffStages + kStageScale + q * 128 + lane * 4;
-        const unsigned char *xrow = smem + kOffStages;
-        const uint32_t abase = tmem + lane_off + kColA + 32u * (uint32_t)h;
-        unsigned char *bdst = smem + kOffB + warp * 256 + (lane & 7) * 16;   // + slot, + chunk position
+        const unsigned char *xrow = smem + kOffStages + xoff;
+        const uint32_t abase = tmem + lane_off + kColA + 16u * (uint32_t)p;
+        // B position of chunks 2 j16 and 2 j16 + 1 of token xn: K-step j16, core matrices 0 and 1
+        unsigned char *bdst = smem + kOffB + j16 * kKStepBytes + (xn >> 3) * 256 + (xn & 7) * 16;
 
         // read back group gp's D buffer (db_e), accumulate, and refill it with the offset
         auto epilogue = [&](int dgp, bool refill) {
@@ -432,16 +468,25 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             fence_after_sync();
             const uint32_t dcol = dbase + (uint32_t)(kMaxN * db_e);
             if (epi) {
-                uint32_t v[32];
-                tmem_ld32(dcol, v);
+                uint32_t v[16];
+                tmem_ld16(dcol, v);
                 tmem_wait_ld();
                 if (refill)
-                    tmem_st32(dcol, offs);
+                    tmem_st16_same(dcol, kOffsetBits);
+                if (kNarrow) {
 #pragma unroll
-                for (int j = 0; j < 32; j++)
-                    acc[j] = mad_wide(v[j], dgp, acc[j]);
+                    for (int j = 0; j < 16; j++)
+                        acc32[j] += v[j] * (uint32_t)dgp;
+                    dblk += (uint32_t)dgp;
+                    if (++nblk == kBlock)
+                        flush();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j++)
+                        accs[128 * j] = (int64_t)mad_wide(v[j], dgp, (uint64_t)accs[128 * j]);
+                }
             } else if (refill) {
-                tmem_st32(dcol, offs);
+                tmem_st16_same(dcol, kOffsetBits);
             }
         };
         auto next_db = [&]() {
@@ -465,28 +510,19 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
                     wait(kBarABEmpty + sl, sl_par ^ 1u);
                 wait(kBarMFull + st, st_par);
-                const uint4 mw = tile_ok ? *reinterpret_cast<const uint4 *>(mrow + st * kStageBytes)
-                                         : make_uint4(0, 0, 0, 0);
+                const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes)
+                                         : make_uint2(0, 0);
                 {
-                    // half h of the group: lanes 64h..64h+63 -> columns 32h..32h+31
-                    uint32_t a[32];
+                    uint32_t a[16];
                     expand_word(mw.x, a);
                     expand_word(mw.y, a + 8);
-                    expand_word(mw.z, a + 16);
-                    expand_word(mw.w, a + 24);
-                    tmem_st32(abase + 64u * (uint32_t)sl, a);
+                    tmem_st16(abase + 64u * (uint32_t)sl, a);
                 }
                 if (x_ok) {
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes);
                     unsigned char *B = bdst + sl * kBBytes;
-                    const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes + xoff0);
-                    const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes + xoff1);
-                    const uint2 ch[4] = {make_uint2(x0.x, x0.y), make_uint2(x0.z, x0.w), make_uint2(x1.x, x1.y),
-                                         make_uint2(x1.z, x1.w)};
-#pragma unroll
-                    for (int it = 0; it < 4; it++) {
-                        const int c = 4 * c4 + it;   // chunk: K elements 8c..8c+7 of the group
-                        *reinterpret_cast<uint4 *>(B + (c >> 1) * kKStepBytes + (c & 1) * 128) = fp16_of_int8x8(ch[it]);
-                    }
+                    *reinterpret_cast<uint4 *>(B) = fp16_of_int8x8(make_uint2(xv.x, xv.y));
+                    *reinterpret_cast<uint4 *>(B + 128) = fp16_of_int8x8(make_uint2(xv.z, xv.w));
                 }
                 const int dg = tile_ok ? *reinterpret_cast<const int *>(srow + st * kStageBytes) : 0;
                 dsum += (uint64_t)(int64_t)dg;
@@ -495,6 +531,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
+                    mbar_arrive(bar(kBarMEmpty + st));   // this warp is done with input stage st
                     mbar_arrive(bar(kBarABFull + sl));
                     if (refill)
                         mbar_arrive(bar(kBarDEmpty + db_e));
@@ -516,15 +553,16 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             epilogue((gp & 1) ? d_lag[1] : d_lag[0], false);
             next_db();
         }
-
-        // y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64)
+        if (kNarrow && epi)
+            flush();
+        // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); narrow: acc_m
         if (epi && tile_ok && row < N) {
-            const uint64_t corr = (uint64_t)kOffsetBits * dsum;
+            const uint64_t corr = kNarrow ? 0ull : (uint64_t)kOffsetBits * dsum;
 #pragma unroll
-            for (int j = 0; j < 32; j++) {
-                const int m = 32 * h + j;
+            for (int j = 0; j < 16; j++) {
+                const int m = 16 * p + j;
                 if (m < M)
-                    y[(size_t)m * N + row] = (int64_t)(acc[j] - corr);
+                    y[(size_t)m * N + row] = (int64_t)((uint64_t)accs[128 * j] - corr);
             }
         }
     }
@@ -541,7 +579,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
 namespace tgi {
 
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                int tiles, int M, cudaStream_t s)
+                int tiles, int M, int64_t max_abs_scale, cudaStream_t s)
 {
     // cuTensorMapEncodeTiled from the driver, looked up once
     using encode_fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -550,6 +588,7 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
     static std::mutex mu;
     static encode_fn encode = nullptr;
     static bool attr_set = false;
+    const bool narrow = max_abs_scale <= kNarrowMaxScale;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!encode) {
@@ -562,8 +601,10 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
             encode = reinterpret_cast<encode_fn>(fn);
         }
         if (!attr_set) {
-            if (cudaFuncSetAttribute(gemv_i8_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(gemv_i8_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes) != cudaSuccess ||
+                cudaFuncSetAttribute(gemv_i8_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes) != cudaSuccess)
                 return TG_ERR_CUDA;
             attr_set = true;
         }
@@ -579,9 +620,12 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return TG_ERR_CUDA;
     const int grid = (tiles + 3) / 4;
-    gemv_i8_mma_kernel<<<grid, kThreads, kSmemBytes, s>>>(reinterpret_cast<const unsigned char *>(masks),
-                                                         reinterpret_cast<const unsigned char *>(scales), xmap, y,
-                                                         N, G, tiles, M);
+    const auto *mk = reinterpret_cast<const unsigned char *>(masks);
+    const auto *sc = reinterpret_cast<const unsigned char *>(scales);
+    if (narrow)
+        gemv_i8_mma_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M);
+    else
+        gemv_i8_mma_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

@@ -155,3 +155,19 @@ def test_extreme_values_batched(M):
     x[0] = -128
     x[-1] = 127
     check(dict(t=t, d=d, x=x))
+
+
+@pytest.mark.parametrize("M", [2, 64])
+def test_narrow_fold_at_its_bound(M):
+    """Scales at |d| = 32767 (the largest the 32-bit block fold of the batched
+    kernel accepts) with every group sum at |P| = 2^14: four groups of P * d sum
+    to 4 * 2^14 * 32767, just inside int32, with both signs."""
+    N, K = 160, 1024
+    t = -np.ones((N, K), np.int8)
+    t[N // 2:] = 1
+    d = np.full((N, K // 128), 32767, np.int32)
+    d[::3] = -32767
+    d[1::7, 2] = 1
+    x = np.full((M, K), -128, np.int8)
+    x[M // 2:, ::2] = 127
+    check(dict(t=t, d=d, x=x))
