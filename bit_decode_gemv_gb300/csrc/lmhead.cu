@@ -59,12 +59,14 @@ constexpr uint64_t kSignBit = 0x8000000000000000ull;
 // Workspace: a region cleared at the start of every call, then per-row data.
 struct Ws {
     unsigned long long *count;   // candidates appended
-    unsigned *hist_row;          // [kHistBins] scores of every row
-    unsigned *hist_cand;         // [kHistBins] exact scores of the candidates
+    unsigned *hist_row;          // [kHistWords] scores of every row (fine bins, then coarse)
+    unsigned *hist_cand;         // [kHistWords] exact scores of the candidates
     int64_t *s1;                 // [N] stage-1 sums (two-stage path)
     uint64_t *cand;              // [N] candidate keys, sign bit flipped (unsigned order)
 };
-constexpr size_t kClearedBytes = 256 + 2 * (size_t)kHistBins * sizeof(unsigned);
+constexpr int kCoarseBins = kHistBins / 64;   // coarse level: 64 fine bins each
+constexpr int kHistWords = kHistBins + kCoarseBins;   // one histogram: fine bins, then coarse bins
+constexpr size_t kClearedBytes = 256 + 2 * (size_t)kHistWords * sizeof(unsigned);
 
 __device__ __forceinline__ uint64_t to_ordered(int64_t v) { return (uint64_t)v ^ kSignBit; }
 __device__ __forceinline__ int64_t from_ordered(uint64_t u) { return (int64_t)(u ^ kSignBit); }
@@ -90,24 +92,32 @@ __device__ __forceinline__ int64_t bin_edge(int b)
     return (int64_t)(64 + (t & 63)) << (t / 64 - 1);
 }
 
+// Count one score: its fine bin and the coarse bin above it.
+__device__ __forceinline__ void count_score(unsigned *hist, int64_t score)
+{
+    const int b = score_bin(score);
+    atomicAdd(hist + b, 1u);
+    atomicAdd(hist + kHistBins + (b >> 6), 1u);
+}
+
 // Lower edge of the bin that holds the k-th largest counted score, found by
-// one warp from the top of the histogram in two levels (32 ranges of 192
-// bins, then the chosen range as 32 runs of 6), every level's loads issued
-// together. INT64_MIN if fewer than k scores were counted.
+// one warp from the top of the histogram in two levels -- the 96 coarse bins
+// (three per lane), then the 64 fine bins of the chosen coarse bin (two per
+// lane) -- each level one round of loads. The counts are read through L2,
+// where other CTAs' atomics land. INT64_MIN if fewer than k scores were
+// counted.
 __device__ int64_t warp_kth_bin_edge(const unsigned *hist, int k)
 {
-    constexpr int per = kHistBins / 32;              // 192 bins per lane
-    constexpr int run = per / 32;                    // 6 bins per lane in level 2
+    static_assert(kCoarseBins == 3 * 32, "three coarse bins per lane");
     const int lane = threadIdx.x & 31;
+    const unsigned kk = (unsigned)k;
 
-    // level 1: lane l owns bins [top - per, top) with top = kHistBins - per * l
-    const int top = kHistBins - per * lane;
-    const uint4 *h4 = reinterpret_cast<const uint4 *>(hist + top - per);
-    unsigned mine = 0;
-#pragma unroll 8
-    for (int j = 0; j < per / 4; j++) {
-        const uint4 v = h4[j];
-        mine += v.x + v.y + v.z + v.w;
+    // level 1: lane l owns coarse bins 95 - 3l, 94 - 3l, 93 - 3l (top down)
+    unsigned c[3], mine = 0;
+#pragma unroll
+    for (int i = 0; i < 3; i++) {
+        c[i] = __ldcg(hist + kHistBins + kCoarseBins - 1 - (3 * lane + i));
+        mine += c[i];
     }
     unsigned incl = mine;
 #pragma unroll
@@ -116,21 +126,30 @@ __device__ int64_t warp_kth_bin_edge(const unsigned *hist, int k)
         if (lane >= o)
             incl += v;
     }
-    unsigned owner = __ballot_sync(0xffffffffu, incl - mine < (unsigned)k && (unsigned)k <= incl);
+    int cb = -1;               // coarse bin holding the k-th score
+    unsigned before = 0;       // scores above that coarse bin
+    if (incl - mine < kk && kk <= incl) {
+        unsigned cum = incl - mine;
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            if (cb < 0 && cum + c[i] >= kk) {
+                cb = kCoarseBins - 1 - (3 * lane + i);
+                before = cum;
+            }
+            cum += c[i];
+        }
+    }
+    unsigned owner = __ballot_sync(0xffffffffu, cb >= 0);
     if (!owner)
         return INT64_MIN;
-    int src = __ffs(owner) - 1;
-    const unsigned before1 = __shfl_sync(0xffffffffu, incl - mine, src);
-    const int top1 = kHistBins - per * src;
+    const int src = __ffs(owner) - 1;
+    cb = __shfl_sync(0xffffffffu, cb, src);
+    before = __shfl_sync(0xffffffffu, before, src);
 
-    // level 2: lane j owns bins [top1 - run*(j+1), top1 - run*j)
-    const int top2 = top1 - run * lane;
-    unsigned c[run], mine2 = 0;
-#pragma unroll
-    for (int i = 0; i < run; i++) {
-        c[i] = hist[top2 - 1 - i];
-        mine2 += c[i];
-    }
+    // level 2: lane l owns fine bins 64 cb + 63 - 2l and 64 cb + 62 - 2l (top down)
+    const int top = 64 * cb + 63 - 2 * lane;
+    const unsigned f0 = __ldcg(hist + top), f1 = __ldcg(hist + top - 1);
+    const unsigned mine2 = f0 + f1;
     unsigned incl2 = mine2;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -138,31 +157,29 @@ __device__ int64_t warp_kth_bin_edge(const unsigned *hist, int k)
         if (lane >= o)
             incl2 += v;
     }
-    const unsigned start2 = before1 + incl2 - mine2;
+    const unsigned start2 = before + incl2 - mine2;
     int found = -1;
-    if (start2 < (unsigned)k && (unsigned)k <= before1 + incl2) {
-        unsigned cum = start2;
-#pragma unroll
-        for (int i = 0; i < run; i++) {
-            if (found < 0 && cum + c[i] >= (unsigned)k)
-                found = top2 - 1 - i;
-            cum += c[i];
-        }
-    }
+    if (start2 < kk && kk <= before + incl2)
+        found = start2 + f0 >= kk ? top : top - 1;
     owner = __ballot_sync(0xffffffffu, found >= 0);
     found = __shfl_sync(0xffffffffu, found, __ffs(owner) - 1);
     return bin_edge(found);
 }
 
-// sum_i |x_i| computed by warp 0 (|v| = v * (v < 0 ? -1 : 1) per byte in one dp4a).
-__device__ __forceinline__ int64_t warp_sum_abs(const int8_t *x, int K)
+// sum_i |x_i| from the warp's register copy of x (chunk lane + 32 j in xr[j],
+// zero past the end): |v| = v * (v < 0 ? -1 : 1) per byte in one dp4a.
+template <int CPL>
+__device__ __forceinline__ int64_t warp_sum_abs_regs(const uint4 (&xr)[CPL])
 {
-    const int lane = threadIdx.x & 31;
     int sa = 0;
-    for (int i = lane; i < K / 4; i += 32) {
-        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x) + i);
-        const uint32_t neg = (v & 0x80808080u) >> 7;
-        sa = dp4a_ss(v, (neg * 0xFEu) | 0x01010101u, sa);
+#pragma unroll
+    for (int j = 0; j < CPL; j++) {
+        const uint32_t w[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t neg = (w[i] & 0x80808080u) >> 7;
+            sa = dp4a_ss(w[i], (neg * 0xFEu) | 0x01010101u, sa);
+        }
     }
     return (int64_t)tgi::warp_sum_i32(sa);
 }
@@ -205,20 +222,13 @@ __global__ void __launch_bounds__(kScanWarps * 32)
 lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
                   const uint8_t *__restrict__ m, const int8_t *__restrict__ x, Ws ws, int N, int K)
 {
-    __shared__ int64_t sh_sum_abs;
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
-    if (threadIdx.x < 32) {
-        const int64_t sa = warp_sum_abs(x, K);
-        if (lane == 0)
-            sh_sum_abs = sa;
-    }
-    __syncthreads();
-    const int64_t sum_abs = sh_sum_abs;
+    const int64_t sum_abs = warp_sum_abs_regs<CPL>(xr);
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += 2 * NW) {
@@ -241,7 +251,7 @@ lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
         }
     }
     if (lane == 0 && best != INT64_MIN)
-        atomicAdd(&ws.hist_row[score_bin(best)], 1u);
+        count_score(ws.hist_row, best);
 }
 
 // Full path: exact logits from both digit groups; each warp counts its largest.
@@ -271,7 +281,7 @@ lmh_full_kernel(const int8_t *__restrict__ hi, const int8_t *__restrict__ lo,
         }
     }
     if (lane == 0 && best != INT64_MIN)
-        atomicAdd(&ws.hist_row[score_bin(best)], 1u);
+        count_score(ws.hist_row, best);
 }
 
 // Append this lane's key (if `take`) to the candidate list, one atomic per
@@ -289,7 +299,7 @@ __device__ __forceinline__ void append_key(Ws ws, bool take, uint64_t key, int64
     base = __shfl_sync(0xffffffffu, base, leader);
     if (take) {
         ws.cand[base + __popc(mask & ((1u << lane) - 1))] = key;
-        atomicAdd(&ws.hist_cand[score_bin(score)], 1u);
+        count_score(ws.hist_cand, score);
     }
 }
 
@@ -300,23 +310,15 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
                    const uint8_t *__restrict__ m, const int8_t *__restrict__ x, Ws ws, int N, int K,
                    int k, int idx_bits)
 {
-    __shared__ int64_t sh[2];
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
-    if (threadIdx.x < 32) {
-        const int64_t sa = warp_sum_abs(x, K);
-        const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
-        if (lane == 0) {
-            sh[0] = sa;
-            sh[1] = tau;
-        }
-    }
-    __syncthreads();
-    const int64_t sum_abs = sh[0], tau = sh[1];
+    // every warp derives the bound's sum |x| and the threshold itself: no block barrier
+    const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
+    const int64_t sum_abs = warp_sum_abs_regs<CPL>(xr);
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
 
     for (int base = wg * 32; base < N; base += NW * 32) {
@@ -599,7 +601,7 @@ Ws carve(void *ws, int64_t N)
     Ws w;
     w.count = reinterpret_cast<unsigned long long *>(p);
     w.hist_row = reinterpret_cast<unsigned *>(p + 256);
-    w.hist_cand = w.hist_row + kHistBins;
+    w.hist_cand = w.hist_row + kHistWords;
     size_t off = kClearedBytes;
     w.s1 = reinterpret_cast<int64_t *>(p + off);
     off += align256((size_t)N * 8);
