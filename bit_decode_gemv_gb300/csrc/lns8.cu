@@ -142,6 +142,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     __shared__ int acc[kRows][8];                  // int32 phase partials of this CTA's groups
     __shared__ int stage[kRows + kMaxCluster][8];  // partials of the rows this CTA owns, per source CTA
     __shared__ int gcorr[kWarps][16][8];           // class-sum corrections of clamped lanes, per warp row
+    __shared__ int64_t arow[kRows][8];             // int64 A of the rows this CTA owns
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -278,31 +279,32 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         remote[((rank * slice) + (rl - dst * slice)) * 8 + p] = acc[rl][p];
     }
     cluster.sync();
-    for (int b = 0; b < slice * 8; b += blockDim.x) {   // uniform over the block: shuffles below see full warps
-        const int item = b + tid;
+    // A: the owner sums its slice's partials in rank order
+    const int rows_here = min(slice, kRows - rank * slice);   // rows of this CTA's slice (last slice may be short)
+    for (int item = tid; item < rows_here * 8; item += blockDim.x) {
         const int i = item >> 3, p = item & 7;
-        const int rl = rank * slice + i;
-        const int row = blockIdx.x * kRows + rl;
-        const bool valid = item < slice * 8 && rl < kRows && row < N;
+        const int row = blockIdx.x * kRows + rank * slice + i;
         int64_t a = 0;
-        if (valid)
-            for (int src = 0; src < csize; src++)
+#pragma unroll
+        for (int src = 0; src < kMaxCluster; src++)
+            if (src < csize)
                 a += stage[src * slice + i][p];
-        if (valid)
+        arow[i][p] = a;
+        if (row < N)
             A[(size_t)row * 8 + p] = a;
-        if (S) {
-            // S in the order p = 0..7: lane p == 0 of each 8-lane row gathers the products
-            double fp = F.f[0];
+    }
+    if (S) {
+        // S: one thread per row, the eight terms in the order p = 0..7
+        __syncthreads();
+        for (int i = tid; i < rows_here; i += blockDim.x) {
+            const int row = blockIdx.x * kRows + rank * slice + i;
+            if (row < N) {
+                double sum = 0.0;
 #pragma unroll
-            for (int pp = 1; pp < 8; pp++)
-                fp = p == pp ? F.f[pp] : fp;   // selects keep F in parameter space
-            const double prod = __dmul_rn((double)a, fp);
-            double sum = 0.0;
-#pragma unroll
-            for (int pp = 0; pp < 8; pp++)
-                sum = __dadd_rn(sum, __shfl_sync(0xffffffffu, prod, (lane & ~7) | pp));
-            if (valid && p == 0)
+                for (int p = 0; p < 8; p++)
+                    sum = __dadd_rn(sum, __dmul_rn((double)arow[i][p], F.f[p]));
                 S[row] = __dmul_rn(sum, 0x1p-9);
+            }
         }
     }
 }
