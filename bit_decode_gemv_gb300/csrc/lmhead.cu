@@ -540,13 +540,25 @@ lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32
     }
     __syncthreads();
     const int64_t tau = sh_tau;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const uint64_t u = ws.cand[i];
-        if ((from_ordered(u) >> idx_bits) >= tau) {
-            const int slot = atomicAdd(&nsel, 1);
-            if (slot < kFilterMax)
-                sel[slot] = u;
-        }
+    // warp-aggregated appends: one shared atomic per warp, not per key
+    auto append_sel = [&](bool take, uint64_t u) {
+        const unsigned mask = __ballot_sync(0xffffffffu, take);
+        if (!mask)
+            return;
+        const int lane = threadIdx.x & 31;
+        const int leader = __ffs(mask) - 1;
+        int base = 0;
+        if (lane == leader)
+            base = atomicAdd(&nsel, __popc(mask));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        const int slot = base + __popc(mask & ((1u << lane) - 1));
+        if (take && slot < kFilterMax)
+            sel[slot] = u;
+    };
+    for (int b = 0; b < n; b += blockDim.x) {   // uniform over the block: full warps in append_sel
+        const int i = b + threadIdx.x;
+        const uint64_t u = i < n ? ws.cand[i] : 0ull;
+        append_sel(i < n && (from_ordered(u) >> idx_bits) >= tau, u);
     }
     __syncthreads();
     int m = nsel;
@@ -556,13 +568,10 @@ lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32
         if (threadIdx.x == 0)
             nsel = 0;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const uint64_t u = ws.cand[i];
-            if (u >= t) {
-                const int slot = atomicAdd(&nsel, 1);
-                if (slot < kFilterMax)
-                    sel[slot] = u;
-            }
+        for (int b = 0; b < n; b += blockDim.x) {
+            const int i = b + threadIdx.x;
+            const uint64_t u = i < n ? ws.cand[i] : 0ull;
+            append_sel(i < n && u >= t, u);
         }
         __syncthreads();
         m = nsel < kFilterMax ? nsel : kFilterMax;
