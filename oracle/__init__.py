@@ -30,6 +30,8 @@ def lib():
             "oracle_gemv_i8": [i64, i64, i64, p, p, p, p],
             "oracle_gemv_i8_masked": [i64, i64, i64, p, p, p, p],
             "oracle_gemv_i8_stateset": [i64, i64, i64, p, p, p, p],
+            "oracle_gemv_i8_frac": [i64, i64, i64, p, p, p, C.c_int, p],
+            "oracle_gemv_q1": [i64, i64, i64, p, p, p, C.c_int, p],
             "oracle_lns8_direct": [i64, i64, p, p, p, p],
             "oracle_lns8_histogram": [i64, i64, p, p, p, p],
             "oracle_lns8_tile64": [i64, i64, p, p, p, p],
@@ -84,6 +86,40 @@ def _gemv(fn_name, t, d, x):
 def gemv_i8(t, d, x):
     """y[m][r] = sum_g d[r,g] * sum_{i in g} t[r,i] x[m,i]  -> int64 [M][N]."""
     return _gemv("oracle_gemv_i8", t, d, x)
+
+
+def gemv_i8_frac(t, d, x, frac):
+    """y[m][r] = sum_g arshift(d[r,g] * sum_{i in g} t[r,i] x[m,i], frac) -> int64 [M][N]
+    (integer engine §4.2 with the per-group floor)."""
+    t, pt = _c(t, np.int8)
+    d, pd = _c(d, np.int32)
+    x = np.atleast_2d(x)
+    x, px = _c(x, np.int8)
+    N, K = t.shape
+    M = x.shape[0]
+    if x.shape[1] != K or d.shape != (N, K // 128):
+        raise ValueError("shape mismatch")
+    y = np.zeros((M, N), dtype=np.int64)
+    _check(lib().oracle_gemv_i8_frac(M, N, K, pt, pd, px, int(frac), y.ctypes.data_as(C.c_void_p)),
+           "oracle_gemv_i8_frac")
+    return y
+
+
+def gemv_q1(bits, d, x, frac=0):
+    """Q1_0 (integer engine §4.1): bits [N][K] in {0,1} for sign -1/+1;
+    y[m][r] = sum_g arshift((2 pos_sum - block_total) * d[r,g], frac)."""
+    b, pb = _c(bits, np.uint8)
+    d, pd = _c(d, np.int32)
+    x = np.atleast_2d(x)
+    x, px = _c(x, np.int8)
+    N, K = b.shape
+    M = x.shape[0]
+    if x.shape[1] != K or d.shape != (N, K // 128):
+        raise ValueError("shape mismatch")
+    y = np.zeros((M, N), dtype=np.int64)
+    _check(lib().oracle_gemv_q1(M, N, K, pb, pd, px, int(frac), y.ctypes.data_as(C.c_void_p)),
+           "oracle_gemv_q1")
+    return y
 
 
 def gemv_i8_masked(t, d, x):

@@ -19,7 +19,9 @@
  *
  * Readings taken where the pages leave a step open (each is listed with its
  * reason in the design notes):
- *   - per-group arshift(., frac) of [IntEngine] §4.1/§4.2 is taken with frac = 0;
+ *   - per-group arshift(., frac) of [IntEngine] §4.1/§4.2 is floor division by
+ *     2^frac of each group's scaled sum; the main apply functions take frac = 0
+ *     and the *_frac functions take it as an argument;
  *   - K must be a multiple of 128 (the group size); other K is rejected;
  *   - LNS8 product code k = a + d - 74: k <= 0 is exact zero, k > 127 saturates
  *     to 127; an activation with code 0 is zero whatever its sign bit;
@@ -77,6 +79,89 @@ int oracle_gemv_i8(int64_t M, int64_t N, int64_t K, const int8_t *t,
                 for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++)
                     signed_sum += (int64_t)t[r * K + i] * (int64_t)x[m * K + i];
                 out += (int64_t)d[r * G + g] * signed_sum;
+            }
+            y[m * N + r] = out;
+        }
+    }
+    return 0;
+}
+
+/*
+ * arshift(v, s) of [IntEngine] §4.1: an arithmetic right shift, i.e. floor
+ * division by 2^s (rounding toward minus infinity), written with C's
+ * truncating division so that it does not rest on how the compiler shifts a
+ * negative number. 0 <= s <= 62.
+ */
+static int64_t oracle_arshift(int64_t v, int s)
+{
+    const int64_t p = (int64_t)1 << s;
+    int64_t q = v / p;
+    if (v % p != 0 && v < 0)
+        q -= 1;
+    return q;
+}
+
+/*
+ * [IntEngine] §4.2 with the per-group floor: for every output o
+ *   out_o = sum_b arshift( signed_sum_b * scale[o][b], frac ),
+ *   signed_sum_b = (sum over the +1 weights of x) - (sum over the -1 weights of x).
+ * t in {-1, 0, 1}; layouts as oracle_gemv_i8.
+ */
+int oracle_gemv_i8_frac(int64_t M, int64_t N, int64_t K, const int8_t *t,
+                        const int32_t *d, const int8_t *x, int frac, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0 || frac < 0 || frac > 62)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            int64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                int64_t plus = 0, minus = 0;
+                for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++) {
+                    if (t[r * K + i] == 1)
+                        plus += x[m * K + i];
+                    else if (t[r * K + i] == -1)
+                        minus += x[m * K + i];
+                    else if (t[r * K + i] != 0)
+                        return -1;
+                }
+                out += oracle_arshift((plus - minus) * (int64_t)d[r * G + g], frac);
+            }
+            y[m * N + r] = out;
+        }
+    }
+    return 0;
+}
+
+/*
+ * [IntEngine] §4.1 Q1_0: 1-bit weights, bit[r][i] in {0, 1} standing for
+ * sign -1 / +1, and for every output o
+ *   signed_sum_b = 2 * pos_sum_b - block_total_b,
+ *   pos_sum_b = sum of x over the weights whose bit is 1,
+ *   block_total_b = sum of x over the group (the same for every output),
+ *   out_o = sum_b arshift( signed_sum_b * scale[o][b], frac ).
+ * Layouts: bits [N][K] uint8 in {0, 1}; d [N][K/128] int32; x [M][K] int8.
+ */
+int oracle_gemv_q1(int64_t M, int64_t N, int64_t K, const uint8_t *bits,
+                   const int32_t *d, const int8_t *x, int frac, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0 || frac < 0 || frac > 62)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            int64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                int64_t pos_sum = 0, block_total = 0;
+                for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++) {
+                    if (bits[r * K + i] > 1)
+                        return -1;
+                    block_total += x[m * K + i];
+                    if (bits[r * K + i] == 1)
+                        pos_sum += x[m * K + i];
+                }
+                out += oracle_arshift((2 * pos_sum - block_total) * (int64_t)d[r * G + g], frac);
             }
             y[m * N + r] = out;
         }

@@ -411,3 +411,89 @@ def test_stage1_bound_is_tight():
     _, _, lo, hi, _ = oracle.lmhead_two_stage(planes, s, x, 2)
     assert logits[1] == hi[1] and logits[4] == lo[4]
     assert hi[1] - lo[1] == 2 * int(s[1]) * 40 * int(np.abs(x.astype(np.int64)).sum())
+
+
+# ---------------------------------------------------------------------------
+# Per-group floor (integer engine §4.1/§4.2 arshift(., frac)) and Q1_0 binary
+# weights (integer engine §4.1)
+# ---------------------------------------------------------------------------
+
+def test_frac_zero_is_the_plain_apply():
+    w = W.tiny(seed=3, N=40, K=384, M=3)
+    np.testing.assert_array_equal(oracle.gemv_i8_frac(w["t"], w["d"], w["x"], 0),
+                                  oracle.gemv_i8(w["t"], w["d"], w["x"]))
+
+
+def test_frac_floors_toward_minus_infinity():
+    # one group, one nonzero lane: the group's scaled sum is -5 or +5
+    K = 128
+    t = np.zeros((2, K), np.int8)
+    t[0, 7] = -1
+    t[1, 7] = 1
+    d = np.ones((2, 1), np.int32)
+    x = np.zeros((1, K), np.int8)
+    x[0, 7] = 5
+    y = oracle.gemv_i8_frac(t, d, x, 1)
+    assert y[0, 0] == -3 and y[0, 1] == 2          # floor(-2.5) = -3, floor(2.5) = 2
+    y = oracle.gemv_i8_frac(t, d, x, 3)
+    assert y[0, 0] == -1 and y[0, 1] == 0          # floor(-5/8) = -1, floor(5/8) = 0
+
+
+def test_frac_floor_is_per_group():
+    # two groups whose scaled sums are each 1: floor(1/2) + floor(1/2) = 0, while
+    # flooring after the sum would give floor(2/2) = 1
+    K = 256
+    t = np.zeros((1, K), np.int8)
+    t[0, 0] = 1
+    t[0, 128] = 1
+    d = np.ones((1, 2), np.int32)
+    x = np.zeros((1, K), np.int8)
+    x[0, 0] = 1
+    x[0, 128] = 1
+    assert oracle.gemv_i8_frac(t, d, x, 1)[0, 0] == 0
+    assert oracle.gemv_i8_frac(t, d, x, 0)[0, 0] == 2
+
+
+def test_frac_matches_a_floor_division_of_each_group():
+    w = W.tiny(seed=8, N=17, K=512, M=2)
+    for frac in (1, 5, 13, 31):
+        y = oracle.gemv_i8_frac(w["t"], w["d"], w["x"], frac)
+        G = 4
+        parts = np.stack([oracle.gemv_i8(w["t"][:, 128 * g:128 * (g + 1)], w["d"][:, g:g + 1],
+                                         w["x"][:, 128 * g:128 * (g + 1)]) for g in range(G)])
+        # python integers: // is floor division
+        ref = np.array([[sum(int(parts[g, m, r]) // (1 << frac) for g in range(G)) for r in range(17)]
+                        for m in range(2)], dtype=np.int64)
+        np.testing.assert_array_equal(y, ref)
+
+
+def test_q1_two_pos_minus_total_equals_signed_sum():
+    # the page's identity 2 * pos_sum - block_total = sum sign * x, checked against
+    # the ternary apply on the same +-1 weights
+    rng = np.random.default_rng(9)
+    N, K, M = 23, 640, 3
+    bits = rng.integers(0, 2, size=(N, K)).astype(np.uint8)
+    signs = (2 * bits.astype(np.int16) - 1).astype(np.int8)
+    d = rng.integers(-(1 << 15), 1 << 15, size=(N, K // 128)).astype(np.int32)
+    x = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    for frac in (0, 4):
+        np.testing.assert_array_equal(oracle.gemv_q1(bits, d, x, frac), oracle.gemv_i8_frac(signs, d, x, frac))
+    # and the plain matrix product for frac = 0
+    ref = np.zeros((M, N), np.int64)
+    for g in range(K // 128):
+        sl = slice(128 * g, 128 * (g + 1))
+        ref += (x[:, sl].astype(np.int64) @ signs[:, sl].T.astype(np.int64)) * d[:, g].astype(np.int64)
+    np.testing.assert_array_equal(oracle.gemv_q1(bits, d, x, 0), ref)
+
+
+def test_q1_special_cases():
+    K = 256
+    x = np.arange(-64, 192, dtype=np.int64).astype(np.int8).reshape(1, K)
+    d = np.array([[3, -2]], np.int32)
+    total = [int(x[0, :128].astype(np.int64).sum()), int(x[0, 128:].astype(np.int64).sum())]
+    ones = np.ones((1, K), np.uint8)
+    zeros = np.zeros((1, K), np.uint8)
+    assert oracle.gemv_q1(ones, d, x)[0, 0] == 3 * total[0] - 2 * total[1]       # every sign +1
+    assert oracle.gemv_q1(zeros, d, x)[0, 0] == -3 * total[0] + 2 * total[1]     # every sign -1
+    with pytest.raises(ValueError):
+        oracle.gemv_q1(np.full((1, K), 2, np.uint8), d, x)
