@@ -30,6 +30,7 @@ TG_ERR_DEVICE = -7
 TG_TERNARY_I8 = 1
 TG_TERNARY_LNS8 = 2
 TG_PLANES8 = 3
+TG_BINARY_Q1 = 4
 
 TG_GROUP = 128
 TG_MAX_M = 64
@@ -62,7 +63,8 @@ class tg_layout(C.Structure):
         ("aux2_off", C.c_int64), ("aux2_bytes", C.c_int64),
         ("total_bytes", C.c_int64), ("max_abs_scale", C.c_int64),
         ("flags", C.c_int64),
-        ("reserved", C.c_int64 * 3),
+        ("frac", C.c_int64),
+        ("reserved", C.c_int64 * 2),
     ]
 
 
@@ -147,8 +149,8 @@ def tg_packed_bytes(kind: int, N: int, K: int) -> int:
 def tg_pack_weights(kind: int, trits: np.ndarray, scales: np.ndarray):
     """Pack host weights; returns (uint8 host blob, tg_layout).
 
-    trits: int8 [N][K] (ternary kinds) or [8][N][K] (TG_PLANES8).
-    scales: int32 [N][K/128] (TG_TERNARY_I8), uint8 [N][K/128] (TG_TERNARY_LNS8),
+    trits: int8 [N][K] (ternary kinds; -1/+1 for TG_BINARY_Q1) or [8][N][K] (TG_PLANES8).
+    scales: int32 [N][K/128] (TG_TERNARY_I8, TG_BINARY_Q1), uint8 [N][K/128] (TG_TERNARY_LNS8),
     int32 [N] (TG_PLANES8).
     """
     trits = np.ascontiguousarray(trits, dtype=np.int8)

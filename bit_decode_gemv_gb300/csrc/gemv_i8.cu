@@ -20,6 +20,10 @@
 // per group and shared by every row). Cost: one LOP3 and one dp4a per four
 // weights, plus one broadcast 16-byte shared-memory load per sixteen.
 //
+// Binary Q1_0 weights (integer_engine.md §4.1) take the same path with one
+// sign bit per weight (see group_pos_q1). Each group's scaled sum is floored
+// by 2^frac on its own (§4.1/§4.2 arshift) before the sum over groups.
+//
 // This file holds the batch-1 kernel (M = 1) and the entry point; every M > 1
 // runs the tensor-core kernel of gemv_i8_mma.cu.
 
@@ -63,6 +67,31 @@ __device__ __forceinline__ int group_dot_t2(const uint32_t w[8], const int8_t *x
     return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
 }
 
+// Q1_0 (integer_engine.md §4.1): sum of x over the +1 weights of one 128-lane
+// group for one row. w[0..3] are the row's four words; word u holds lanes
+// 32u + 4j + b in bit 8b + j. Masking bit j of every byte in place,
+// w & (0x01010101 << j), gives four unsigned bytes 2^j * [weight is +1], and
+// one dp4a against the four activations 32u + 4j .. 32u + 4j + 3 accumulates
+// 2^j times their positive part; each column sum is shifted back exactly.
+__device__ __forceinline__ int group_pos_q1(const uint32_t w[4], const int8_t *xg)
+{
+    int a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(xg + 32 * u);
+        const uint4 hi = *reinterpret_cast<const uint4 *>(xg + 32 * u + 16);
+        const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            a[j] = dp4a_us(w[u] & (0x01010101u << j), xv[j], a[j]);
+    }
+    int pos = 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+        pos += a[j] >> j;
+    return pos;
+}
+
 // ---------------------------------------------------------------------------
 // Batch 1. One CTA per tile of 32 rows; lane l of every warp owns row 32T + l;
 // the CTA's W warps split the row's groups (warp w takes g = w, w + W, ...;
@@ -77,11 +106,12 @@ __device__ __forceinline__ int group_dot_t2(const uint32_t w[8], const int8_t *x
 // with several GEMVs' loads, and triggering after the compute, which leaves
 // the memory idle between GEMVs.)
 // ---------------------------------------------------------------------------
-template <int GPW>
+template <int GPW, bool kQ1>
 __global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
 gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
-                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G)
+                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac)
 {
+    constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
     extern __shared__ __align__(16) unsigned char smem[];
     int8_t *xs = reinterpret_cast<int8_t *>(smem);                   // [G*128]
     int *tsum = reinterpret_cast<int *>(smem + G * 128);             // [G]
@@ -91,7 +121,7 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     const int nwarps = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint4 *tmask = masks + (size_t)tile * G * 64;               // 64 uint4 per (tile, group)
+    const uint4 *tmask = masks + (size_t)tile * G * kChunks;
     const int32_t *tscale = scales + (size_t)tile * G * kTileRows;
 
     uint4 m0[GPW], m1[GPW];
@@ -101,8 +131,8 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         for (int j = 0; j < GPW; j++) {
             const int g = g0 + j * nwarps;
             if (g < G) {
-                m0[j] = tgi::ldg_stream(tmask + g * 64 + lane);
-                m1[j] = tgi::ldg_stream(tmask + g * 64 + 32 + lane);
+                m0[j] = tgi::ldg_stream(tmask + g * kChunks + lane);
+                m1[j] = kQ1 ? make_uint4(0, 0, 0, 0) : tgi::ldg_stream(tmask + g * kChunks + 32 + lane);
                 dg[j] = __ldg(tscale + g * kTileRows + lane);
             } else {
                 m0[j] = m1[j] = make_uint4(0, 0, 0, 0);
@@ -132,10 +162,17 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         for (int j = 0; j < GPW; j++) {
             const int g = g0 + j * nwarps;
             if (g < G) {
-                const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
-                                       m1[j].x, m1[j].y, m1[j].z, m1[j].w};
-                const int P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
-                acc += (int64_t)dg[j] * (int64_t)P;
+                int P;
+                if (kQ1) {
+                    // 2 * pos_sum - block_total
+                    const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                    P = 2 * group_pos_q1(w, xs + g * 128) - tsum[g];
+                } else {
+                    const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                           m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                    P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
+                }
+                acc += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
             }
         }
         g0 += nwarps * GPW;
@@ -161,11 +198,11 @@ constexpr int kMmaMinTokens = 2;
 
 size_t m1_smem_bytes(int G, int warps) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + warps * 32 * 8; }
 
-template <int GPW>
+template <int GPW, bool kQ1>
 cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
-                      int G, int tiles, bool pdl, cudaStream_t s)
+                      int G, int tiles, int frac, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_i8_m1_kernel<GPW>;
+    auto kern = gemv_i8_m1_kernel<GPW, kQ1>;
     const int max_warps = GPW >= 4 ? 16 : 32;
     int warps = (G + GPW - 1) / GPW;
     if (warps > max_warps)
@@ -186,7 +223,7 @@ cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G);
+    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, frac);
 }
 
 }  // namespace
@@ -196,7 +233,9 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
 {
     if (!L || !w || !x || !y)
         return TG_ERR_ARG;
-    if (L->kind != TG_TERNARY_I8 || L->version != 1)
+    if ((L->kind != TG_TERNARY_I8 && L->kind != TG_BINARY_Q1) || L->version != 1)
+        return TG_ERR_ARG;
+    if (L->frac < 0 || L->frac > 62)
         return TG_ERR_ARG;
     if (!tgi::aligned(w, 256) || !tgi::aligned(x, 16) || !tgi::aligned(y, 8))
         return TG_ERR_ARG;
@@ -219,18 +258,29 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         const bool pdl = (L->flags & TG_FLAG_CONST_WEIGHTS) != 0;
         // One group per warp up to K = 4096 (32 warps), then two per warp up to
         // K = 8192; beyond that 16 warps loop over batches of four groups each.
+        const int frac = (int)L->frac;
         cudaError_t e;
-        if (G <= 32)
-            e = launch_m1<1>(masks, scales, x, y, N, G, tiles, pdl, s);
-        else if (G <= 64)
-            e = launch_m1<2>(masks, scales, x, y, N, G, tiles, pdl, s);
-        else
-            e = launch_m1<4>(masks, scales, x, y, N, G, tiles, pdl, s);
+        if (L->kind == TG_BINARY_Q1) {
+            if (G <= 32)
+                e = launch_m1<1, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+            else if (G <= 64)
+                e = launch_m1<2, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+            else
+                e = launch_m1<4, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+        } else {
+            if (G <= 32)
+                e = launch_m1<1, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+            else if (G <= 64)
+                e = launch_m1<2, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+            else
+                e = launch_m1<4, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+        }
         if (e != cudaSuccess)
             return TG_ERR_CUDA;
     } else {
         static_assert(kMmaMinTokens == 2, "every M > 1 takes the tensor-core kernel");
-        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale, s);
+        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale,
+                                L->kind == TG_BINARY_Q1, (int)L->frac, s);
     }
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

@@ -277,20 +277,42 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t *out)
     }
 }
 
-// kNarrow: every |d| <= kNarrowMaxScale, so kBlock groups of exact P * d sum
-// below 2^31 in magnitude: the fold is one wrapping 32-bit multiply-add per
-// value and a 64-bit flush every kBlock groups. Otherwise one 64-bit wide
-// multiply-add per value.
+// Q1_0: expand one word of sign bits (lane 4j + b in bit 8b + j, set for +1)
+// into 8 fp16 pairs, out[2j] = lanes 4j, 4j + 1 and out[2j + 1] = lanes
+// 4j + 2, 4j + 3. Selector nibbles 1 and 3 are 1 + 2 * bit: table byte 1 is
+// 0xBC (-1: 0xBC00), byte 3 is 0x3C (+1: 0x3C00), byte 0 the zero low byte.
+__device__ __forceinline__ void expand_word_q1(uint32_t w, uint32_t *out)
+{
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const uint32_t s01 = ((j <= 5 ? w << (5 - j) : w >> (j - 5)) & 0x2020u) | 0x1010u;   // bits j, 8 + j
+        const uint32_t s23 = ((w >> (11 + j)) & 0x2020u) | 0x1010u;                          // bits 16 + j, 24 + j
+        out[2 * j] = __byte_perm(0x3C00BC00u, 0u, s01);
+        out[2 * j + 1] = __byte_perm(0x3C00BC00u, 0u, s23);
+    }
+}
+
+// Folds of a group's accumulator bits (0x4B400000 + P) into the outputs:
+// kFoldNarrow: frac = 0 and every |d| <= kNarrowMaxScale, so kBlock groups of
+//   exact P * d sum below 2^31 in magnitude: one wrapping 32-bit multiply-add
+//   per value and a 64-bit flush every kBlock groups;
+// kFoldWide: frac = 0, larger scales: one 64-bit multiply-add per value and
+//   0x4B400000 * sum_g d subtracted at the end;
+// kFoldFloor: frac > 0: each group's P * d is floored by 2^frac on its own
+//   (integer_engine.md §4.1/§4.2 arshift) before it is added.
+constexpr int kFoldNarrow = 0, kFoldWide = 1, kFoldFloor = 2;
 constexpr int kBlock = 4;
 constexpr int64_t kNarrowMaxScale = 32767;   // 4 * 2^14 * 32767 < 2^31
 static_assert((int64_t)kBlock * 16384 * kNarrowMaxScale < ((int64_t)1 << 31), "narrow fold bound");
 
-template <bool kNarrow>
+template <bool kQ1, int kFold>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char *__restrict__ scales,
                    const __grid_constant__ CUtensorMap xmap, int64_t *__restrict__ y, int N, int G, int tiles,
-                   int M)
+                   int M, int frac)
 {
+    constexpr bool kNarrow = kFold == kFoldNarrow;
+    constexpr uint32_t kMaskBytes = kQ1 ? 512u : 1024u;   // mask bytes of one (tile, group)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ volatile int abort_flag;   // set when a bounded wait gave up
@@ -346,7 +368,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
 
     if (warp == kComputeWarps + kMmaWarps) {
         // ---------------- copy warp: inputs of group g -> stage g % kStages ----------------
-        const uint32_t tx = (uint32_t)tiles_here * (1024u + 128u) + (uint32_t)(kMaxN * TG_GROUP);
+        const uint32_t tx = (uint32_t)tiles_here * (kMaskBytes + 128u) + (uint32_t)(kMaxN * TG_GROUP);
         auto copy_inputs = [&](int g) {
             const int st = g % kStages;
             const uint32_t sdst = sbase + kOffStages + st * kStageBytes;
@@ -356,7 +378,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             __syncwarp();
             if (lane < tiles_here) {
                 const size_t unit = (size_t)(blockIdx.x * 4 + lane) * G + g;
-                bulk_copy(sdst + kStageMask + lane * 1024, masks + unit * 1024, 1024, b);
+                bulk_copy(sdst + kStageMask + lane * 1024, masks + unit * kMaskBytes, kMaskBytes, b);
                 bulk_copy(sdst + kStageScale + lane * 128, scales + unit * 128, 128, b);
             } else if (lane == 31) {
                 // 64 token rows x 128 bytes of group g (rows from M on read as zero)
@@ -454,8 +476,10 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         int db_e = 0;                    // D buffer of group g - kLag
         uint32_t db_par = 0;
         // this thread's 32 weights: group lanes 32p..32p+31 = words 2(p%2), 2(p%2)+1 of half p/2
-        const unsigned char *mrow = smem + kOffStages + kStageMask + q * 1024 + (p >> 1) * 512 + lane * 16 +
-                                    (p & 1) * 8;
+        // Q1: word p of the row's 16 bytes (group lanes 32p..32p+31)
+        const unsigned char *mrow = kQ1 ? smem + kOffStages + kStageMask + q * 1024 + lane * 16 + 4 * p
+                                        : smem + kOffStages + kStageMask + q * 1024 + (p >> 1) * 512 + lane * 16 +
+                                              (p & 1) * 8;
         const unsigned char *srow = smem + kOffStages + kStageScale + q * 128 + lane * 4;
         const unsigned char *xrow = smem + kOffStages + xoff;
         const uint32_t abase = tmem + lane_off + kColA + 16u * (uint32_t)p;
@@ -480,10 +504,16 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                     dblk += (uint32_t)dgp;
                     if (++nblk == kBlock)
                         flush();
-                } else {
+                } else if (kFold == kFoldWide) {
 #pragma unroll
                     for (int j = 0; j < 16; j++)
                         accs[128 * j] = (int64_t)mad_wide(v[j], dgp, (uint64_t)accs[128 * j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const int32_t P = (int32_t)(v[j] - kOffsetBits);
+                        accs[128 * j] += ((int64_t)P * dgp) >> frac;   // the group's floor
+                    }
                 }
             } else if (refill) {
                 tmem_st16_same(dcol, kOffsetBits);
@@ -510,12 +540,17 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
                     wait(kBarABEmpty + sl, sl_par ^ 1u);
                 wait(kBarMFull + st, st_par);
-                const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes)
-                                         : make_uint2(0, 0);
                 {
                     uint32_t a[16];
-                    expand_word(mw.x, a);
-                    expand_word(mw.y, a + 8);
+                    if (kQ1) {
+                        const uint32_t mw = tile_ok ? *reinterpret_cast<const uint32_t *>(mrow + st * kStageBytes) : 0u;
+                        expand_word_q1(mw, a);
+                    } else {
+                        const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes)
+                                                 : make_uint2(0, 0);
+                        expand_word(mw.x, a);
+                        expand_word(mw.y, a + 8);
+                    }
                     tmem_st16(abase + 64u * (uint32_t)sl, a);
                 }
                 if (x_ok) {
@@ -555,9 +590,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         }
         if (kNarrow && epi)
             flush();
-        // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); narrow: acc_m
+        // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); otherwise acc_m
         if (epi && tile_ok && row < N) {
-            const uint64_t corr = kNarrow ? 0ull : (uint64_t)kOffsetBits * dsum;
+            const uint64_t corr = kFold == kFoldWide ? (uint64_t)kOffsetBits * dsum : 0ull;
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const int m = 16 * p + j;
@@ -579,7 +614,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
 namespace tgi {
 
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                int tiles, int M, int64_t max_abs_scale, cudaStream_t s)
+                int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s)
 {
     // cuTensorMapEncodeTiled from the driver, looked up once
     using encode_fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -588,7 +623,7 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
     static std::mutex mu;
     static encode_fn encode = nullptr;
     static bool attr_set = false;
-    const bool narrow = max_abs_scale <= kNarrowMaxScale;
+    const int fold = frac > 0 ? kFoldFloor : max_abs_scale <= kNarrowMaxScale ? kFoldNarrow : kFoldWide;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!encode) {
@@ -601,11 +636,14 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
             encode = reinterpret_cast<encode_fn>(fn);
         }
         if (!attr_set) {
-            if (cudaFuncSetAttribute(gemv_i8_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemBytes) != cudaSuccess ||
-                cudaFuncSetAttribute(gemv_i8_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemBytes) != cudaSuccess)
-                return TG_ERR_CUDA;
+            void (*kernels[6])(const unsigned char *, const unsigned char *, const CUtensorMap, int64_t *, int, int,
+                               int, int, int) = {
+                gemv_i8_mma_kernel<false, kFoldNarrow>, gemv_i8_mma_kernel<false, kFoldWide>,
+                gemv_i8_mma_kernel<false, kFoldFloor>,  gemv_i8_mma_kernel<true, kFoldNarrow>,
+                gemv_i8_mma_kernel<true, kFoldWide>,    gemv_i8_mma_kernel<true, kFoldFloor>};
+            for (auto k : kernels)
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+                    return TG_ERR_CUDA;
             attr_set = true;
         }
     }
@@ -622,10 +660,23 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
     const int grid = (tiles + 3) / 4;
     const auto *mk = reinterpret_cast<const unsigned char *>(masks);
     const auto *sc = reinterpret_cast<const unsigned char *>(scales);
-    if (narrow)
-        gemv_i8_mma_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M);
-    else
-        gemv_i8_mma_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M);
+#define TGI_MMA_LAUNCH(Q, F) gemv_i8_mma_kernel<Q, F><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M, frac)
+    if (q1) {
+        if (fold == kFoldNarrow)
+            TGI_MMA_LAUNCH(true, kFoldNarrow);
+        else if (fold == kFoldWide)
+            TGI_MMA_LAUNCH(true, kFoldWide);
+        else
+            TGI_MMA_LAUNCH(true, kFoldFloor);
+    } else {
+        if (fold == kFoldNarrow)
+            TGI_MMA_LAUNCH(false, kFoldNarrow);
+        else if (fold == kFoldWide)
+            TGI_MMA_LAUNCH(false, kFoldWide);
+        else
+            TGI_MMA_LAUNCH(false, kFoldFloor);
+    }
+#undef TGI_MMA_LAUNCH
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

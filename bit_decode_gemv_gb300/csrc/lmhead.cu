@@ -650,7 +650,7 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
 {
     if (!L || !w || !x || !argmax || !ids || !scores)
         return TG_ERR_ARG;
-    if (L->kind != TG_PLANES8 || L->version != 1)
+    if (L->kind != TG_PLANES8 || L->version != 1 || L->frac != 0)
         return TG_ERR_ARG;
     if (!tgi::aligned(w, 256) || !tgi::aligned(x, 16) || (logits && !tgi::aligned(logits, 8)) ||
         !tgi::aligned(argmax, 4) || !tgi::aligned(ids, 4) || !tgi::aligned(scores, 8) ||

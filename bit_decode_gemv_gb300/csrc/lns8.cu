@@ -316,7 +316,7 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
 {
     if (!L || !w || !xa || !A)
         return TG_ERR_ARG;
-    if (L->kind != TG_TERNARY_LNS8 || L->version != 1)
+    if (L->kind != TG_TERNARY_LNS8 || L->version != 1 || L->frac != 0)
         return TG_ERR_ARG;
     if (!tgi::aligned(w, 256) || !tgi::aligned(xa, 16) || !tgi::aligned(A, 8) ||
         (S && !tgi::aligned(S, 8)))

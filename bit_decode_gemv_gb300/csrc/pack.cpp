@@ -4,6 +4,8 @@
 //  * ternary rows as the W_nonzero / W_negative bitmask pair (BitState brief
 //    §4), two bits per weight, interleaved so that one 32-bit word yields four
 //    lanes per byte-masked extract and one warp reads 512 contiguous bytes;
+//  * binary Q1_0 rows (integer_engine.md §4.1) as one sign bit per weight,
+//    interleaved the same way (one 16-byte chunk per row and group);
 //  * the 8 base-3 planes of the lm_head (SKaiNET issue #337, BITNET_PLANES)
 //    as two balanced base-3 digit groups of four planes, one byte per weight
 //    each, plus the row's own bound on the planes 4-7 residual.
@@ -64,7 +66,7 @@ extern "C" const char *tg_status_string(int status)
     case TG_OK: return "ok";
     case TG_ERR_ARG: return "invalid argument (null or misaligned pointer, unknown kind, wrong layout)";
     case TG_ERR_SHAPE: return "invalid shape (N, K, M or k out of range)";
-    case TG_ERR_VALUE: return "invalid value (trit outside {-1,0,1} or row scale <= 0)";
+    case TG_ERR_VALUE: return "invalid value (trit outside {-1,0,1}, binary weight not -1/+1, or row scale <= 0)";
     case TG_ERR_BOUND: return "integer bound exceeded: a worst-case sum could overflow";
     case TG_ERR_WORKSPACE: return "workspace or output buffer missing, misaligned or too small";
     case TG_ERR_CUDA: return "CUDA error";
@@ -77,7 +79,7 @@ extern "C" int tg_layout_init(int kind, int64_t N, int64_t K, tg_layout *out)
 {
     if (!out)
         return TG_ERR_ARG;
-    if (kind != TG_TERNARY_I8 && kind != TG_TERNARY_LNS8 && kind != TG_PLANES8)
+    if (kind != TG_TERNARY_I8 && kind != TG_TERNARY_LNS8 && kind != TG_PLANES8 && kind != TG_BINARY_Q1)
         return TG_ERR_ARG;
     if (N < 1 || K < TG_GROUP || K % TG_GROUP != 0 || N > ((int64_t)1 << 31) - 1 ||
         K > ((int64_t)1 << 24))
@@ -100,10 +102,10 @@ extern "C" int tg_layout_init(int kind, int64_t N, int64_t K, tg_layout *out)
         L.aux2_off = align_up(L.scale_off + L.scale_bytes);
         L.aux2_bytes = N;
         L.total_bytes = align_up(L.aux2_off + L.aux2_bytes);
-    } else if (kind == TG_TERNARY_I8) {
+    } else if (kind == TG_TERNARY_I8 || kind == TG_BINARY_Q1) {
         L.tiles = (N + tgi::kTileRows - 1) / tgi::kTileRows;
         L.mask_off = 0;
-        L.mask_bytes = L.tiles * L.G * tgi::kTileRows * 32;
+        L.mask_bytes = L.tiles * L.G * tgi::kTileRows * (kind == TG_BINARY_Q1 ? 16 : 32);
         L.scale_off = align_up(L.mask_bytes);
         L.scale_bytes = L.tiles * L.G * tgi::kTileRows * 4;
         L.total_bytes = align_up(L.scale_off + L.scale_bytes);
@@ -161,6 +163,45 @@ bool pack_masks(const tg_layout &L, const int8_t *t, uint8_t *out)
                             }
                             store_u32(chunk + 4 * u, word);
                         }
+                    }
+                }
+            }
+        }
+    });
+    for (char b : bad)
+        if (b)
+            return false;
+    return true;
+}
+
+// Pack binary rows [N][K] (every value -1 or +1) into the Q1 layout (tg.h):
+// per (tile, group), lane l's 16 bytes are four words; word u holds group
+// lanes 32u + 4j + b in bit 8b + j, set for +1. False on a value other than
+// -1 or +1.
+bool pack_q1(const tg_layout &L, const int8_t *t, uint8_t *out)
+{
+    const int64_t N = L.N, K = L.K, G = L.G;
+    std::vector<char> bad((size_t)L.tiles, 0);
+    parallel_rows(L.tiles, [&](int64_t t0, int64_t t1) {
+        for (int64_t T = t0; T < t1; T++) {
+            for (int64_t g = 0; g < G; g++) {
+                uint8_t *blk = out + L.mask_off + (T * G + g) * 512;
+                for (int l = 0; l < tgi::kTileRows; l++) {
+                    const int64_t r = T * tgi::kTileRows + l;
+                    for (int u = 0; u < 4; u++) {
+                        uint32_t word = 0;
+                        if (r < N) {
+                            const int8_t *src = t + r * K + g * TG_GROUP + u * 32;
+                            for (int j = 0; j < 8; j++) {
+                                for (int b = 0; b < 4; b++) {
+                                    const int8_t v = src[4 * j + b];
+                                    if (v != 1 && v != -1)
+                                        bad[(size_t)T] = 1;
+                                    word |= (uint32_t)(v == 1) << (8 * b + j);
+                                }
+                            }
+                        }
+                        store_u32(blk + l * 16 + 4 * u, word);
                     }
                 }
             }
@@ -236,8 +277,8 @@ extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *tri
     uint8_t *out = static_cast<uint8_t *>(out_v);
     std::memset(out, 0, (size_t)L.total_bytes);
 
-    if (kind == TG_TERNARY_I8) {
-        if (!pack_masks(L, trits, out))
+    if (kind == TG_TERNARY_I8 || kind == TG_BINARY_Q1) {
+        if (!(kind == TG_BINARY_Q1 ? pack_q1(L, trits, out) : pack_masks(L, trits, out)))
             return TG_ERR_VALUE;
         const int64_t G = L.G;
         int64_t maxabs = 0;

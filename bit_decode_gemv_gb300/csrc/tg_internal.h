@@ -25,6 +25,6 @@ int lmhead_take_device_error(void *stream);
 // Small-batch ternary GEMM on the tensor cores (2 <= M <= 64); arguments as
 // checked by tg_gemv_i8. Returns a tg_status.
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                int tiles, int M, int64_t max_abs_scale, cudaStream_t s);
+                int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s);
 
 }  // namespace tgi

@@ -9,8 +9,9 @@
  *      representation):
  *          y[m][r] = sum_g d[r][g] * ( sum_{i in group g} t[r][i] * x[m][i] ).
  *      Groups are 128 weights; the per-group partial is an int32, the sum over
- *      groups an int64. The per-group arshift(., frac) of §4.1/§4.2 is taken
- *      with frac = 0.
+ *      groups an int64. The same call takes binary Q1_0 weights {-1, +1}
+ *      (§4.1, one sign bit per weight) and the per-group floor arshift(., frac)
+ *      of §4.1/§4.2 (layout field frac, 0 by default).
  *
  *   2. LNS8 S1|E4|L3 eight-phase accumulation (BitState brief §3, §3.1 and the
  *      generic variant of §4): every nonzero product state
@@ -68,7 +69,8 @@ enum {
 enum {
     TG_TERNARY_I8 = 1,   /* ternary weights, int32 scale per 128-weight group   */
     TG_TERNARY_LNS8 = 2, /* ternary weights, uint8 LNS8 scale code per group    */
-    TG_PLANES8 = 3       /* 8 ternary base-3 planes, int32 scale per row        */
+    TG_PLANES8 = 3,      /* 8 ternary base-3 planes, int32 scale per row        */
+    TG_BINARY_Q1 = 4     /* binary Q1_0 weights {-1,+1}, int32 scale per group  */
 };
 
 #define TG_GROUP 128     /* weights per group (BitState brief §2: 128-weight groups) */
@@ -89,6 +91,13 @@ enum {
  *          (W_negative). W_negative is set only where W_nonzero is.
  *   scales [tiles][G][32]: int32 scale of row 32T + l.
  *   Rows N..32*tiles-1 are padding: zero masks, zero scales.
+ * TG_BINARY_Q1 (integer_engine.md §4.1 Q1_0; rows tiled by 32, tiles = ceil(N/32)):
+ *   masks  [tiles][G][32][16 B]: for tile T, group g and row r = 32T + l,
+ *          16 bytes = four little-endian uint32 words; word u holds group
+ *          lanes 32u + (0..31), lane 32u + 4j + b in bit 8b + j, set for a +1
+ *          weight and clear for -1.
+ *   scales [tiles][G][32]: int32 scale of row 32T + l (as TG_TERNARY_I8).
+ *   Rows N..32*tiles-1 are padding: zero bits, zero scales.
  * TG_TERNARY_LNS8 (rows in blocks of 16, tiles = ceil(N/16)): the same mask
  * pair, ordered for 16x8x16 tensor-core steps:
  *   masks  [tiles][G][32][16 B]: entry l = 4q + j (q = 0..7, j = 0..3) holds,
@@ -122,7 +131,9 @@ typedef struct tg_layout {
     int64_t total_bytes;
     int64_t max_abs_scale;  /* max |scale| seen when packing (0 from tg_layout_init) */
     int64_t flags;          /* TG_FLAG_* bits, 0 after packing; the caller may set them */
-    int64_t reserved[3];
+    int64_t frac;           /* per-group floor shift (TG_TERNARY_I8, TG_BINARY_Q1): 0..62;
+                               0 after packing; the caller may set it; 0 for other kinds */
+    int64_t reserved[2];
 } tg_layout;
 
 /*
@@ -151,10 +162,10 @@ size_t tg_packed_bytes(int kind, int64_t N, int64_t K);
 
 /*
  * Pack host weights into the device layout above (host -> host, synchronous).
- *   trits   TG_TERNARY_*: int8 [N][K] in {-1,0,1};
+ *   trits   TG_TERNARY_*: int8 [N][K] in {-1,0,1}; TG_BINARY_Q1: int8 [N][K] in {-1,+1};
  *           TG_PLANES8:   int8 [8][N][K] in {-1,0,1}, plane p weighs 3^(7-p)
  *           (SKaiNET #337: plane p has weight 3^-p; scaled by 3^7 to integers).
- *   scales  TG_TERNARY_I8: int32 [N][K/128]; TG_TERNARY_LNS8: uint8 [N][K/128]
+ *   scales  TG_TERNARY_I8, TG_BINARY_Q1: int32 [N][K/128]; TG_TERNARY_LNS8: uint8 [N][K/128]
  *           LNS8 codes; TG_PLANES8: int32 [N], each >= 1.
  *   out     host buffer of out_bytes >= tg_packed_bytes(kind, N, K); any
  *           alignment. layout receives the description (may not be NULL).
@@ -165,10 +176,15 @@ int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *trits, const v
                     void *out, size_t out_bytes, tg_layout *layout);
 
 /*
- * Ternary GEMV / small-batch GEMM with int8 activations (integer_engine.md
- * §4.2 with §4.4; BitState brief §4 masks):
- *   y[m][r] = sum_g d[r][g] * sum_{i in group g} t[r][i] * x[m][i]   (int64)
- *   layout  a TG_TERNARY_I8 layout from tg_pack_weights (max_abs_scale set).
+ * Ternary (or binary Q1_0) GEMV / small-batch GEMM with int8 activations
+ * (integer_engine.md §4.1, §4.2 with §4.4; BitState brief §4 masks):
+ *   y[m][r] = sum_g arshift( d[r][g] * sum_{i in group g} t[r][i] * x[m][i], frac )   (int64)
+ *   arshift(v, frac) is floor(v / 2^frac) (each group's scaled sum floored on
+ *   its own, then summed); frac = layout->frac, 0 by default (no floor). For
+ *   TG_BINARY_Q1 every t is -1 or +1 and the group's signed sum is formed as
+ *   2 * (sum of x over the +1 weights) - (sum of x over the group).
+ *   layout  a TG_TERNARY_I8 or TG_BINARY_Q1 layout from tg_pack_weights
+ *           (max_abs_scale set), frac in 0..62.
  *   w       device copy of the packed blob, 256-byte aligned.
  *   x       device int8 [M][K], 16-byte aligned; any value in [-128, 127].
  *   M       1..TG_MAX_M tokens (1 = batch-1 decode).

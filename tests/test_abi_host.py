@@ -102,6 +102,41 @@ def test_pack_i8_layout(N, K):
     assert not t[N:].any() and not s[N:].any()          # padding rows are zero
 
 
+def decode_q1(blob, L):
+    """Independent reader of the Q1 layout -> (signs [N][K] in {-1,+1}, scales [N][G])."""
+    N, K, G, T = L.N, L.K, L.G, L.tiles
+    words = blob[L.mask_off:L.mask_off + L.mask_bytes].view("<u4").reshape(T, G, 32, 4)   # [T][G][row][u]
+    sg = np.zeros((T * 32, K), dtype=np.int8)
+    for j in range(8):
+        for b in range(4):
+            bit = ((words >> (8 * b + j)) & 1).astype(np.int8)        # [T][G][row][u]
+            for u in range(4):
+                lanes = np.arange(G) * 128 + 32 * u + 4 * j + b
+                sg[:, lanes] = (2 * bit[:, :, :, u] - 1).transpose(0, 2, 1).reshape(T * 32, G)
+    s = blob[L.scale_off:L.scale_off + L.scale_bytes].view("<i4").reshape(T, G, 32)
+    return sg, s.transpose(0, 2, 1).reshape(T * 32, G)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 256), (70, 640)])
+def test_pack_q1_layout(N, K):
+    rng = np.random.default_rng(N + K)
+    signs = (2 * rng.integers(0, 2, size=(N, K)) - 1).astype(np.int8)
+    d = rng.integers(-(1 << 20), 1 << 20, size=(N, K // 128)).astype(np.int32)
+    blob, L = tg.tg_pack_weights(tg.TG_BINARY_Q1, signs, d)
+    assert L.kind == tg.TG_BINARY_Q1 and L.frac == 0
+    assert L.mask_bytes == L.tiles * L.G * 32 * 16          # one bit per weight
+    assert L.max_abs_scale == int(np.abs(d.astype(np.int64)).max())
+    sg, s = decode_q1(blob, L)
+    np.testing.assert_array_equal(sg[:N], signs)
+    np.testing.assert_array_equal(s[:N], d)
+    assert not s[N:].any()
+    with pytest.raises(tg.TgError) as e:                      # a zero is not a binary weight
+        bad = signs.copy()
+        bad[0, 0] = 0
+        tg.tg_pack_weights(tg.TG_BINARY_Q1, bad, d)
+    assert e.value.status == tg.TG_ERR_VALUE
+
+
 def decode_lns8(blob, L):
     """Independent reader of the LNS8 fragment layout -> (t [16*tiles][K], codes)."""
     G, T, K = L.G, L.tiles, L.K
@@ -203,6 +238,10 @@ def test_gemv_argument_errors():
     big = tg.tg_layout.from_buffer_copy(L)
     big.G, big.K, big.max_abs_scale = 1 << 20, 128 << 20, (1 << 31) - 1
     assert status_of(f, big, A256, A256, 1, A256, 0) == tg.TG_ERR_BOUND
+    for frac in (-1, 63):                                                     # floor shift out of range
+        fr = tg.tg_layout.from_buffer_copy(L)
+        fr.frac = frac
+        assert status_of(f, fr, A256, A256, 1, A256, 0) == tg.TG_ERR_ARG
 
 
 def test_lns8_argument_errors():
@@ -215,6 +254,9 @@ def test_lns8_argument_errors():
     big = tg.tg_layout.from_buffer_copy(L)
     big.K, big.G = 65536, 512
     assert status_of(f, big, A256, A256, A256, None, 0) == tg.TG_ERR_BOUND
+    fr = tg.tg_layout.from_buffer_copy(L)
+    fr.frac = 3                                                                # no floor for LNS8
+    assert status_of(f, fr, A256, A256, A256, None, 0) == tg.TG_ERR_ARG
 
 
 def test_lmhead_argument_errors():

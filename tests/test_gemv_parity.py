@@ -171,3 +171,77 @@ def test_narrow_fold_at_its_bound(M):
     x = np.full((M, K), -128, np.int8)
     x[M // 2:, ::2] = 127
     check(dict(t=t, d=d, x=x))
+
+
+# ---------------------------------------------------------------------------
+# Binary Q1_0 weights and the per-group floor (integer engine §4.1, §4.2)
+# ---------------------------------------------------------------------------
+
+def check_q1(w, frac=0, rows=None):
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import gemv, pack_to_device
+    wd, L = pack_to_device(tg.TG_BINARY_Q1, w["t"], w["d"])
+    L.frac = frac
+    y = gemv(wd, L, w["x"])
+    bits = (w["t"] > 0).astype(np.uint8)
+    if rows is None:
+        np.testing.assert_array_equal(y, oracle.gemv_q1(bits, w["d"], w["x"], frac))
+    else:
+        np.testing.assert_array_equal(y[:, rows], oracle.gemv_q1(bits[rows], w["d"][rows], w["x"], frac))
+
+
+def check_frac(w, frac):
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import gemv, pack_to_device
+    wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
+    L.frac = frac
+    np.testing.assert_array_equal(gemv(wd, L, w["x"]), oracle.gemv_i8_frac(w["t"], w["d"], w["x"], frac))
+
+
+def test_q1_ffn_up_full_size():
+    check_q1(W.ffn_up_q1())
+
+
+@pytest.mark.parametrize("N,K,M", [(1, 128, 1), (33, 256, 1), (257, 2560, 1), (40, 16384, 1),
+                                   (97, 640, 2), (97, 640, 17), (300, 1024, 64)])
+def test_q1_shapes(N, K, M):
+    check_q1(W.ffn_up_q1(seed=N + K + M, N=N, K=K, M=M))
+
+
+def test_q1_batched_full_size_sampled_rows():
+    w = W.ffn_up_q1(seed=5, N=13824, K=5120, M=64)
+    w["x"] = W.x_uniform(5, (64, 5120))
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.random.default_rng(1).choice(13824, 100, replace=False),
+                                     np.arange(13790, 13824)]))
+    check_q1(w, rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 2, 64])
+@pytest.mark.parametrize("frac", [1, 7, 20])
+def test_frac_ternary(M, frac):
+    w = W.batched(seed=M + frac, M=M, N=300, K=1024)
+    check_frac(w, frac)
+
+
+@pytest.mark.parametrize("M", [1, 64])
+@pytest.mark.parametrize("frac", [3, 15])
+def test_frac_q1(M, frac):
+    check_q1(W.ffn_up_q1(seed=7 * M + frac, N=200, K=768, M=M), frac)
+
+
+@pytest.mark.parametrize("M", [1, 2, 64])
+def test_extreme_values_q1_and_floor(M):
+    """int32-extreme scales (the 64-bit fold), with and without the floor."""
+    N, K = 160, 512
+    rng = np.random.default_rng(11 + M)
+    t = (2 * rng.integers(0, 2, size=(N, K)) - 1).astype(np.int8)
+    t[:40] = -1
+    d = rng.integers(np.iinfo(np.int32).min, np.iinfo(np.int32).max, size=(N, K // 128),
+                     dtype=np.int64).astype(np.int32)
+    d[::3] = np.iinfo(np.int32).max
+    d[1::3] = np.iinfo(np.int32).min
+    x = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
+    x[0] = -128
+    for frac in (0, 1, 33, 62):
+        check_q1(dict(t=t, d=d, x=x), frac)
+    check_frac(dict(t=np.where(t > 0, 1, np.where(rng.random((N, K)) < 0.3, 0, -1)).astype(np.int8), d=d, x=x), 9)

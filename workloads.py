@@ -15,6 +15,8 @@ Workloads (sizes and distributions):
                                        x uniform [-127, 127].
 * ``ffn_up``   N=6912,   K=2560, M=1   t with P(0)=P(+1)=P(-1)=1/3; d uniform
                                        [1, 2^15); x = clip(rint(N(0, 40^2)), +-127).
+* ``ffn_up_q1`` as ``ffn_up`` with binary Q1_0 weights: -1 or +1 with
+                                       probability 1/2 each.
 * ``lns8``     N=4096,   K=4096        LNS8 activations: each lane is exact zero
                                        with probability 0.1, otherwise its code is
                                        clip(rint(N(74, 12^2)), 1, 127) with a fair
@@ -46,6 +48,7 @@ _STREAM_IDS = {
     "planes": 8,
     "ternary_rows": 9,
     "row_scale": 10,
+    "signs": 11,
 }
 
 
@@ -56,6 +59,11 @@ def _rng(seed: int, stream: str) -> np.random.Generator:
 def trits(seed: int, shape, stream: str = "t") -> np.ndarray:
     """Ternary values with P(-1) = P(0) = P(+1) = 1/3, int8."""
     return _rng(seed, stream).integers(-1, 2, size=shape, dtype=np.int8)
+
+
+def signs(seed: int, shape) -> np.ndarray:
+    """Binary Q1_0 weights: -1 or +1 with probability 1/2 each, int8."""
+    return (2 * _rng(seed, "signs").integers(0, 2, size=shape, dtype=np.int8) - 1).astype(np.int8)
 
 
 def group_scales(seed: int, n: int, k: int, lo: int = 1, hi: int = 1 << 15) -> np.ndarray:
@@ -119,6 +127,11 @@ def tiny(seed: int = 0, N: int = 256, K: int = 512, M: int = 1) -> dict:
 def ffn_up(seed: int = 0, N: int = 6912, K: int = 2560, M: int = 1) -> dict:
     return dict(kind="i8", N=N, K=K, M=M,
                 t=trits(seed, (N, K)), d=group_scales(seed, N, K), x=x_normal40(seed, (M, K)))
+
+
+def ffn_up_q1(seed: int = 0, N: int = 6912, K: int = 2560, M: int = 1) -> dict:
+    return dict(kind="q1", N=N, K=K, M=M,
+                t=signs(seed, (N, K)), d=group_scales(seed, N, K), x=x_normal40(seed, (M, K)))
 
 
 def lns8(seed: int = 0, N: int = 4096, K: int = 4096) -> dict:
