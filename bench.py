@@ -23,7 +23,8 @@ Also reported on the same line:
                launch time, against the measured HBM copy bandwidth;
   cpu_baseline the CPU oracle timed on a bounded sample on the host cores;
   rows         the other hot-path calls (LNS8, lm_head both paths, batched
-               M=64), each timed alone (skip with --no-rows);
+               M=64, Q1_0 and the floor shift at batch 1), each timed alone
+               (skip with --no-rows);
   clocks       nvidia-smi SM clocks and throttle reasons during the timed region.
 
 --impl reference times the CPU oracle on the same workload and metric.
@@ -67,7 +68,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--quick", action="store_true", help="= --no-rows --no-cpu (for profiler runs)")
     ap.add_argument("--row", default=None,
-                    help="time only these rows (comma list of lns8, lm_head, batched) and exit")
+                    help="time only these rows (comma list of lns8, lm_head, batched, q1) and exit")
     a = ap.parse_args()
     if a.quick:
         a.no_rows = a.no_cpu = True
@@ -292,13 +293,20 @@ def row_lns8(tg, torch, stream, dev):
     xa = dev(w["xa"])
     A = torch.empty((L.N, 8), dtype=torch.int64, device="cuda")
     S = torch.empty((L.N,), dtype=torch.float64, device="cuda")
-    g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(L, wd[i % R], xa, A, S, h), R)
-    g.replay()
-    t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
     alg = L.mask_bytes + L.N * L.G + L.K + L.N * 8 * 8 + L.N * 8
-    return {"lns8": {"workload": "N=4096 K=4096 LNS8 eight-phase", "us": round(t * 1e6, 3),
-                     "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
-                     "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}}
+    out = {}
+    for key, flags in (("lns8", 0), ("lns8_stateset", tg.TG_FLAG_LNS8_STATE_SET)):
+        Lr = tg.tg_layout.from_buffer_copy(L)
+        Lr.flags = flags
+        g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(Lr, wd[i % R], xa, A, S, h), R)
+        g.replay()
+        t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
+        out[key] = {"workload": "N=4096 K=4096 LNS8 eight-phase, "
+                                + ("state-population route" if flags else "direct route"),
+                    "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
+                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}
+        del g
+    return out
 
 
 def row_lm_head(tg, torch, stream, dev):
@@ -356,7 +364,37 @@ def row_batched(tg, torch, stream, dev):
                             "tops_int": round(2 * macs / t / 1e12, 2), "copies": R}}
 
 
-ROWS = {"lns8": row_lns8, "lm_head": row_lm_head, "batched": row_batched}
+def _gemv_m1_row(tg, torch, stream, dev, kind, w, frac):
+    """Per-call time of one batch-1 GEMV shape, weights rotated over copies, PDL on."""
+    hbm, _ = measured_peaks()
+    blob, L = tg.tg_pack_weights(kind, w["t"], w["d"])
+    L.frac = frac
+    L.flags |= tg.TG_FLAG_CONST_WEIGHTS
+    R = min(_copies_for(blob.size), 512)
+    wd = [dev(blob) for _ in range(R)]
+    xd = dev(w["x"])
+    y = torch.empty((1, L.N), dtype=torch.int64, device="cuda")
+    g = capture_graph(torch, lambda i, h: tg.tg_gemv_i8(L, wd[i % R], xd, 1, y, h), R)
+    g.replay()
+    t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
+    alg = L.mask_bytes + L.scale_bytes + L.K + L.N * 8
+    return {"us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
+            "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "hbm", "copies": R}
+
+
+def row_q1(tg, torch, stream, dev):
+    """Q1_0 binary weights and the per-group floor shift on the ffn_up shape, batch 1."""
+    out = {}
+    r = _gemv_m1_row(tg, torch, stream, dev, tg.TG_TERNARY_I8, W.ffn_up(), 0)
+    out["ternary_ffn_up"] = {"workload": "N=6912 K=2560 ternary, batch 1 (same timing as below)", **r}
+    r = _gemv_m1_row(tg, torch, stream, dev, tg.TG_BINARY_Q1, W.ffn_up_q1(), 0)
+    out["q1_ffn_up"] = {"workload": "N=6912 K=2560 Q1_0 binary, batch 1", **r}
+    r = _gemv_m1_row(tg, torch, stream, dev, tg.TG_TERNARY_I8, W.ffn_up(), 4)
+    out["ternary_ffn_up_frac4"] = {"workload": "N=6912 K=2560 ternary, batch 1, frac=4", **r}
+    return out
+
+
+ROWS = {"lns8": row_lns8, "lm_head": row_lm_head, "batched": row_batched, "q1": row_q1}
 
 
 def measure_rows(tg, torch, stream, dev, names=None):

@@ -335,6 +335,8 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
     const uint8_t *codes = base + L->scale_off;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = (int)L->G, N = (int)L->N;
+    if (L->flags & TG_FLAG_LNS8_STATE_SET)
+        return tgi::lns8_stateset(masks, codes, xa, A, S, F.f, N, G, (int)L->tiles, s);
     const int gpc = (G + kMaxCluster - 1) / kMaxCluster;   // groups per CTA
     const int csize = (G + gpc - 1) / gpc;                 // CTAs per cluster, <= 8
 

@@ -27,4 +27,9 @@ int lmhead_take_device_error(void *stream);
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
                 int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s);
 
+// LNS8 eight-phase GEMV by the state-population route (TG_FLAG_LNS8_STATE_SET);
+// arguments as checked by tg_gemv_lns8_phase. Returns a tg_status.
+int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S,
+                  const double F[8], int N, int G, int tiles, cudaStream_t s);
+
 }  // namespace tgi

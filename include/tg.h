@@ -147,6 +147,15 @@ typedef struct tg_layout {
  */
 #define TG_FLAG_CONST_WEIGHTS 1
 
+/*
+ * Layout flag (TG_TERNARY_LNS8): tg_gemv_lns8_phase takes the signed
+ * state-population route of the BitState brief (§4, W_nonzero / W_negative
+ * with C_s = popcount(M) - 2 * popcount(M & PNEG), and §6, the activation state
+ * sets built once and reused across rows) instead of the direct per-lane
+ * route. A and S are identical; only the work and its cost differ.
+ */
+#define TG_FLAG_LNS8_STATE_SET 2
+
 /* Static string naming a status code. Never NULL. */
 const char *tg_status_string(int status);
 

@@ -1,4 +1,6 @@
-"""GPU parity of tg_gemv_lns8_phase against the CPU oracle.
+"""GPU parity of tg_gemv_lns8_phase against the CPU oracle, for both routes:
+the direct per-lane route and the state-population route
+(TG_FLAG_LNS8_STATE_SET).
 
 A[r][p] must be bit-exact. S is compared within 1e-12 relative error, the
 tolerance for the fp64 materialisation; the denominator is max(|S|, 2^-40 *
@@ -23,10 +25,15 @@ def built():
     ensure_built()
 
 
-def check(w, with_S=True):
+ROUTES = ["direct", "stateset"]
+
+
+def check(w, with_S=True, route="direct"):
     import bit_decode_gemv_gb300 as tg
     from gpu_helpers import lns8, pack_to_device
     wd, L = pack_to_device(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    if route == "stateset":
+        L.flags |= tg.TG_FLAG_LNS8_STATE_SET
     A, S = lns8(wd, L, w["xa"], with_S)
     A_ref = oracle.lns8_direct(w["t"], w["dcode"], w["xa"])
     np.testing.assert_array_equal(A, A_ref)
@@ -40,8 +47,9 @@ def check(w, with_S=True):
     return A, S
 
 
-def test_lns8_workload_full_size():
-    check(W.lns8())
+@pytest.mark.parametrize("route", ROUTES)
+def test_lns8_workload_full_size(route):
+    check(W.lns8(), route=route)
 
 
 def wide(seed, N, K):
@@ -54,12 +62,14 @@ def wide(seed, N, K):
     return w
 
 
+@pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("N,K", [(1, 128), (33, 128), (95, 384), (1000, 4096), (40, 12800)])
-def test_clamp_heavy_and_ragged(N, K):
-    check(wide(N, N, K))
+def test_clamp_heavy_and_ragged(N, K, route):
+    check(wide(N, N, K), route=route)
 
 
-def test_extreme_codes():
+@pytest.mark.parametrize("route", ROUTES)
+def test_extreme_codes(route):
     N, K = 64, 256
     t = np.ones((N, K), np.int8)
     t[1::2] = -1
@@ -68,10 +78,60 @@ def test_extreme_codes():
     dcode = np.full((N, 2), 255, np.uint8)
     dcode[::4] = 0
     dcode[1::4] = 74
-    A, _ = check(dict(t=t, dcode=dcode, xa=xa))
+    A, _ = check(dict(t=t, dcode=dcode, xa=xa), route=route)
     # scale code 255 saturates every product to code 127 = phase 7, band 15
     assert np.count_nonzero(A[2, :7]) == 0 and abs(A[2, 7]) > 0
 
 
-def test_without_S():
-    check(W.lns8(seed=3, N=77, K=512), with_S=False)
+@pytest.mark.parametrize("route", ROUTES)
+def test_without_S(route):
+    check(W.lns8(seed=3, N=77, K=512), with_S=False, route=route)
+
+
+@pytest.mark.parametrize("route", ROUTES)
+@pytest.mark.parametrize("n_states", [1, 2, 8, 32, 127])
+def test_state_cardinality(n_states, route):
+    """Activations drawn from a set of n_states codes: every state has many
+    lanes when the set is small, one lane each when it is large."""
+    w = W.lns8(seed=n_states, N=300, K=2048)
+    w["xa"] = W.lns8_activations_states(n_states, 2048, n_states)
+    check(w, route=route)
+
+
+@pytest.mark.parametrize("route", ROUTES)
+@pytest.mark.parametrize("zero_frac", [0.0, 0.9, 1.0])
+def test_weight_zero_density(zero_frac, route):
+    w = W.lns8(seed=5, N=130, K=1024)
+    w["t"] = W.trits_sparse(5, (130, 1024), zero_frac)
+    check(w, route=route)
+
+
+@pytest.mark.parametrize("route", ROUTES)
+def test_all_activations_zero(route):
+    """Every activation code 0 (with both signs): no state is active, A = 0."""
+    w = W.lns8(seed=9, N=70, K=256)
+    w["xa"] = np.where(np.arange(256) % 2 == 0, 0x80, 0x00).astype(np.uint8)
+    A, S = check(w, route=route)
+    assert not A.any() and not S.any()
+
+
+@pytest.mark.parametrize("route", ROUTES)
+def test_one_state_saturates_or_vanishes(route):
+    """One active code per group and scale codes at both ends, so that in each
+    (row, group) the single state is either dropped (k <= 0), saturated
+    (k > 127) or routed, on both sides of a 64-row tile boundary."""
+    N, K = 130, 512
+    rng = np.random.default_rng(11)
+    t = rng.integers(-1, 2, size=(N, K), dtype=np.int8)
+    xa = np.repeat(np.array([1, 127, 74, 0x80 | 60], np.uint8), 128)
+    dcode = rng.choice(np.array([0, 1, 73, 74, 75, 128, 200, 255], np.uint8), size=(N, K // 128))
+    check(dict(t=t, dcode=dcode, xa=xa), route=route)
+
+
+def test_routes_agree_bitwise_on_the_workload():
+    """The two routes return the same A and the same S bits on the workload."""
+    w = W.lns8(seed=4, N=1024, K=4096)
+    A0, S0 = check(w, route="direct")
+    A1, S1 = check(w, route="stateset")
+    np.testing.assert_array_equal(A0, A1)
+    np.testing.assert_array_equal(S0.view(np.int64), S1.view(np.int64))

@@ -49,6 +49,8 @@ _STREAM_IDS = {
     "ternary_rows": 9,
     "row_scale": 10,
     "signs": 11,
+    "sparse_t": 12,
+    "states": 13,
 }
 
 
@@ -59,6 +61,14 @@ def _rng(seed: int, stream: str) -> np.random.Generator:
 def trits(seed: int, shape, stream: str = "t") -> np.ndarray:
     """Ternary values with P(-1) = P(0) = P(+1) = 1/3, int8."""
     return _rng(seed, stream).integers(-1, 2, size=shape, dtype=np.int8)
+
+
+def trits_sparse(seed: int, shape, zero_frac: float) -> np.ndarray:
+    """Ternary values with P(0) = zero_frac and P(-1) = P(+1), int8."""
+    r = _rng(seed, "sparse_t")
+    t = np.where(r.random(shape) < 0.5, 1, -1).astype(np.int8)
+    t[r.random(shape) < zero_frac] = 0
+    return t
 
 
 def signs(seed: int, shape) -> np.ndarray:
@@ -93,6 +103,22 @@ def lns8_activations(seed: int, k: int) -> np.ndarray:
     zero = _rng(seed, "zero").random(k) < 0.1
     code[zero] = 0
     sign = _rng(seed, "sign").integers(0, 2, size=k, dtype=np.int64)
+    return ((sign << 7) | code).astype(np.uint8)
+
+
+def lns8_activations_states(seed: int, k: int, n_states: int) -> np.ndarray:
+    """LNS8 activation bytes whose nonzero codes come from a set of n_states.
+
+    The set is the n_states codes nearest to 74 (code 74 = 1.0; the lower code
+    first on a tie), every nonzero lane draws one of them uniformly, and lanes
+    are exact zero with probability 0.1 and carry a fair-coin sign, as in
+    lns8_activations. n_states = 127 is every code 1..127.
+    """
+    pool = sorted(range(1, 128), key=lambda c: (abs(c - 74), c))[:n_states]
+    r = _rng(seed, "states")
+    code = np.asarray(pool, dtype=np.int64)[r.integers(0, n_states, size=k)]
+    code[r.random(k) < 0.1] = 0
+    sign = r.integers(0, 2, size=k, dtype=np.int64)
     return ((sign << 7) | code).astype(np.uint8)
 
 
