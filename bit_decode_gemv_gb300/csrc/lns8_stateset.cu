@@ -14,43 +14,42 @@
 //
 // Sparse state sets. The brief lists sparse (state, lane mask) pairs for the
 // active states only, and warp ballot / match-any instead of a bit transpose.
-// A group's 128 lanes are split into four 32-lane words; one warp builds, per
-// word, the list of (code, lane mask) pairs of the codes present in that word:
-// lane l of the warp takes the activation at bit l of the word, and
-// __match_any_sync on the code returns the mask itself. Entries are stored
-// sorted by (word, code & 7). A state contributes only in the words where it
-// has lanes, so a row pays two popcounts per (row, entry) and about 85 entries
-// per group on normally distributed codes, not 4 x 45 word-state pairs.
+// A group's 128 lanes are split into four 32-lane words; per word, one warp
+// builds the list of (code, lane mask) entries of the codes present in that
+// word: lane l of the warp takes the activation at bit l of the word, and
+// __match_any_sync on the code returns the entry's mask itself. A state pays
+// only in the words where it has lanes: about 85 entries per group for
+// normally distributed codes instead of 4 x 45 word-state pairs. Entries with
+// several lanes come first in each word's list; a single-lane entry needs no
+// popcount (popcount of a word with at most one bit set is a bit test), which
+// keeps the popcount pipe (a quarter of the integer rate) for the others.
 //
-// Reuse. The entry list depends only on the activations: the warp that builds
-// it applies it to 64 rows (lane = rows q and q + 8 of one of four 16-row
-// blocks), which is the "encode once per activation tile, intersect and count
-// per row" split of the brief.
+// Reuse. The lists depend only on the activations; they are built once per
+// CTA and applied to its 128 rows: "encode once per activation tile,
+// intersect and count per row".
 //
-// Bit order. The weight blob is the LNS8 fragment layout (16-row blocks; entry
-// 4q + j of a group holds rows q and q + 8 at lanes 16c + {2j, 2j+1, 2j+8,
-// 2j+9}). A lane converts its four entries j into one W_nonzero and one
-// effective-negative word per row and j, with two byte permutes and two
-// shift-and-merge steps per word pair; the activation masks use the bit order
-// this conversion produces (lane_col below), so no bit transpose is needed.
+// Class sums on the tensor core. With e = d - 74 = 8 beta + delta, a state
+// a = 8c + q lands in phase (q + delta) & 7 with band c + beta + [q + delta >=
+// 8], so per (row, group) it is enough to form the class sums
+//   G[row][q] = sum over entries of class q of C[row][entry] * 2^c,
+// a contraction of C (rows x entries) with V (entries x 8), V[entry][q] =
+// 2^c where the entry's code has class q. A 16x8x16 bf16 MMA takes 16 rows x
+// 16 entries: C is in [-32, 32] and V a power of two, both exact in bf16, and
+// every partial sum is an integer of magnitude at most 128 * 2^15 = 2^22, so
+// fp32 accumulation is exact. The lane layout is the LNS8 fragment layout
+// itself: lane (g, t) of a warp holds rows g and g + 8 of a 16-row block at
+// the 32 lanes of word t, exactly the A-fragment rows it feeds, so each lane
+// computes C for four entries of its own word per 16-entry tile. G is then
+// shifted by beta + carry (exact either way: each term of G[q] is a multiple
+// of 2^-shift when the shift is negative) into A[(q + delta) & 7].
 //
-// Phase factorisation, as in the direct route: with e = d - 74 = 8 beta +
-// delta, a state a = 8c + q lands in phase (q + delta) & 7 with band c + beta +
-// [q + delta >= 8]. Per (row, group) the kernel sums G[q] = sum C_a 2^c over
-// the entries of phase class q (an unrolled loop per class, so the eight sums
-// stay in registers) and adds G[q] * 2^(beta + carry) into A[(q + delta) & 7]
-// (an exact shift either way: every term of G[q] is a multiple of 2^-shift
-// when the shift is negative). Where a row can clamp in a group (decided from
-// the group's smallest and largest nonzero code), the whole warp takes a
-// checked loop that leaves out k <= 0 and sends k > 127 to 2^15 in phase 7.
+// Clamps. A (warp, group) whose rows could clamp (decided from the group's
+// smallest and largest nonzero code and the warp's scale codes) takes a
+// checked loop: C of a (row, entry) with k <= 0 is set to 0, and with k > 127
+// it goes to 2^15 in phase 7 instead.
 //
-// Cost. Popcount issues at a quarter of the integer rate per SM, and there
-// are 4 popcounts per (lane, entry), so the route is popcount-bound. It beats
-// the direct route only where activations have few distinct codes per group;
-// the reuse and cardinality sweeps measure where.
-//
-// Reduction: int32 phase partials per CTA in shared memory, then the same
-// cluster push reduction and fixed-order fp64 S as the direct route.
+// Reduction: int32 phase partials per CTA in shared memory, then the cluster
+// push reduction and the fixed-order fp64 S of the direct route.
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -65,14 +64,16 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kWarps = 8;          // warps per CTA; each owns whole groups
-constexpr int kRows = 64;          // rows per CTA: four 16-row blocks
+constexpr int kWarps = 8;           // warps per CTA; warp w owns one 16-row block
+constexpr int kRows = kWarps * 16;  // rows per CTA
+constexpr int kChunk = 8;           // groups whose entry lists are staged at once (one builder warp each)
+constexpr int kListStride = 36;     // entries per word list: 32 + 4, so the four lists of a tile
+                                    // sit in different banks
 constexpr int kMaxCluster = 8;
-constexpr int kMaxEntries = 128;   // (word, code) entries of a group: at most one per lane
 constexpr unsigned kFull = 0xffffffffu;
 
-// Group lane held at bit `bit` of compact word j (the order the weight
-// conversion below produces for both rows of a lane).
+// Group lane held at bit `bit` of compact word j (the order convert_word
+// produces for both rows of a lane).
 __device__ __forceinline__ int lane_col(int j, int bit)
 {
     const int x = 7 - (bit & 7);
@@ -80,70 +81,148 @@ __device__ __forceinline__ int lane_col(int j, int bit)
     return 16 * c + 2 * j + 8 * ((x >> 1) & 1) + (bit >> 4);
 }
 
-struct RowWords {
-    uint32_t nz[4];   // W_nonzero, compact word j
-    uint32_t ng[4];   // W_negative, compact word j (activation sign applied later)
-};
-
-// One 16-byte LNS8 entry (words u = 0..3) -> compact word j of rows q and q+8.
-__device__ __forceinline__ void convert_entry(uint4 w, int j, RowWords &rq, RowWords &rq8)
+// One 16-byte LNS8 entry (words u = 0..3, both rows of a lane) -> the compact
+// W_nonzero and W_negative words of rows q and q + 8.
+__device__ __forceinline__ void convert_word(uint4 w, uint32_t &nz0, uint32_t &ng0, uint32_t &nz1,
+                                             uint32_t &ng1)
 {
     const uint32_t nza0 = __byte_perm(w.x, w.y, 0x6240), nga0 = __byte_perm(w.x, w.y, 0x7351);
     const uint32_t nza1 = __byte_perm(w.z, w.w, 0x6240), nga1 = __byte_perm(w.z, w.w, 0x7351);
-    rq.nz[j] = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
-    rq8.nz[j] = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
-    rq.ng[j] = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
-    rq8.ng[j] = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
+    nz0 = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
+    nz1 = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
+    ng0 = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
+    ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
 }
 
-// Entry scan of one group for the two rows of a lane. kChecked: apply the
-// per-row k range (k <= 0 dropped, k > 127 counted into hi).
-template <bool kChecked>
-__device__ __forceinline__ void scan_group(const uint2 *list, const int *offs, const uint32_t (&nz0)[4],
-                                           const uint32_t (&ne0)[4], const uint32_t (&nz1)[4],
-                                           const uint32_t (&ne1)[4], int e0, int e1, int (&g0)[8],
-                                           int (&g1)[8], int &hi0, int &hi1)
+struct GroupMeta {
+    int tiles;         // 16-entry tiles (4 entries of each word)
+    int tiles_multi;   // leading tiles that hold an entry with several lanes
+    int amin, amax;    // smallest and largest nonzero code (amax = 0: none)
+    uint32_t sg[4];    // activation sign, compact word j
+};
+
+// bf16 pair (lo, hi) of two integers of magnitude below 2^8: the fp32 value
+// from the 1.5 * 2^23 magic number, whose low 16 mantissa bits are zero.
+__device__ __forceinline__ uint32_t bf16x2_int(int lo, int hi)
 {
+    const float flo = __int_as_float(0x4B400000 + lo) - 12582912.0f;
+    const float fhi = __int_as_float(0x4B400000 + hi) - 12582912.0f;
+    return __byte_perm(__float_as_uint(flo), __float_as_uint(fhi), 0x7632);
+}
+
+// Exact fp32 integer of magnitude at most 2^22 -> int.
+__device__ __forceinline__ int int_of_f32(float v) { return __float_as_int(v + 12582912.0f) - 0x4B400000; }
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Signed population of an entry in one row. kSingle: the mask has one lane.
+template <bool kSingle>
+__device__ __forceinline__ int entry_pop(uint32_t nz, uint32_t ne, uint32_t m)
+{
+    if (kSingle)
+        return (nz & m) ? ((ne & m) ? -1 : 1) : 0;
+    return __popc(nz & m) - 2 * __popc(ne & m);
+}
+
+// V of an entry for class n: bf16 2^(code >> 3) (bits 16..31 of y) if the
+// entry's code has class n, else 0; padding entries carry y = 0.
+__device__ __forceinline__ uint32_t v_of(uint32_t y, uint32_t n) { return ((y & 7u) == n) ? (y >> 16) : 0u; }
+
+// One 16-entry tile: C of this lane's four entries in its two rows -> A
+// fragment, their V for class gq -> B fragment, one MMA.
+template <bool kSingle, bool kChecked>
+__device__ __forceinline__ void tile_step(const uint2 *L, int t, uint32_t nz0, uint32_t ne0, uint32_t nz1,
+                                          uint32_t ne1, int e0, int e1, uint32_t gq, float (&d)[4], int &hi0,
+                                          int &hi1)
+{
+    const uint4 p01 = *reinterpret_cast<const uint4 *>(L + 4 * t);
+    const uint4 p23 = *reinterpret_cast<const uint4 *>(L + 4 * t + 2);
+    const uint32_t m[4] = {p01.x, p01.z, p23.x, p23.z};
+    const uint32_t y[4] = {p01.y, p01.w, p23.y, p23.w};
+    int c0[4], c1[4];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int b = offs[8 * j + q], end = offs[8 * j + q + 1];
-            for (int e = b; e < end; e++) {
-                const uint2 en = list[e];
-                const int pw = (int)(en.y & 0xffffu);
-                const int c0 = __popc(nz0[j] & en.x) - 2 * __popc(ne0[j] & en.x);
-                const int c1 = __popc(nz1[j] & en.x) - 2 * __popc(ne1[j] & en.x);
-                if (kChecked) {
-                    const int code = (int)(en.y >> 16);
-                    const int k0 = code + e0, k1 = code + e1;
-                    g0[q] += ((unsigned)(k0 - 1) < 127u) ? c0 * pw : 0;
-                    g1[q] += ((unsigned)(k1 - 1) < 127u) ? c1 * pw : 0;
-                    hi0 += k0 > 127 ? c0 : 0;
-                    hi1 += k1 > 127 ? c1 : 0;
-                } else {
-                    g0[q] += c0 * pw;
-                    g1[q] += c1 * pw;
-                }
+    for (int i = 0; i < 4; i++) {
+        c0[i] = entry_pop<kSingle>(nz0, ne0, m[i]);
+        c1[i] = entry_pop<kSingle>(nz1, ne1, m[i]);
+        if (kChecked) {
+            const int code = (int)(y[i] & 0x7fu);
+            const int k0 = code + e0, k1 = code + e1;
+            if ((unsigned)(k0 - 1) >= 127u) {
+                hi0 += k0 > 127 ? c0[i] : 0;
+                c0[i] = 0;
+            }
+            if ((unsigned)(k1 - 1) >= 127u) {
+                hi1 += k1 > 127 ? c1[i] : 0;
+                c1[i] = 0;
             }
         }
     }
+    const uint32_t b0 = v_of(y[0], gq) | (v_of(y[1], gq) << 16);
+    const uint32_t b1 = v_of(y[2], gq) | (v_of(y[3], gq) << 16);
+    mma_bf16_16816(d, bf16x2_int(c0[0], c0[1]), bf16x2_int(c1[0], c1[1]), bf16x2_int(c0[2], c0[3]),
+                   bf16x2_int(c1[2], c1[3]), b0, b1);
 }
 
-// G[q] * 2^(beta + carry) into phase (q + delta) & 7 of one row's partials.
-__device__ __forceinline__ void route_row(int *acc_row, const int (&g)[8], int hi, int e)
+template <bool kChecked>
+__device__ __forceinline__ void scan_group(const uint2 *L, const GroupMeta &M, uint32_t nz0, uint32_t ne0,
+                                           uint32_t nz1, uint32_t ne1, int e0, int e1, uint32_t gq,
+                                           float (&d)[4], int &hi0, int &hi1)
 {
-    const int delta = e & 7, beta = e >> 3;
+    int t = 0;
+    for (; t < M.tiles_multi; t++)
+        tile_step<false, kChecked>(L, t, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+    for (; t < M.tiles; t++)
+        tile_step<true, kChecked>(L, t, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+}
+
+// Entry lists of group g (warp-wide): per word j, the entries with several
+// lanes first, then the single-lane ones, then zero padding up to 32.
+__device__ __forceinline__ void build_lists(const uint8_t *__restrict__ xa, int g, int lane, uint2 (*lists)[kListStride],
+                                            GroupMeta &M)
+{
+    const unsigned lt = (1u << lane) - 1u;
+    unsigned amin = 255u, amax = 0u;
+    int maxn = 0, maxm = 0;
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
-        const int v = g[q];
-        if (v != 0) {
-            const int sh = beta + ((q + delta) >> 3);
-            atomicAdd(&acc_row[(q + delta) & 7], sh >= 0 ? v << sh : v >> -sh);
+    for (int j = 0; j < 4; j++) {
+        const unsigned a = xa[(size_t)g * TG_GROUP + lane_col(j, lane)];
+        const unsigned code = a & 0x7fu;
+        const uint32_t sg = __ballot_sync(kFull, a >> 7);
+        amin = min(amin, code ? code : 255u);
+        amax = max(amax, code);
+        const unsigned mm = __match_any_sync(kFull, code);
+        const bool leader = code != 0 && (mm & lt) == 0;
+        const bool multi = leader && (mm & (mm - 1)) != 0;
+        const unsigned bm = __ballot_sync(kFull, multi);
+        const unsigned bs = __ballot_sync(kFull, leader && !multi);
+        const int nm = __popc(bm), n = nm + __popc(bs);
+        if (leader) {
+            const int slot = multi ? __popc(bm & lt) : nm + __popc(bs & lt);
+            lists[j][slot] = make_uint2(mm, code | ((127u + (code >> 3)) << 23));
         }
+        if (lane >= n)
+            lists[j][lane] = make_uint2(0u, 0u);
+        if (lane == 0)
+            M.sg[j] = sg;
+        maxn = max(maxn, n);
+        maxm = max(maxm, nm);
     }
-    if (hi != 0)
-        atomicAdd(&acc_row[7], hi << 15);
+    amin = __reduce_min_sync(kFull, amin);
+    amax = __reduce_max_sync(kFull, amax);
+    if (lane == 0) {
+        M.tiles = (maxn + 3) >> 2;
+        M.tiles_multi = (maxm + 3) >> 2;
+        M.amin = (int)amin;
+        M.amax = (int)amax;
+    }
 }
 
 struct PhaseF {
@@ -155,8 +234,8 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                      const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
                      PhaseF F, int N, int G, int tiles, int gpc)
 {
-    __shared__ uint2 list[kWarps][kMaxEntries];       // (lane mask, code << 16 | 2^(code >> 3))
-    __shared__ int offs[kWarps][33];                  // entry offsets per (word, phase class)
+    __shared__ __align__(16) uint2 lists[kChunk][4][kListStride];
+    __shared__ GroupMeta meta[kChunk];
     __shared__ int acc[kRows][8];                     // int32 phase partials of this CTA's groups
     __shared__ int stage[kRows + kMaxCluster][8];     // partials of the rows this CTA owns, per source CTA
     __shared__ int64_t arow[kRows][8];                // int64 A of the rows this CTA owns
@@ -166,96 +245,82 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
     const int csize = (int)cluster.num_blocks();
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int q = lane & 7;                               // rows q and q + 8 of ...
-    const int blk = blockIdx.x * (kRows / 16) + (lane >> 3);   // ... this 16-row block
-    const int rl0 = 16 * (lane >> 3) + q;                 // CTA-local row of the first of them
+    const uint32_t gq = (uint32_t)lane >> 2, tq = (uint32_t)lane & 3u;
+    const int blk = blockIdx.x * kWarps + warp;       // 16-row block of this warp
     const bool blk_ok = blk < tiles;
+    const int rl0 = warp * 16 + (int)gq;              // CTA-local rows rl0 and rl0 + 8
+    const int row0 = blockIdx.x * kRows + rl0;
+    const bool v0 = row0 < N, v1 = row0 + 8 < N;
     const int g_begin = rank * gpc;
     const int g_end = min(G, g_begin + gpc);
-    const unsigned lt = (1u << lane) - 1u;
 
     for (int i = tid; i < kRows * 8; i += blockDim.x)
         (&acc[0][0])[i] = 0;
-    __syncthreads();
 
-    for (int g = g_begin + warp; g < g_end; g += kWarps) {
-        // weights of this lane's two rows (issued first, used after the build)
-        uint4 wv[4] = {};
-        int d0 = 0, d1 = 0;
-        if (blk_ok) {
-            const uint4 *src = masks + ((size_t)blk * G + g) * 32 + 4 * q;
-#pragma unroll
-            for (int j = 0; j < 4; j++)
-                wv[j] = tgi::ldg_stream(src + j);
-            const uint8_t *dc = codes + ((size_t)blk * G + g) * 16;
-            d0 = dc[q];
-            d1 = dc[q + 8];
-        }
-
-        // state sets of this group: per word, one entry per code present
-        uint32_t sg[4];
-        int base = 0;
-        unsigned amin = 255u, amax = 0u;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const unsigned a = xa[(size_t)g * TG_GROUP + lane_col(j, lane)];
-            const unsigned code = a & 0x7fu;
-            sg[j] = __ballot_sync(kFull, a >> 7);
-            amin = min(amin, code ? code : 255u);
-            amax = max(amax, code);
-            const unsigned mm = __match_any_sync(kFull, code);
-            const bool leader = code != 0 && (mm & lt) == 0;
-            int slot = 0;
-#pragma unroll
-            for (int c = 0; c < 8; c++) {
-                const bool mine = leader && (int)(code & 7u) == c;
-                const unsigned bal = __ballot_sync(kFull, mine);
-                if (mine)
-                    slot = base + __popc(bal & lt);
-                if (lane == 0)
-                    offs[warp][8 * j + c] = base;
-                base += __popc(bal);
+    for (int c0 = g_begin; c0 < g_end; c0 += kChunk) {
+        const int ng = min(kChunk, g_end - c0);
+        if (warp < ng)
+            build_lists(xa, c0 + warp, lane, lists[warp], meta[warp]);
+        __syncthreads();
+        for (int gl = 0; gl < ng; gl++) {
+            const int g = c0 + gl;
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            int d0 = 0, d1 = 0;
+            if (blk_ok) {
+                w = tgi::ldg_stream(masks + ((size_t)blk * G + g) * 32 + lane);
+                const uint8_t *dc = codes + ((size_t)blk * G + g) * 16;
+                d0 = dc[gq];
+                d1 = dc[gq + 8];
             }
-            if (leader)
-                list[warp][slot] = make_uint2(mm, (code << 16) | (1u << (code >> 3)));
-        }
-        if (lane == 0)
-            offs[warp][32] = base;
-        amin = __reduce_min_sync(kFull, amin);
-        amax = __reduce_max_sync(kFull, amax);
-        __syncwarp();
+            const GroupMeta &M = meta[gl];
+            uint32_t nz0, ng0, nz1, ng1;
+            convert_word(w, nz0, ng0, nz1, ng1);
+            const uint32_t sg = M.sg[tq];
+            const uint32_t ne0 = nz0 & (ng0 ^ sg), ne1 = nz1 & (ng1 ^ sg);
+            const int e0 = d0 - 74, e1 = d1 - 74;
 
-        // this lane's rows: compact W_nonzero and effective-negative words
-        RowWords r0, r1;
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-            convert_entry(wv[j], j, r0, r1);
-        uint32_t ne0[4], ne1[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            ne0[j] = r0.nz[j] & (r0.ng[j] ^ sg[j]);
-            ne1[j] = r1.nz[j] & (r1.ng[j] ^ sg[j]);
-        }
+            // can any row of this warp clamp in this group? (rows past N have
+            // zero weights and are left out)
+            const int emin = (int)__reduce_min_sync(
+                                 kFull, min(v0 ? (unsigned)(e0 + 128) : 511u, v1 ? (unsigned)(e1 + 128) : 511u)) - 128;
+            const int emax = (int)__reduce_max_sync(
+                                 kFull, max(v0 ? (unsigned)(e0 + 128) : 0u, v1 ? (unsigned)(e1 + 128) : 0u)) - 128;
+            const bool safe = M.amax == 0 || (M.amin + emin >= 1 && M.amax + emax <= 127);
 
-        const int e0 = d0 - 74, e1 = d1 - 74;
-        const bool any = amax != 0;
-        const bool fast = !any || ((int)amin + min(e0, e1) >= 1 && (int)amax + max(e0, e1) <= 127);
-        int g0[8] = {0, 0, 0, 0, 0, 0, 0, 0}, g1[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        int hi0 = 0, hi1 = 0;
-        if (__all_sync(kFull, fast))
-            scan_group<false>(list[warp], offs[warp], r0.nz, ne0, r1.nz, ne1, e0, e1, g0, g1, hi0, hi1);
-        else
-            scan_group<true>(list[warp], offs[warp], r0.nz, ne0, r1.nz, ne1, e0, e1, g0, g1, hi0, hi1);
-        route_row(acc[rl0], g0, hi0, e0);
-        route_row(acc[rl0 + 8], g1, hi1, e1);
-        __syncwarp();   // the list and offsets are rebuilt for the next group
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            int hi0 = 0, hi1 = 0;
+            const uint2 *L = lists[gl][tq];
+            if (safe)
+                scan_group<false>(L, M, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+            else
+                scan_group<true>(L, M, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+
+            // d = G[gq][2tq], G[gq][2tq+1], G[gq+8][2tq], G[gq+8][2tq+1]
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                const int e = r ? e1 : e0;
+                const int delta = e & 7, beta = e >> 3;
+#pragma unroll
+                for (int i = 0; i < 2; i++) {
+                    const int v = int_of_f32(d[2 * r + i]);
+                    if (v != 0) {
+                        const int q = 2 * (int)tq + i;
+                        const int sh = beta + ((q + delta) >> 3);
+                        atomicAdd(&acc[rl0 + 8 * r][(q + delta) & 7], sh >= 0 ? v << sh : v >> -sh);
+                    }
+                }
+                const int h = r ? hi1 : hi0;
+                if (h != 0)
+                    atomicAdd(&acc[rl0 + 8 * r][7], h << 15);
+            }
+        }
+        __syncthreads();   // the lists are rebuilt for the next chunk
     }
 
     // Cluster reduction: CTA `dst` of the cluster owns rows [dst * slice,
-    // (dst + 1) * slice) of the 64; every CTA stores its partials of those rows
-    // into the owner's staging area, one barrier makes them visible, and each
-    // owner sums its slice in rank order.
-    __syncthreads();
+    // (dst + 1) * slice) of the 128; every CTA stores its partials of those
+    // rows into the owner's staging area, one barrier makes them visible, and
+    // each owner sums its slice in rank order.
     const int slice = (kRows + csize - 1) / csize;
     for (int item = tid; item < kRows * 8; item += blockDim.x) {
         const int rl = item >> 3, p = item & 7;
@@ -302,9 +367,8 @@ int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, i
     PhaseF f;
     for (int p = 0; p < 8; p++)
         f.f[p] = F[p];
-    const int csize = min(kMaxCluster, (G + kWarps - 1) / kWarps);   // one group per warp where possible
-    const int gpc = (G + csize - 1) / csize;
-    const int cl = (G + gpc - 1) / gpc;
+    const int gpc = (G + kMaxCluster - 1) / kMaxCluster;   // groups per CTA
+    const int cl = (G + gpc - 1) / gpc;                     // CTAs per cluster, <= 8
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((N + kRows - 1) / kRows), (unsigned)cl);
