@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--quick", action="store_true", help="= --no-rows --no-cpu (for profiler runs)")
+    ap.add_argument("--sweep", default=None, choices=["lns8_routes"],
+                    help="run a measurement sweep instead of the bench and exit")
     ap.add_argument("--row", default=None,
                     help="time only these rows (comma list of lns8, lm_head, batched, q1) and exit")
     a = ap.parse_args()
@@ -406,6 +408,66 @@ def measure_rows(tg, torch, stream, dev, names=None):
     return out
 
 
+def _lns8_route_point(tg, torch, stream, dev, w):
+    """Per-call µs of both LNS8 routes on one workload (weights rotated over
+    copies, each route from its own CUDA graph); the two routes' A must agree."""
+    blob, L = tg.tg_pack_weights(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    R = min(_copies_for(blob.size), 256)
+    wd = [dev(blob) for _ in range(R)]
+    xa = dev(w["xa"])
+    A = [torch.empty((L.N, 8), dtype=torch.int64, device="cuda") for _ in range(2)]
+    S = torch.empty((L.N,), dtype=torch.float64, device="cuda")
+    us = []
+    for k, flags in enumerate((0, tg.TG_FLAG_LNS8_STATE_SET)):
+        Lr = tg.tg_layout.from_buffer_copy(L)
+        Lr.flags = flags
+        g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(Lr, wd[i % R], xa, A[k], S, h), R)
+        g.replay()
+        reps = max(2, min(20, int(2e5 / R)))
+        us.append(event_time(torch, lambda i: g.replay(), reps, stream) / (reps * R) * 1e6)
+        del g
+    if not torch.equal(A[0], A[1]):
+        raise SystemExit("LNS8 routes disagree")
+    states = [len(set((w["xa"][g * 128:(g + 1) * 128] & 0x7F).tolist()) - {0}) for g in range(L.G)]
+    return {"direct_us": round(us[0], 3), "stateset_us": round(us[1], 3),
+            "stateset_over_direct": round(us[1] / us[0], 3),
+            "states_per_group": round(float(np.mean(states)), 1), "weight_copies": R}
+
+
+def run_sweep_lns8_routes(args):
+    """The reuse sweep (rows sharing one activation vector), the activation
+    state-cardinality sweep and the ternary zero-density sweep of the two LNS8
+    routes, one JSON line per point."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from bit_decode_gemv_gb300 import build as tgbuild
+    tgbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    K = 4096
+    for N in (1, 8, 32, 128, 512, 2048, 4096, 16384):
+        r = _lns8_route_point(tg, torch, stream, dev, W.lns8(seed=1, N=N, K=K))
+        print(json.dumps({"sweep": "reuse", "N": N, "K": K, **r}), flush=True)
+        torch.cuda.empty_cache()
+    for n in (1, 2, 4, 8, 16, 32, 64, 127):
+        w = W.lns8(seed=2, N=4096, K=K)
+        w["xa"] = W.lns8_activations_states(n, K, n)
+        r = _lns8_route_point(tg, torch, stream, dev, w)
+        print(json.dumps({"sweep": "cardinality", "N": 4096, "K": K, "code_set": n, **r}), flush=True)
+        torch.cuda.empty_cache()
+    for z in (0.0, 1 / 3, 0.9):
+        w = W.lns8(seed=3, N=4096, K=K)
+        w["t"] = W.trits_sparse(3, (4096, K), z)
+        r = _lns8_route_point(tg, torch, stream, dev, w)
+        print(json.dumps({"sweep": "zero_density", "N": 4096, "K": K, "zero_frac": round(z, 3), **r}),
+              flush=True)
+        torch.cuda.empty_cache()
+
+
 def run_row_only(args):
     """--row NAME: time one of the other hot-path calls alone (for profiler runs)."""
     import torch
@@ -580,7 +642,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.row:
+    if args.sweep == "lns8_routes":
+        run_sweep_lns8_routes(args)
+    elif args.row:
         run_row_only(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -235,8 +235,11 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 for (int half = 0; half < 2; half++) {
                     const int e = ec[gl][half];
                     int *acc_row = acc[warp * 16 + gq + 8 * half];
-                    // quad-uniform: the four threads of a quad hold the same row
-                    const bool clamp_free = lo > 127 || (lo + e >= 1 && hi + e <= 127);
+                    // quad-uniform: the four threads of a quad hold the same row.
+                    // Rows past N (zero weights, scale code 0) never need the
+                    // clamp correction.
+                    const bool clamp_free = lo > 127 || (lo + e >= 1 && hi + e <= 127) ||
+                                            rb * 16 + gq + 8 * half >= N;
                     int clamp = 0;
                     if (!clamp_free) {
                         int *gc = gcorr[warp][gq + 8 * half];

@@ -94,11 +94,11 @@ __device__ __forceinline__ void convert_word(uint4 w, uint32_t &nz0, uint32_t &n
     ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
 }
 
-struct GroupMeta {
-    int tiles;         // 16-entry tiles (4 entries of each word)
-    int tiles_multi;   // leading tiles that hold an entry with several lanes
-    int amin, amax;    // smallest and largest nonzero code (amax = 0: none)
-    uint32_t sg[4];    // activation sign, compact word j
+struct WordMeta {
+    int n, n_multi;    // entries, and of them those with several lanes
+    int amin, amax;    // smallest and largest nonzero code of the word (amax = 0: none)
+    uint32_t sg;       // activation sign, compact word
+    uint32_t pad[3];
 };
 
 // bf16 pair (lo, hi) of two integers of magnitude below 2^8: the fp32 value
@@ -136,6 +136,12 @@ __device__ __forceinline__ int entry_pop(uint32_t nz, uint32_t ne, uint32_t m)
 // entry's code has class n, else 0; padding entries carry y = 0.
 __device__ __forceinline__ uint32_t v_of(uint32_t y, uint32_t n) { return ((y & 7u) == n) ? (y >> 16) : 0u; }
 
+// bf16 bits of the signed population of a single-lane entry: +1, -1 or 0.
+__device__ __forceinline__ uint32_t single_bf16(uint32_t nz, uint32_t ne, uint32_t m)
+{
+    return (nz & m) ? ((ne & m) ? 0xBF80u : 0x3F80u) : 0u;
+}
+
 // One 16-entry tile: C of this lane's four entries in its two rows -> A
 // fragment, their V for class gq -> B fragment, one MMA.
 template <bool kSingle, bool kChecked>
@@ -147,81 +153,86 @@ __device__ __forceinline__ void tile_step(const uint2 *L, int t, uint32_t nz0, u
     const uint4 p23 = *reinterpret_cast<const uint4 *>(L + 4 * t + 2);
     const uint32_t m[4] = {p01.x, p01.z, p23.x, p23.z};
     const uint32_t y[4] = {p01.y, p01.w, p23.y, p23.w};
-    int c0[4], c1[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        c0[i] = entry_pop<kSingle>(nz0, ne0, m[i]);
-        c1[i] = entry_pop<kSingle>(nz1, ne1, m[i]);
-        if (kChecked) {
-            const int code = (int)(y[i] & 0x7fu);
-            const int k0 = code + e0, k1 = code + e1;
-            if ((unsigned)(k0 - 1) >= 127u) {
-                hi0 += k0 > 127 ? c0[i] : 0;
-                c0[i] = 0;
-            }
-            if ((unsigned)(k1 - 1) >= 127u) {
-                hi1 += k1 > 127 ? c1[i] : 0;
-                c1[i] = 0;
-            }
-        }
-    }
     const uint32_t b0 = v_of(y[0], gq) | (v_of(y[1], gq) << 16);
     const uint32_t b1 = v_of(y[2], gq) | (v_of(y[3], gq) << 16);
-    mma_bf16_16816(d, bf16x2_int(c0[0], c0[1]), bf16x2_int(c1[0], c1[1]), bf16x2_int(c0[2], c0[3]),
-                   bf16x2_int(c1[2], c1[3]), b0, b1);
+    if constexpr (kSingle && !kChecked) {
+        mma_bf16_16816(d, single_bf16(nz0, ne0, m[0]) | (single_bf16(nz0, ne0, m[1]) << 16),
+                       single_bf16(nz1, ne1, m[0]) | (single_bf16(nz1, ne1, m[1]) << 16),
+                       single_bf16(nz0, ne0, m[2]) | (single_bf16(nz0, ne0, m[3]) << 16),
+                       single_bf16(nz1, ne1, m[2]) | (single_bf16(nz1, ne1, m[3]) << 16), b0, b1);
+    } else {
+        int c0[4], c1[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            c0[i] = entry_pop<kSingle>(nz0, ne0, m[i]);
+            c1[i] = entry_pop<kSingle>(nz1, ne1, m[i]);
+            if (kChecked) {
+                const int code = (int)(y[i] & 0x7fu);
+                const int k0 = code + e0, k1 = code + e1;
+                if ((unsigned)(k0 - 1) >= 127u) {
+                    hi0 += k0 > 127 ? c0[i] : 0;
+                    c0[i] = 0;
+                }
+                if ((unsigned)(k1 - 1) >= 127u) {
+                    hi1 += k1 > 127 ? c1[i] : 0;
+                    c1[i] = 0;
+                }
+            }
+        }
+        mma_bf16_16816(d, bf16x2_int(c0[0], c0[1]), bf16x2_int(c1[0], c1[1]), bf16x2_int(c0[2], c0[3]),
+                       bf16x2_int(c1[2], c1[3]), b0, b1);
+    }
 }
 
-template <bool kChecked>
-__device__ __forceinline__ void scan_group(const uint2 *L, const GroupMeta &M, uint32_t nz0, uint32_t ne0,
-                                           uint32_t nz1, uint32_t ne1, int e0, int e1, uint32_t gq,
-                                           float (&d)[4], int &hi0, int &hi1)
+// All tiles of a group: the leading tiles with multi-lane entries by popcount,
+// the rest by bit tests.
+__device__ __forceinline__ void scan_group_fast(const uint2 *L, int tiles_multi, int tiles, uint32_t nz0,
+                                                uint32_t ne0, uint32_t nz1, uint32_t ne1, uint32_t gq, float (&d)[4])
 {
+    int h0 = 0, h1 = 0;
     int t = 0;
-    for (; t < M.tiles_multi; t++)
-        tile_step<false, kChecked>(L, t, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
-    for (; t < M.tiles; t++)
-        tile_step<true, kChecked>(L, t, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+    for (; t < tiles_multi; t++)
+        tile_step<false, false>(L, t, nz0, ne0, nz1, ne1, 0, 0, gq, d, h0, h1);
+    for (; t < tiles; t++)
+        tile_step<true, false>(L, t, nz0, ne0, nz1, ne1, 0, 0, gq, d, h0, h1);
 }
 
-// Entry lists of group g (warp-wide): per word j, the entries with several
+// The same with the per-row k range applied; rare, so kept out of line.
+__device__ __noinline__ void scan_group_checked(const uint2 *L, int tiles, uint32_t nz0, uint32_t ne0, uint32_t nz1,
+                                                uint32_t ne1, int e0, int e1, uint32_t gq, float (&d)[4], int &hi0,
+                                                int &hi1)
+{
+    for (int t = 0; t < tiles; t++)
+        tile_step<false, true>(L, t, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+}
+
+// Entry list of word j of a group (warp-wide): the entries with several
 // lanes first, then the single-lane ones, then zero padding up to 32.
-__device__ __forceinline__ void build_lists(const uint8_t *__restrict__ xa, int g, int lane, uint2 (*lists)[kListStride],
-                                            GroupMeta &M)
+__device__ __forceinline__ void build_word(unsigned a, int lane, uint2 *list, WordMeta &M)
 {
     const unsigned lt = (1u << lane) - 1u;
-    unsigned amin = 255u, amax = 0u;
-    int maxn = 0, maxm = 0;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const unsigned a = xa[(size_t)g * TG_GROUP + lane_col(j, lane)];
-        const unsigned code = a & 0x7fu;
-        const uint32_t sg = __ballot_sync(kFull, a >> 7);
-        amin = min(amin, code ? code : 255u);
-        amax = max(amax, code);
-        const unsigned mm = __match_any_sync(kFull, code);
-        const bool leader = code != 0 && (mm & lt) == 0;
-        const bool multi = leader && (mm & (mm - 1)) != 0;
-        const unsigned bm = __ballot_sync(kFull, multi);
-        const unsigned bs = __ballot_sync(kFull, leader && !multi);
-        const int nm = __popc(bm), n = nm + __popc(bs);
-        if (leader) {
-            const int slot = multi ? __popc(bm & lt) : nm + __popc(bs & lt);
-            lists[j][slot] = make_uint2(mm, code | ((127u + (code >> 3)) << 23));
-        }
-        if (lane >= n)
-            lists[j][lane] = make_uint2(0u, 0u);
-        if (lane == 0)
-            M.sg[j] = sg;
-        maxn = max(maxn, n);
-        maxm = max(maxm, nm);
+    const unsigned code = a & 0x7fu;
+    const uint32_t sg = __ballot_sync(kFull, a >> 7);
+    const unsigned mm = __match_any_sync(kFull, code);
+    const bool leader = code != 0 && (mm & lt) == 0;
+    const bool multi = leader && (mm & (mm - 1)) != 0;
+    const unsigned bm = __ballot_sync(kFull, multi);
+    const unsigned bs = __ballot_sync(kFull, leader && !multi);
+    const int nm = __popc(bm), n = nm + __popc(bs);
+    if (leader) {
+        const int slot = multi ? __popc(bm & lt) : nm + __popc(bs & lt);
+        list[slot] = make_uint2(mm, code | ((127u + (code >> 3)) << 23));
     }
-    amin = __reduce_min_sync(kFull, amin);
-    amax = __reduce_max_sync(kFull, amax);
+    if (lane >= n)
+        list[lane] = make_uint2(0u, 0u);
+    const unsigned amin = __reduce_min_sync(kFull, code ? code : 255u);
+    const unsigned amax = __reduce_max_sync(kFull, code);
     if (lane == 0) {
-        M.tiles = (maxn + 3) >> 2;
-        M.tiles_multi = (maxm + 3) >> 2;
+        M.n = n;
+        M.n_multi = nm;
         M.amin = (int)amin;
         M.amax = (int)amax;
+        M.sg = sg;
     }
 }
 
@@ -235,7 +246,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                      PhaseF F, int N, int G, int tiles, int gpc)
 {
     __shared__ __align__(16) uint2 lists[kChunk][4][kListStride];
-    __shared__ GroupMeta meta[kChunk];
+    __shared__ WordMeta meta[kChunk][4];
     __shared__ int acc[kRows][8];                     // int32 phase partials of this CTA's groups
     __shared__ int stage[kRows + kMaxCluster][8];     // partials of the rows this CTA owns, per source CTA
     __shared__ int64_t arow[kRows][8];                // int64 A of the rows this CTA owns
@@ -259,23 +270,41 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
 
     for (int c0 = g_begin; c0 < g_end; c0 += kChunk) {
         const int ng = min(kChunk, g_end - c0);
-        if (warp < ng)
-            build_lists(xa, c0 + warp, lane, lists[warp], meta[warp]);
+        // weights and scale codes of the chunk's first group, in flight during the build
+        uint4 wn = make_uint4(0u, 0u, 0u, 0u);
+        int dn = 0;
+        if (blk_ok) {
+            wn = tgi::ldg_stream(masks + ((size_t)blk * G + c0) * 32 + lane);
+            const uint8_t *dc = codes + ((size_t)blk * G + c0) * 16;
+            dn = dc[gq] | (dc[gq + 8] << 8);
+        }
+        // entry lists: one (group, word) item per warp at a time
+        for (int item = warp; item < 4 * ng; item += kWarps) {
+            const int gl = item >> 2, j = item & 3;
+            const unsigned a = xa[(size_t)(c0 + gl) * TG_GROUP + lane_col(j, lane)];
+            build_word(a, lane, lists[gl][j], meta[gl][j]);
+        }
         __syncthreads();
         for (int gl = 0; gl < ng; gl++) {
-            const int g = c0 + gl;
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            int d0 = 0, d1 = 0;
-            if (blk_ok) {
-                w = tgi::ldg_stream(masks + ((size_t)blk * G + g) * 32 + lane);
-                const uint8_t *dc = codes + ((size_t)blk * G + g) * 16;
-                d0 = dc[gq];
-                d1 = dc[gq + 8];
+            const uint4 w = wn;
+            const int d0 = dn & 0xff, d1 = dn >> 8;
+            if (blk_ok && gl + 1 < ng) {   // the next group's weights are in flight during this one
+                wn = tgi::ldg_stream(masks + ((size_t)blk * G + c0 + gl + 1) * 32 + lane);
+                const uint8_t *dc = codes + ((size_t)blk * G + c0 + gl + 1) * 16;
+                dn = dc[gq] | (dc[gq + 8] << 8);
             }
-            const GroupMeta &M = meta[gl];
+            const WordMeta *M = meta[gl];
+            int maxn = M[0].n, maxm = M[0].n_multi, amin = M[0].amin, amax = M[0].amax;
+#pragma unroll
+            for (int j = 1; j < 4; j++) {
+                maxn = max(maxn, M[j].n);
+                maxm = max(maxm, M[j].n_multi);
+                amin = min(amin, M[j].amin);
+                amax = max(amax, M[j].amax);
+            }
             uint32_t nz0, ng0, nz1, ng1;
             convert_word(w, nz0, ng0, nz1, ng1);
-            const uint32_t sg = M.sg[tq];
+            const uint32_t sg = M[tq].sg;
             const uint32_t ne0 = nz0 & (ng0 ^ sg), ne1 = nz1 & (ng1 ^ sg);
             const int e0 = d0 - 74, e1 = d1 - 74;
 
@@ -285,15 +314,16 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                                  kFull, min(v0 ? (unsigned)(e0 + 128) : 511u, v1 ? (unsigned)(e1 + 128) : 511u)) - 128;
             const int emax = (int)__reduce_max_sync(
                                  kFull, max(v0 ? (unsigned)(e0 + 128) : 0u, v1 ? (unsigned)(e1 + 128) : 0u)) - 128;
-            const bool safe = M.amax == 0 || (M.amin + emin >= 1 && M.amax + emax <= 127);
+            const bool safe = amax == 0 || (amin + emin >= 1 && amax + emax <= 127);
 
             float d[4] = {0.f, 0.f, 0.f, 0.f};
             int hi0 = 0, hi1 = 0;
             const uint2 *L = lists[gl][tq];
+            const int tiles_g = (maxn + 3) >> 2, tiles_m = (maxm + 3) >> 2;
             if (safe)
-                scan_group<false>(L, M, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+                scan_group_fast(L, tiles_m, tiles_g, nz0, ne0, nz1, ne1, gq, d);
             else
-                scan_group<true>(L, M, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
+                scan_group_checked(L, tiles_g, nz0, ne0, nz1, ne1, e0, e1, gq, d, hi0, hi1);
 
             // d = G[gq][2tq], G[gq][2tq+1], G[gq+8][2tq], G[gq+8][2tq+1]
 #pragma unroll
@@ -301,10 +331,10 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                 const int e = r ? e1 : e0;
                 const int delta = e & 7, beta = e >> 3;
 #pragma unroll
-                for (int i = 0; i < 2; i++) {
-                    const int v = int_of_f32(d[2 * r + i]);
+                for (int c = 0; c < 2; c++) {
+                    const int v = int_of_f32(d[2 * r + c]);
                     if (v != 0) {
-                        const int q = 2 * (int)tq + i;
+                        const int q = 2 * (int)tq + c;
                         const int sh = beta + ((q + delta) >> 3);
                         atomicAdd(&acc[rl0 + 8 * r][(q + delta) & 7], sh >= 0 ? v << sh : v >> -sh);
                     }
