@@ -67,7 +67,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--quick", action="store_true", help="= --no-rows --no-cpu (for profiler runs)")
-    ap.add_argument("--sweep", default=None, choices=["lns8_routes"],
+    ap.add_argument("--sweep", default=None, choices=["lns8_routes", "gemv_m"],
                     help="run a measurement sweep instead of the bench and exit")
     ap.add_argument("--row", default=None,
                     help="time only these rows (comma list of lns8, lm_head, batched, q1) and exit")
@@ -468,6 +468,42 @@ def run_sweep_lns8_routes(args):
         torch.cuda.empty_cache()
 
 
+def run_sweep_gemv_m(args):
+    """Per-call time of tg_gemv_i8 against the token count M on the ffn_up and
+    batched shapes (weights rotated over copies), one JSON line per point."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from bit_decode_gemv_gb300 import build as tgbuild
+    tgbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    hbm, _ = measured_peaks()
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    for name, N, K in (("ffn_up", 6912, 2560), ("batched", 13824, 5120)):
+        w = W.batched(seed=5, M=64, N=N, K=K)
+        blob, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+        R = min(_copies_for(blob.size), 128)
+        wd = [dev(blob) for _ in range(R)]
+        for M in (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64):
+            xd = dev(w["x"][:M])
+            y = torch.empty((M, N), dtype=torch.int64, device="cuda")
+            g = capture_graph(torch, lambda i, h: tg.tg_gemv_i8(L, wd[i % R], xd, M, y, h), R)
+            g.replay()
+            reps = max(2, min(20, int(4e4 / R)))
+            t = event_time(torch, lambda i: g.replay(), reps, stream) / (reps * R)
+            wbytes = L.mask_bytes + L.scale_bytes
+            print(json.dumps({"sweep": "gemv_m", "shape": name, "N": N, "K": K, "M": M,
+                              "us": round(t * 1e6, 3), "us_per_token": round(t * 1e6 / M, 3),
+                              "weight_gbs": round(wbytes / t / 1e9, 1),
+                              "frac_hbm": round(wbytes / t / 1e9 / hbm, 4)}), flush=True)
+            del g
+        del wd
+        torch.cuda.empty_cache()
+
+
 def run_row_only(args):
     """--row NAME: time one of the other hot-path calls alone (for profiler runs)."""
     import torch
@@ -644,6 +680,8 @@ def main():
     args = parse()
     if args.sweep == "lns8_routes":
         run_sweep_lns8_routes(args)
+    elif args.sweep == "gemv_m":
+        run_sweep_gemv_m(args)
     elif args.row:
         run_row_only(args)
     elif args.impl == "reference":

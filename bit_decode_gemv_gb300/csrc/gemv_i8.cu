@@ -24,8 +24,8 @@
 // sign bit per weight (see group_pos_q1). Each group's scaled sum is floored
 // by 2^frac on its own (§4.1/§4.2 arshift) before the sum over groups.
 //
-// This file holds the batch-1 kernel (M = 1) and the entry point; every M > 1
-// runs the tensor-core kernel of gemv_i8_mma.cu.
+// This file holds the batch-1 kernel (M = 1) and the entry point, which picks
+// the kernel for M > 1 (see kDp4aMaxTokens below).
 
 #include <cuda_runtime.h>
 
@@ -193,8 +193,15 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     }
 }
 
-// From this many tokens on, tg_gemv_i8 runs the tensor-core kernel (gemv_i8_mma.cu).
-constexpr int kMmaMinTokens = 2;
+// Kernel per token count (measured crossovers on GB300, ffn_up and batched
+// shapes): M = 1 the batch-1 kernel above; 2..kDp4aMaxTokens the CUDA-core
+// dp4a kernel (gemv_i8_mt.cu: cheapest per group when only a few tokens share
+// each weight); then the warp-MMA kernel (gemv_i8_hmma.cu) for one token tile,
+// or two when K is at most kHmmaTwoTileMaxK; above that the tensor-memory
+// kernel (gemv_i8_mma.cu), whose cost hardly grows with M up to 64.
+constexpr int kDp4aMaxTokens = 4;
+constexpr int kHmmaMaxTokens = 16;
+constexpr int kHmmaTwoTileMaxK = 4096;
 
 size_t m1_smem_bytes(int G, int warps) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + warps * 32 * 8; }
 
@@ -277,8 +284,12 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         }
         if (e != cudaSuccess)
             return TG_ERR_CUDA;
+    } else if (M <= kDp4aMaxTokens) {
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, (int)L->frac, s);
+    } else if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G)) {
+        return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1,
+                                 (int)L->frac, s);
     } else {
-        static_assert(kMmaMinTokens == 2, "every M > 1 takes the tensor-core kernel");
         return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale,
                                 L->kind == TG_BINARY_Q1, (int)L->frac, s);
     }

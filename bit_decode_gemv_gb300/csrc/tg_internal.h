@@ -27,6 +27,17 @@ int lmhead_take_device_error(void *stream);
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
                 int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s);
 
+// Ternary / Q1_0 GEMV for a few tokens on the CUDA cores (2 <= M); arguments as
+// checked by tg_gemv_i8. Returns a tg_status.
+int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
+               int M, bool q1, int frac, cudaStream_t s);
+
+// Ternary / Q1_0 GEMV for a few tokens through warp-level fp16 MMAs; the token
+// activations' fragments must fit in shared memory (gemv_i8_hmma_fits(G)).
+bool gemv_i8_hmma_fits(int G);
+int gemv_i8_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
+                 int M, bool q1, int frac, cudaStream_t s);
+
 // LNS8 eight-phase GEMV by the state-population route (TG_FLAG_LNS8_STATE_SET);
 // arguments as checked by tg_gemv_lns8_phase. Returns a tg_status.
 int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S,

@@ -139,7 +139,7 @@ def test_const_weights_back_to_back(N, K):
             np.testing.assert_array_equal(outs[rep * 4 + i].cpu().numpy(), oracle.gemv_i8(w["t"], w["d"], xi))
 
 
-@pytest.mark.parametrize("M", [2, 31, 64])
+@pytest.mark.parametrize("M", [2, 4, 5, 12, 31, 64])
 def test_extreme_values_batched(M):
     """Largest group sums |P| = 2^14 and int32-extreme scales with several tokens."""
     N, K = 300, 1024
@@ -216,20 +216,20 @@ def test_q1_batched_full_size_sampled_rows():
     check_q1(w, rows=rows)
 
 
-@pytest.mark.parametrize("M", [1, 2, 64])
+@pytest.mark.parametrize("M", [1, 2, 5, 12, 64])
 @pytest.mark.parametrize("frac", [1, 7, 20])
 def test_frac_ternary(M, frac):
     w = W.batched(seed=M + frac, M=M, N=300, K=1024)
     check_frac(w, frac)
 
 
-@pytest.mark.parametrize("M", [1, 64])
+@pytest.mark.parametrize("M", [1, 3, 8, 64])
 @pytest.mark.parametrize("frac", [3, 15])
 def test_frac_q1(M, frac):
     check_q1(W.ffn_up_q1(seed=7 * M + frac, N=200, K=768, M=M), frac)
 
 
-@pytest.mark.parametrize("M", [1, 2, 64])
+@pytest.mark.parametrize("M", [1, 2, 5, 12, 64])
 def test_extreme_values_q1_and_floor(M):
     """int32-extreme scales (the 64-bit fold), with and without the floor."""
     N, K = 160, 512
@@ -245,3 +245,17 @@ def test_extreme_values_q1_and_floor(M):
     for frac in (0, 1, 33, 62):
         check_q1(dict(t=t, d=d, x=x), frac)
     check_frac(dict(t=np.where(t > 0, 1, np.where(rng.random((N, K)) < 0.3, 0, -1)).astype(np.int8), d=d, x=x), 9)
+
+
+# Token counts on both sides of every kernel boundary of tg_gemv_i8 (the dp4a
+# kernel up to 4 tokens, the warp-MMA kernel up to 8, or 16 when K <= 4096 and
+# the activations' fragments fit, the tensor-memory kernel above), at K below
+# and above those limits, ternary and Q1_0, with and without the floor.
+@pytest.mark.parametrize("K", [640, 4608, 12800, 16384])
+@pytest.mark.parametrize("M", [2, 4, 5, 8, 9, 16, 17])
+def test_every_token_count_path(M, K):
+    N = 97 if K <= 4608 else 40
+    check(W.batched(seed=M * K, M=M, N=N, K=K))
+    check_frac(W.batched(seed=M * K + 1, M=M, N=N, K=K), 5)
+    check_q1(W.ffn_up_q1(seed=M * K + 2, N=N, K=K, M=M))
+    check_q1(W.ffn_up_q1(seed=M * K + 3, N=N, K=K, M=M), 11)
