@@ -32,6 +32,7 @@ def lib():
             "oracle_gemv_i8_stateset": [i64, i64, i64, p, p, p, p],
             "oracle_gemv_i8_frac": [i64, i64, i64, p, p, p, C.c_int, p],
             "oracle_gemv_q1": [i64, i64, i64, p, p, p, C.c_int, p],
+            "oracle_gemv_x64": [i64, i64, i64, p, p, p, C.c_int, p],
             "oracle_lns8_direct": [i64, i64, p, p, p, p],
             "oracle_lns8_histogram": [i64, i64, p, p, p, p],
             "oracle_lns8_tile64": [i64, i64, p, p, p, p],
@@ -102,6 +103,24 @@ def gemv_i8_frac(t, d, x, frac):
     y = np.zeros((M, N), dtype=np.int64)
     _check(lib().oracle_gemv_i8_frac(M, N, K, pt, pd, px, int(frac), y.ctypes.data_as(C.c_void_p)),
            "oracle_gemv_i8_frac")
+    return y
+
+
+def gemv_x64(t, d, x, frac=0):
+    """int64 fixed-point activations (integer engine §4.4, exact modulo 2^64 as
+    its §5 states): y[m][r] = sum_g arshift(d[r,g] * sum_{i in g} t[r,i] x[m,i],
+    frac) with every sum and product wrapping modulo 2^64. t in {-1,0,1}."""
+    t, pt = _c(t, np.int8)
+    d, pd = _c(d, np.int32)
+    x = np.atleast_2d(x)
+    x, px = _c(x, np.int64)
+    N, K = t.shape
+    M = x.shape[0]
+    if x.shape[1] != K or d.shape != (N, K // 128):
+        raise ValueError("shape mismatch")
+    y = np.zeros((M, N), dtype=np.int64)
+    _check(lib().oracle_gemv_x64(M, N, K, pt, pd, px, int(frac), y.ctypes.data_as(C.c_void_p)),
+           "oracle_gemv_x64")
     return y
 
 

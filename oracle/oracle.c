@@ -134,6 +134,52 @@ int oracle_gemv_i8_frac(int64_t M, int64_t N, int64_t K, const int8_t *t,
     return 0;
 }
 
+/* The int64 value of a 64-bit two's-complement pattern (no implementation-defined conversion). */
+static int64_t oracle_signed64(uint64_t v)
+{
+    if (v <= (uint64_t)INT64_MAX)
+        return (int64_t)v;
+    return -(int64_t)(~v) - 1;
+}
+
+/*
+ * [IntEngine] §4.4 fixed-point int64 activations, with §5's statement that the
+ * limb-decomposed apply is exact modulo 2^64: for every output o
+ *   out_o = sum_b arshift( signed_sum_b * scale[o][b], frac ),
+ *   signed_sum_b = sum_i t_i x_i,
+ * with x int64 and every sum and product taken modulo 2^64 (two's-complement
+ * wrapping); arshift acts on the int64 value of each group's wrapped product.
+ * Where no step leaves the int64 range this is the exact integer result.
+ * t in {-1, 0, 1} (a Q1_0 row is the case t in {-1, 1}); x [M][K] int64.
+ */
+int oracle_gemv_x64(int64_t M, int64_t N, int64_t K, const int8_t *t,
+                    const int32_t *d, const int64_t *x, int frac, int64_t *y)
+{
+    if (M < 1 || N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0 || frac < 0 || frac > 62)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t r = 0; r < N; r++) {
+            uint64_t out = 0;
+            for (int64_t g = 0; g < G; g++) {
+                uint64_t s = 0;
+                for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++) {
+                    if (t[r * K + i] == 1)
+                        s += (uint64_t)x[m * K + i];
+                    else if (t[r * K + i] == -1)
+                        s -= (uint64_t)x[m * K + i];
+                    else if (t[r * K + i] != 0)
+                        return -1;
+                }
+                const uint64_t v = s * (uint64_t)(int64_t)d[r * G + g];
+                out += (uint64_t)oracle_arshift(oracle_signed64(v), frac);
+            }
+            y[m * N + r] = oracle_signed64(out);
+        }
+    }
+    return 0;
+}
+
 /*
  * [IntEngine] §4.1 Q1_0: 1-bit weights, bit[r][i] in {0, 1} standing for
  * sign -1 / +1, and for every output o

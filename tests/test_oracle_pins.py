@@ -497,3 +497,92 @@ def test_q1_special_cases():
     assert oracle.gemv_q1(zeros, d, x)[0, 0] == -3 * total[0] + 2 * total[1]     # every sign -1
     with pytest.raises(ValueError):
         oracle.gemv_q1(np.full((1, K), 2, np.uint8), d, x)
+
+
+# ---------------------------------------------------------------------------
+# int64 fixed-point activations (integer engine §4.4), exact modulo 2^64 (its
+# §5: the limb-decomposed apply "recombined in int64 (exact mod-2^64)").
+# ---------------------------------------------------------------------------
+
+def _signed_digits(x):
+    """Signed base-256 digits s_0..s_7 in [-128, 127] with x = sum s_l 256^l
+    (mod 2^64), from Python integers (a carry per digit, no wrapping)."""
+    digits = np.zeros((8,) + x.shape, dtype=np.int8)
+    u = [int(v) % (1 << 64) for v in x.ravel()]
+    for l in range(8):
+        for idx, v in enumerate(u):
+            b = v & 0xFF
+            s = b - 256 if b >= 128 else b
+            digits[l].ravel()[idx] = s
+            u[idx] = (v - s) >> 8
+    return digits
+
+
+def _wrap64(v):
+    v %= 1 << 64
+    return v - (1 << 64) if v >= 1 << 63 else v
+
+
+def test_x64_on_the_int8_range_is_the_int8_apply():
+    w = W.batched(seed=21, M=3, N=50, K=512)
+    for frac in (0, 3, 40):
+        np.testing.assert_array_equal(oracle.gemv_x64(w["t"], w["d"], w["x"].astype(np.int64), frac),
+                                      oracle.gemv_i8_frac(w["t"], w["d"], w["x"], frac))
+
+
+@pytest.mark.parametrize("frac", [0, 1, 17, 62])
+def test_x64_matches_numpy_wrapping_int64(frac):
+    """numpy int64 matmul, products and sums wrap modulo 2^64, and >> on int64
+    is the arithmetic shift: the same definition through other primitives."""
+    rng = np.random.default_rng(frac)
+    N, K, M = 23, 384, 4
+    t = rng.integers(-1, 2, size=(N, K), dtype=np.int8)
+    d = rng.integers(np.iinfo(np.int32).min, np.iinfo(np.int32).max, size=(N, K // 128),
+                     dtype=np.int64).astype(np.int32)
+    x = rng.integers(np.iinfo(np.int64).min, np.iinfo(np.int64).max, size=(M, K), dtype=np.int64)
+    x[0, :7] = np.iinfo(np.int64).min
+    x[1, :7] = np.iinfo(np.int64).max
+    G = K // 128
+    with np.errstate(over="ignore"):
+        P = np.einsum("rgi,mgi->mrg", t.reshape(N, G, 128).astype(np.int64), x.reshape(M, G, 128))
+        ref = ((P * d.astype(np.int64)[None]) >> frac).sum(axis=2)
+    np.testing.assert_array_equal(oracle.gemv_x64(t, d, x, frac), ref)
+
+
+def test_x64_is_the_base256_limb_sum_of_int8_applies():
+    """The page's decomposition: with x = sum_l 256^l s_l (signed digits), the
+    apply of x equals sum_l 256^l (apply of s_l) modulo 2^64 (frac = 0)."""
+    rng = np.random.default_rng(5)
+    N, K, M = 9, 256, 2
+    t = rng.integers(-1, 2, size=(N, K), dtype=np.int8)
+    d = rng.integers(-(1 << 31), 1 << 31, size=(N, K // 128), dtype=np.int64).astype(np.int32)
+    x = rng.integers(np.iinfo(np.int64).min, np.iinfo(np.int64).max, size=(M, K), dtype=np.int64)
+    digits = _signed_digits(x)
+    limb = [oracle.gemv_i8(t, d, digits[l]) for l in range(8)]
+    expect = np.array([[_wrap64(sum(int(limb[l][m, r]) << (8 * l) for l in range(8))) for r in range(N)]
+                       for m in range(M)], dtype=np.int64)
+    np.testing.assert_array_equal(oracle.gemv_x64(t, d, x), expect)
+
+
+def test_x64_wraparound_closed_forms():
+    N, K = 3, 128
+    t = np.zeros((N, K), np.int8)
+    d = np.ones((N, 1), np.int32)
+    x = np.zeros((1, K), np.int64)
+    # row 0: 128 lanes of +2^57 -> P = 2^64 = 0 (mod 2^64)
+    t[0] = 1
+    x[0, :] = 1 << 57
+    # row 1: one lane -1 on x = INT64_MIN -> P = 2^63 = INT64_MIN (mod 2^64)
+    t[1, 5] = -1
+    x2 = x.copy()
+    x2[0, 5] = np.iinfo(np.int64).min
+    y = oracle.gemv_x64(t, d, x)
+    assert y[0, 0] == 0
+    y2 = oracle.gemv_x64(t, d, x2)
+    assert y2[0, 1] == np.iinfo(np.int64).min
+    # the floor acts on the wrapped product: P = 2^62, d = 2 -> -2^63, >> 1 -> -2^62
+    t3 = np.zeros((1, K), np.int8)
+    t3[0, 0] = 1
+    x3 = np.zeros((1, K), np.int64)
+    x3[0, 0] = 1 << 62
+    assert oracle.gemv_x64(t3, np.full((1, 1), 2, np.int32), x3, 1)[0, 0] == -(1 << 62)
