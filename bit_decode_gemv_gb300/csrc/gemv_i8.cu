@@ -248,8 +248,10 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         return TG_ERR_ARG;
     if (L->N < 1 || L->K < TG_GROUP || L->K % TG_GROUP || M < 1 || M > TG_MAX_M)
         return TG_ERR_SHAPE;
-    // |y| <= G * 128 * 128 * max|d| must stay well inside int64.
-    if ((double)L->G * 16384.0 * (double)L->max_abs_scale >= 4.0e18)
+    const bool x64 = (L->flags & TG_FLAG_X_INT64) != 0;
+    // int8 activations: |y| <= G * 128 * 128 * max|d| must stay well inside
+    // int64 (int64 activations wrap modulo 2^64 by definition).
+    if (!x64 && (double)L->G * 16384.0 * (double)L->max_abs_scale >= 4.0e18)
         return TG_ERR_BOUND;
 
     const auto *base = static_cast<const unsigned char *>(w);
@@ -258,6 +260,10 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = (int)L->G, N = (int)L->N;
     const int tiles = (int)L->tiles;
+
+    if (x64)   // int64 activations: the digit-plane dp4a kernel for every M
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, true,
+                               (int)L->frac, s);
 
     if (M == 1) {
         if (m1_smem_bytes(G, 32) > 200 * 1024)
@@ -285,7 +291,8 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         if (e != cudaSuccess)
             return TG_ERR_CUDA;
     } else if (M <= kDp4aMaxTokens) {
-        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, (int)L->frac, s);
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, false,
+                               (int)L->frac, s);
     } else if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G)) {
         return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1,
                                  (int)L->frac, s);

@@ -12,6 +12,16 @@
 // and one broadcast 16-byte shared load per sixteen, and the weights are read
 // from memory once for all tokens.
 //
+// int64 fixed-point activations (integer engine §4.4; exact modulo 2^64 as
+// its §5 states): each x is split into signed base-256 digits s_0..s_7 in
+// [-128, 127] with x = sum_l 256^l s_l (mod 2^64) -- the bytes of
+// (x + 0x8080...80) XOR 0x8080...80 -- and every digit plane is an ordinary
+// int8 activation vector for the arithmetic above. Per group and token the
+// planes' P_l are recombined as sum_l P_l 2^(8l) in wrapping 64-bit
+// arithmetic, multiplied by d, floored and summed, all modulo 2^64. Only the
+// planes up to the highest nonzero digit of the staged tokens are processed
+// (one plane for activations in int8 range, three for magnitudes below 2^23).
+//
 // Mapping: one CTA per 32-row tile (lane l of every warp owns row 32T + l),
 // the CTA's warps split the groups GPW at a time with every mask load of a
 // batch issued before its compute, as in the batch-1 kernel. The tokens are
@@ -100,19 +110,33 @@ __device__ __forceinline__ int group_p(const uint32_t (&wm)[32], const int8_t *x
     }
 }
 
-template <int GPW, bool kQ1>
+// The signed base-256 digits of x (mod 2^64), byte l = digit l.
+__device__ __forceinline__ uint64_t signed_digits(uint64_t x)
+{
+    return (x + 0x8080808080808080ull) ^ 0x8080808080808080ull;
+}
+
+template <bool kX64>
+__host__ __device__ constexpr int planes_max() { return kX64 ? 8 : 1; }
+
+template <int GPW, bool kQ1, bool kX64>
 __global__ void __launch_bounds__(kMaxWarps * 32)
 gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
-                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int M, int chunk,
+                  const void *__restrict__ xv, int64_t *__restrict__ y, int N, int G, int M, int chunk,
                   int frac)
 {
     constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group)
+    constexpr int kPlanes = planes_max<kX64>();
     extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int top_plane;
     const int K = G * 128;
-    int8_t *xs = reinterpret_cast<int8_t *>(smem);                                   // [chunk][K]
-    int *tsum = reinterpret_cast<int *>(smem + (size_t)chunk * K);                     // [chunk][G]
+    const size_t vrows = (size_t)chunk * kPlanes;                                      // staged activation rows
+    int8_t *xs = reinterpret_cast<int8_t *>(smem);                                   // [vrows][K]
+    int *tsum = reinterpret_cast<int *>(smem + vrows * K);                             // [vrows][G]
     unsigned long long *ysum = reinterpret_cast<unsigned long long *>(
-        smem + (size_t)chunk * K + (((size_t)chunk * G * 4 + 15) & ~(size_t)15));      // [chunk][32]
+        smem + vrows * K + ((vrows * G * 4 + 15) & ~(size_t)15));                      // [chunk][32]
+    const int8_t *x = static_cast<const int8_t *>(xv);
+    const uint64_t *x64 = static_cast<const uint64_t *>(xv);
 
     const int tile = blockIdx.x;
     const int nwarps = blockDim.x >> 5;
@@ -143,15 +167,57 @@ gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         };
         load_batch(warp);
 
-        // stage the chunk's activations, their group totals, zero the row sums
-        const uint4 *xsrc = reinterpret_cast<const uint4 *>(x + (size_t)m0 * K);
-        for (int i = threadIdx.x; i < mc * K / 16; i += blockDim.x)
-            reinterpret_cast<uint4 *>(xs)[i] = __ldg(xsrc + i);
-        for (int tgx = warp; tgx < mc * G; tgx += nwarps) {
-            const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m0 * K + (size_t)tgx * 128) + lane);
-            const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
+        // stage the chunk's activations (row t * planes + l holds digit plane l
+        // of token t), their group totals, zero the row sums
+        int planes = 1;
+        if constexpr (kX64) {
+            const uint64_t *xc = x64 + (size_t)m0 * K;
+            if (threadIdx.x == 0)
+                top_plane = 0;
+            __syncthreads();
+            int top = 0;
+            for (int i = threadIdx.x; i < mc * K; i += blockDim.x) {
+                const uint64_t dv = signed_digits(__ldg(reinterpret_cast<const unsigned long long *>(xc) + i));
+                if (dv)
+                    top = max(top, (63 - __clzll((long long)dv)) >> 3);
+            }
+            top = (int)__reduce_max_sync(0xffffffffu, (unsigned)top);
             if (lane == 0)
-                tsum[tgx] = s;
+                atomicMax(&top_plane, top);
+            __syncthreads();
+            planes = top_plane + 1;
+            for (int i = threadIdx.x; i < mc * (K / 4); i += blockDim.x) {
+                const int t = i / (K / 4), c = i - t * (K / 4);
+                const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(xc + (size_t)t * K + 4 * c);
+                const ulonglong2 v01 = __ldg(src), v23 = __ldg(src + 1);
+                const uint64_t dv[4] = {signed_digits(v01.x), signed_digits(v01.y), signed_digits(v23.x),
+                                        signed_digits(v23.y)};
+                for (int l = 0; l < planes; l++) {
+                    const uint32_t word = (uint32_t)((dv[0] >> (8 * l)) & 0xFF) |
+                                          ((uint32_t)((dv[1] >> (8 * l)) & 0xFF) << 8) |
+                                          ((uint32_t)((dv[2] >> (8 * l)) & 0xFF) << 16) |
+                                          ((uint32_t)((dv[3] >> (8 * l)) & 0xFF) << 24);
+                    *reinterpret_cast<uint32_t *>(xs + ((size_t)t * planes + l) * K + 4 * c) = word;
+                }
+            }
+            __syncthreads();
+            for (int vg = warp; vg < mc * planes * G; vg += nwarps) {
+                const uint32_t v = *(reinterpret_cast<const uint32_t *>(xs + (size_t)vg * 128) + lane);
+                const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
+                if (lane == 0)
+                    tsum[vg] = s;
+            }
+        } else {
+            const uint4 *xsrc = reinterpret_cast<const uint4 *>(x + (size_t)m0 * K);
+            for (int i = threadIdx.x; i < mc * K / 16; i += blockDim.x)
+                reinterpret_cast<uint4 *>(xs)[i] = __ldg(xsrc + i);
+            for (int tgx = warp; tgx < mc * G; tgx += nwarps) {
+                const uint32_t v =
+                    __ldg(reinterpret_cast<const uint32_t *>(x + (size_t)m0 * K + (size_t)tgx * 128) + lane);
+                const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
+                if (lane == 0)
+                    tsum[tgx] = s;
+            }
         }
         for (int i = threadIdx.x; i < mc * 32; i += blockDim.x)
             ysum[i] = 0ull;
@@ -166,8 +232,20 @@ gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
                     masked_words<kQ1>(r0[j], r1[j], wm);
                     const int64_t d = dg[j];
                     for (int t = 0; t < mc; t++) {
-                        const int P = group_p<kQ1>(wm, xs + (size_t)t * K + (size_t)g * 128, tsum[t * G + g]);
-                        atomicAdd(&ysum[t * 32 + lane], (unsigned long long)((d * (int64_t)P) >> frac));
+                        if constexpr (kX64) {
+                            // sum_l P_l 2^(8l), times d, floored: all modulo 2^64
+                            uint64_t p64 = 0;
+                            for (int l = 0; l < planes; l++) {
+                                const int vt = t * planes + l;
+                                const int P = group_p<kQ1>(wm, xs + (size_t)vt * K + (size_t)g * 128, tsum[vt * G + g]);
+                                p64 += (uint64_t)(int64_t)P << (8 * l);
+                            }
+                            const int64_t v = (int64_t)(p64 * (uint64_t)d);
+                            atomicAdd(&ysum[t * 32 + lane], (unsigned long long)(v >> frac));
+                        } else {
+                            const int P = group_p<kQ1>(wm, xs + (size_t)t * K + (size_t)g * 128, tsum[t * G + g]);
+                            atomicAdd(&ysum[t * 32 + lane], (unsigned long long)((d * (int64_t)P) >> frac));
+                        }
                     }
                 }
             }
@@ -184,25 +262,27 @@ gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     }
 }
 
-size_t mt_smem_bytes(int G, int chunk)
+size_t mt_smem_bytes(int G, int chunk, int planes)
 {
-    return (size_t)chunk * G * 128 + (((size_t)chunk * G * 4 + 15) & ~(size_t)15) + (size_t)chunk * 32 * 8;
+    const size_t rows = (size_t)chunk * planes;
+    return rows * G * 128 + ((rows * G * 4 + 15) & ~(size_t)15) + (size_t)chunk * 32 * 8;
 }
 
-template <int GPW, bool kQ1>
-cudaError_t launch_mt(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
+template <int GPW, bool kQ1, bool kX64>
+cudaError_t launch_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G,
                       int tiles, int M, int frac, cudaStream_t s)
 {
-    auto kern = gemv_i8_mt_kernel<GPW, kQ1>;
+    auto kern = gemv_i8_mt_kernel<GPW, kQ1, kX64>;
+    constexpr int kPlanes = planes_max<kX64>();
     int warps = (G + GPW - 1) / GPW;
     if (warps > kMaxWarps)
         warps = kMaxWarps;
-    int chunk = (int)(kStageBytes / ((size_t)G * 128 + 4 * (size_t)G + 256));
+    int chunk = (int)(kStageBytes / (kPlanes * ((size_t)G * 128 + 4 * (size_t)G) + 256));
     if (chunk > M)
         chunk = M;
     if (chunk < 1)
         chunk = 1;
-    const size_t smem = mt_smem_bytes(G, chunk);
+    const size_t smem = mt_smem_bytes(G, chunk, kPlanes);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -210,22 +290,29 @@ cudaError_t launch_mt(const uint4 *masks, const int32_t *scales, const int8_t *x
     return cudaGetLastError();
 }
 
+template <bool kX64>
+cudaError_t dispatch_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G,
+                        int tiles, int M, bool q1, int frac, cudaStream_t s)
+{
+    if (q1)
+        return G <= 32 ? launch_mt<2, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s)
+                       : launch_mt<4, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s);
+    return G <= 32 ? launch_mt<2, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s)
+                   : launch_mt<4, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s);
+}
+
 }  // namespace
 
 namespace tgi {
 
-int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
-               int M, bool q1, int frac, cudaStream_t s)
+int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G, int tiles,
+               int M, bool q1, bool x64, int frac, cudaStream_t s)
 {
-    if ((size_t)G * 128 + 4 * (size_t)G + 256 > kStageBytes)
-        return TG_ERR_SHAPE;   // one token's activations must fit (K <= 147,000 or so)
-    cudaError_t e;
-    if (q1)
-        e = G <= 32 ? launch_mt<2, true>(masks, scales, x, y, N, G, tiles, M, frac, s)
-                    : launch_mt<4, true>(masks, scales, x, y, N, G, tiles, M, frac, s);
-    else
-        e = G <= 32 ? launch_mt<2, false>(masks, scales, x, y, N, G, tiles, M, frac, s)
-                    : launch_mt<4, false>(masks, scales, x, y, N, G, tiles, M, frac, s);
+    const size_t planes = x64 ? 8 : 1;
+    if (planes * ((size_t)G * 128 + 4 * (size_t)G) + 256 > kStageBytes)
+        return TG_ERR_SHAPE;   // one token's activation planes must fit
+    const cudaError_t e = x64 ? dispatch_mt<true>(masks, scales, x, y, N, G, tiles, M, q1, frac, s)
+                              : dispatch_mt<false>(masks, scales, x, y, N, G, tiles, M, q1, frac, s);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

@@ -27,10 +27,11 @@ int lmhead_take_device_error(void *stream);
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
                 int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s);
 
-// Ternary / Q1_0 GEMV for a few tokens on the CUDA cores (2 <= M); arguments as
-// checked by tg_gemv_i8. Returns a tg_status.
-int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
-               int M, bool q1, int frac, cudaStream_t s);
+// Ternary / Q1_0 GEMV for a few tokens on the CUDA cores; x is int8 [M][K], or
+// int64 [M][K] when x64 (sums modulo 2^64). Arguments as checked by
+// tg_gemv_i8. Returns a tg_status.
+int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G, int tiles,
+               int M, bool q1, bool x64, int frac, cudaStream_t s);
 
 // Ternary / Q1_0 GEMV for a few tokens through warp-level fp16 MMAs; the token
 // activations' fragments must fit in shared memory (gemv_i8_hmma_fits(G)).

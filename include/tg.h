@@ -156,6 +156,18 @@ typedef struct tg_layout {
  */
 #define TG_FLAG_LNS8_STATE_SET 2
 
+/*
+ * Layout flag (TG_TERNARY_I8, TG_BINARY_Q1): the activations of tg_gemv_i8 are
+ * int64 fixed-point values (integer_engine.md §4.4) -- x points to int64
+ * [M][K], 16-byte aligned, passed through the int8_t pointer. Every sum and
+ * product of the apply is then taken modulo 2^64 (two's-complement wrapping,
+ * §5: the base-256 limb decomposition is exact modulo 2^64): the result is
+ * exact whenever no step leaves the int64 range, and there is no TG_ERR_BOUND
+ * check. Computed by signed base-256 digit planes of x, as many as the largest
+ * activation needs.
+ */
+#define TG_FLAG_X_INT64 4
+
 /* Static string naming a status code. Never NULL. */
 const char *tg_status_string(int status);
 

@@ -284,3 +284,10 @@ def test_lmhead_argument_errors():
     big.max_abs_scale = 1 << 31
     assert status_of(f, big, A256, A256, 10, None, A256, A256, A256, None, A256, wsb, 0) == tg.TG_ERR_BOUND
     assert tg.tg_lmhead_workspace_bytes(tg.tg_layout_init(tg.TG_TERNARY_I8, 8, 128), 4) == 0
+
+
+def test_layout_flags_are_distinct_bits():
+    import bit_decode_gemv_gb300 as tg
+    flags = [tg.TG_FLAG_CONST_WEIGHTS, tg.TG_FLAG_LNS8_STATE_SET, tg.TG_FLAG_X_INT64]
+    assert all(f & (f - 1) == 0 for f in flags)
+    assert len(set(flags)) == 3 and sum(flags) == (flags[0] | flags[1] | flags[2])

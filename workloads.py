@@ -51,6 +51,7 @@ _STREAM_IDS = {
     "signs": 11,
     "sparse_t": 12,
     "states": 13,
+    "x64": 14,
 }
 
 
@@ -104,6 +105,18 @@ def lns8_activations(seed: int, k: int) -> np.ndarray:
     code[zero] = 0
     sign = _rng(seed, "sign").integers(0, 2, size=k, dtype=np.int64)
     return ((sign << 7) | code).astype(np.uint8)
+
+
+def x_fixed64(seed: int, shape, frac_bits: int = 16, sigma: float = 1.0) -> np.ndarray:
+    """int64 fixed-point activations with frac_bits fractional bits:
+    rint(N(0, sigma^2) * 2^frac_bits)."""
+    return np.rint(_rng(seed, "x64").normal(0.0, sigma, size=shape) * float(1 << frac_bits)).astype(np.int64)
+
+
+def x_int64_full(seed: int, shape) -> np.ndarray:
+    """int64 activations uniform over the whole int64 range."""
+    return _rng(seed, "x64").integers(np.iinfo(np.int64).min, np.iinfo(np.int64).max, size=shape,
+                                      dtype=np.int64, endpoint=True)
 
 
 def lns8_activations_states(seed: int, k: int, n_states: int) -> np.ndarray:
