@@ -22,8 +22,9 @@ Also reported on the same line:
   roofline     the GEMV kernel's algorithmic bytes per launch / its average
                launch time, against the measured HBM copy bandwidth;
   cpu_baseline the CPU oracle timed on a bounded sample on the host cores;
-  rows         the other hot-path calls (LNS8, lm_head both paths, batched
-               M=64, Q1_0 and the floor shift at batch 1), each timed alone
+  rows         the other hot-path calls (LNS8 both routes, lm_head both paths,
+               batched M=64, Q1_0, the floor shift and int64 activations at
+               batch 1), each timed alone
                (skip with --no-rows);
   clocks       nvidia-smi SM clocks and throttle reasons during the timed region.
 
@@ -70,7 +71,7 @@ def parse():
     ap.add_argument("--sweep", default=None, choices=["lns8_routes", "gemv_m"],
                     help="run a measurement sweep instead of the bench and exit")
     ap.add_argument("--row", default=None,
-                    help="time only these rows (comma list of lns8, lm_head, batched, q1) and exit")
+                    help="time only these rows (comma list of lns8, lm_head, batched, q1, x64) and exit")
     a = ap.parse_args()
     if a.quick:
         a.no_rows = a.no_cpu = True
@@ -384,6 +385,32 @@ def _gemv_m1_row(tg, torch, stream, dev, kind, w, frac):
             "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "hbm", "copies": R}
 
 
+def row_x64(tg, torch, stream, dev):
+    """int64 fixed-point activations on the ffn_up shape, batch 1: Q.16 values
+    (three digit planes) and full-range values (eight)."""
+    hbm, _ = measured_peaks()
+    out = {}
+    w = W.ffn_up()
+    blob, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    L.flags |= tg.TG_FLAG_X_INT64
+    R = min(_copies_for(blob.size), 512)
+    wd = [dev(blob) for _ in range(R)]
+    y = torch.empty((1, L.N), dtype=torch.int64, device="cuda")
+    for key, x in (("x64_q16_ffn_up", W.x_fixed64(0, (1, L.K), frac_bits=16)),
+                   ("x64_full_ffn_up", W.x_int64_full(0, (1, L.K)))):
+        xd = dev(x)
+        g = capture_graph(torch, lambda i, h: tg.tg_gemv_i8(L, wd[i % R], xd, 1, y, h), R)
+        g.replay()
+        t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
+        alg = L.mask_bytes + L.scale_bytes + 8 * L.K + L.N * 8
+        out[key] = {"workload": "N=6912 K=2560 ternary, batch 1, int64 activations "
+                                + ("rint(N(0,1) 2^16)" if "q16" in key else "uniform over int64"),
+                    "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
+                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "copies": R}
+        del g
+    return out
+
+
 def row_q1(tg, torch, stream, dev):
     """Q1_0 binary weights and the per-group floor shift on the ffn_up shape, batch 1."""
     out = {}
@@ -396,7 +423,7 @@ def row_q1(tg, torch, stream, dev):
     return out
 
 
-ROWS = {"lns8": row_lns8, "lm_head": row_lm_head, "batched": row_batched, "q1": row_q1}
+ROWS = {"lns8": row_lns8, "lm_head": row_lm_head, "batched": row_batched, "q1": row_q1, "x64": row_x64}
 
 
 def measure_rows(tg, torch, stream, dev, names=None):
