@@ -33,6 +33,8 @@ def lib():
             "oracle_gemv_i8_frac": [i64, i64, i64, p, p, p, C.c_int, p],
             "oracle_gemv_q1": [i64, i64, i64, p, p, p, C.c_int, p],
             "oracle_gemv_x64": [i64, i64, i64, p, p, p, C.c_int, p],
+            "oracle_lns8_purelns": [i64, i64, p, p, p, C.c_int, p, p, p],
+            "oracle_lns_tables": [C.c_int, p, p, p],
             "oracle_lns8_direct": [i64, i64, p, p, p, p],
             "oracle_lns8_histogram": [i64, i64, p, p, p, p],
             "oracle_lns8_tile64": [i64, i64, p, p, p, p],
@@ -168,6 +170,40 @@ def _lns8(fn_name, t, dcode, xa):
 def lns8_direct(t, dcode, xa):
     """A[r][p] by direct eight-phase accumulation -> int64 [N][8]."""
     return _lns8("oracle_lns8_direct", t, dcode, xa)
+
+
+def lns_tables(F):
+    """(LOG8[0..128], KP[len], KM[len]) of the pure fractional-LNS reduction (BitState brief §5.2)."""
+    lib().oracle_lns_table_len.argtypes = [C.c_int]
+    lib().oracle_lns_table_len.restype = C.c_int64
+    n = int(lib().oracle_lns_table_len(int(F)))
+    if n < 0:
+        raise ValueError("F must be 1..6")
+    log8 = np.zeros(129, np.int64)
+    kp = np.zeros(n, np.int64)
+    km = np.zeros(n, np.int64)
+    _check(lib().oracle_lns_tables(int(F), log8.ctypes.data_as(C.c_void_p), kp.ctypes.data_as(C.c_void_p),
+                                   km.ctypes.data_as(C.c_void_p)), "oracle_lns_tables")
+    return log8, kp, km
+
+
+def lns8_purelns(t, dcode, xa, F):
+    """Pure fractional-LNS reduction of the LNS8 product states (BitState brief
+    §5.2, this library's reading; see oracle.c): (sign int64 [N], lam int64 [N]
+    = log magnitude * 2^F in code units, S fp64 [N])."""
+    t, pt = _c(t, np.int8)
+    dcode, pd = _c(dcode, np.uint8)
+    xa, px = _c(xa, np.uint8)
+    N, K = t.shape
+    if xa.shape != (K,) or dcode.shape != (N, K // 128):
+        raise ValueError("shape mismatch")
+    sign = np.zeros(N, np.int64)
+    lam = np.zeros(N, np.int64)
+    S = np.zeros(N, np.float64)
+    _check(lib().oracle_lns8_purelns(N, K, pt, pd, px, int(F), sign.ctypes.data_as(C.c_void_p),
+                                     lam.ctypes.data_as(C.c_void_p), S.ctypes.data_as(C.c_void_p)),
+           "oracle_lns8_purelns")
+    return sign, lam, S
 
 
 def lns8_histogram(t, dcode, xa):

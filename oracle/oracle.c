@@ -493,6 +493,151 @@ int oracle_lns8_stateset(int64_t N, int64_t K, const int8_t *t, const uint8_t *d
     return 0;
 }
 
+/*
+ * Pure fractional-LNS reduction ([BitState] §5.2), as this library reads it
+ * (the page fixes the primitives, not the table rounding or the tree shapes):
+ *
+ *   A value is (s, L): s in {-1, 0, +1} (0 = exact zero), L its log magnitude
+ *   in code units with F fractional bits, held as the integer L * 2^F; the
+ *   value is s * 2^((L - 74) / 8).
+ *   Count fold: a signed state population C != 0 of product code k becomes
+ *   (sign C, k * 2^F + LOG8[|C|]), LOG8[n] = round(8 log2(n) 2^F), n <= 128.
+ *   Pairwise add, hi = the operand with the larger L (the first on a tie),
+ *   diff = L_hi - L_lo:
+ *     same sign:     (s_hi, L_hi + KP[diff]),  KP[i] = round(8 log2(1 + 2^(-i / (8 2^F))) 2^F)
+ *     opposite sign: diff = 0 -> exact zero,
+ *                    else (s_hi, L_hi + KM[diff]), KM[i] = round(8 log2(1 - 2^(-i / (8 2^F))) 2^F)
+ *   with KP[i] = KM[i] = 0 from i = (8F + 40) 2^F on (both round to 0 there).
+ *   Balanced tree over 2^m values: add(tree(left half), tree(right half)).
+ *   Per row: each group's signed populations C_g[k] (k = a + d - 74 with the
+ *   zero / saturation rule of the direct route) are folded into buckets; per
+ *   phase p the sixteen band slots k = 8b + p form a tree; the groups' phase
+ *   aggregates form a tree over G padded with zeros to a power of two; the
+ *   eight phase aggregates form the final tree (8 -> 4 -> 2 -> 1).
+ * Rounding is round half away from zero (llround). 1 <= F <= 6.
+ * Output per row: sign[r], lam[r] (= L * 2^F) and S[r] = s * 2^((L - 74) / 8).
+ */
+typedef struct {
+    int8_t s;
+    int64_t lam;
+} oracle_lnsv;
+
+static int64_t oracle_lns_len(int F) { return (int64_t)(8 * F + 40) << F; }
+
+static oracle_lnsv oracle_lns_add(oracle_lnsv u, oracle_lnsv v, const int64_t *KP, const int64_t *KM, int64_t len)
+{
+    if (u.s == 0)
+        return v;
+    if (v.s == 0)
+        return u;
+    const oracle_lnsv hi = u.lam >= v.lam ? u : v;
+    const oracle_lnsv lo = u.lam >= v.lam ? v : u;
+    const int64_t diff = hi.lam - lo.lam;
+    oracle_lnsv r = hi;
+    if (hi.s == lo.s) {
+        r.lam = hi.lam + (diff < len ? KP[diff] : 0);
+    } else if (diff == 0) {
+        r.s = 0;
+        r.lam = 0;
+    } else {
+        r.lam = hi.lam + (diff < len ? KM[diff] : 0);
+    }
+    return r;
+}
+
+static oracle_lnsv oracle_lns_tree(const oracle_lnsv *v, int64_t n, const int64_t *KP, const int64_t *KM,
+                                   int64_t len)
+{
+    if (n == 1)
+        return v[0];
+    return oracle_lns_add(oracle_lns_tree(v, n / 2, KP, KM, len), oracle_lns_tree(v + n / 2, n / 2, KP, KM, len),
+                          KP, KM, len);
+}
+
+/* The three tables of the pure-LNS reduction for F fractional bits (definitions above). */
+int oracle_lns_tables(int F, int64_t *LOG8 /*[129]*/, int64_t *KP /*[len]*/, int64_t *KM /*[len]*/)
+{
+    if (F < 1 || F > 6)
+        return -1;
+    const double scale = ldexp(1.0, F);
+    const int64_t len = oracle_lns_len(F);
+    LOG8[0] = 0;
+    for (int n = 1; n <= 128; n++)
+        LOG8[n] = llround(8.0 * log2((double)n) * scale);
+    for (int64_t i = 0; i < len; i++) {
+        const double q = exp2(-(double)i / (8.0 * scale));
+        KP[i] = llround(8.0 * log2(1.0 + q) * scale);
+        KM[i] = i == 0 ? 0 : llround(8.0 * log2(1.0 - q) * scale);
+    }
+    return 0;
+}
+
+int64_t oracle_lns_table_len(int F) { return (F < 1 || F > 6) ? -1 : oracle_lns_len(F); }
+
+int oracle_lns8_purelns(int64_t N, int64_t K, const int8_t *t, const uint8_t *dcode, const uint8_t *xa, int F,
+                        int64_t *sign, int64_t *lam, double *S)
+{
+    if (N < 1 || K < ORACLE_GROUP || K % ORACLE_GROUP != 0 || F < 1 || F > 6)
+        return -1;
+    const int64_t G = K / ORACLE_GROUP;
+    int64_t Gp = 1;
+    while (Gp < G)
+        Gp *= 2;
+    const int64_t len = oracle_lns_len(F);
+    int64_t LOG8[129];
+    int64_t *KP = malloc(sizeof(int64_t) * (size_t)len);
+    int64_t *KM = malloc(sizeof(int64_t) * (size_t)len);
+    oracle_lnsv *gagg = malloc(sizeof(oracle_lnsv) * (size_t)(8 * Gp));   /* [phase][group] */
+    if (!KP || !KM || !gagg) {
+        free(KP);
+        free(KM);
+        free(gagg);
+        return -1;
+    }
+    oracle_lns_tables(F, LOG8, KP, KM);
+    for (int64_t r = 0; r < N; r++) {
+        for (int64_t g = 0; g < Gp; g++) {
+            int64_t C[128];
+            memset(C, 0, sizeof(C));
+            if (g < G) {
+                for (int64_t i = g * ORACLE_GROUP; i < (g + 1) * ORACLE_GROUP; i++) {
+                    const int tv = t[r * K + i];
+                    const int a = xa[i] & 0x7f;
+                    if (tv == 0 || a == 0)
+                        continue;
+                    int k = a + (int)dcode[r * G + g] - 74;
+                    if (k <= 0)
+                        continue;
+                    if (k > 127)
+                        k = 127;
+                    const int neg = (tv < 0) ^ (xa[i] >> 7);
+                    C[k] += neg ? -1 : 1;
+                }
+            }
+            for (int p = 0; p < 8; p++) {
+                oracle_lnsv slots[16];
+                for (int b = 0; b < 16; b++) {
+                    const int64_t c = C[8 * b + p];
+                    slots[b].s = (int8_t)(c > 0 ? 1 : (c < 0 ? -1 : 0));
+                    slots[b].lam = c == 0 ? 0 : (int64_t)(8 * b + p) * ((int64_t)1 << F) + LOG8[c < 0 ? -c : c];
+                }
+                gagg[p * Gp + g] = oracle_lns_tree(slots, 16, KP, KM, len);
+            }
+        }
+        oracle_lnsv ph[8];
+        for (int p = 0; p < 8; p++)
+            ph[p] = oracle_lns_tree(gagg + p * Gp, Gp, KP, KM, len);
+        const oracle_lnsv R = oracle_lns_tree(ph, 8, KP, KM, len);
+        sign[r] = R.s;
+        lam[r] = R.s == 0 ? 0 : R.lam;
+        S[r] = R.s == 0 ? 0.0 : (double)R.s * exp2(((double)R.lam / ldexp(1.0, F) - 74.0) / 8.0);
+    }
+    free(KP);
+    free(KM);
+    free(gagg);
+    return 0;
+}
+
 /* F[p] = 2^((p - 2) / 8) ([BitState] §3), as fp64 from libm's exp2. */
 void oracle_lns8_F(double F[8])
 {

@@ -586,3 +586,94 @@ def test_x64_wraparound_closed_forms():
     x3 = np.zeros((1, K), np.int64)
     x3[0, 0] = 1 << 62
     assert oracle.gemv_x64(t3, np.full((1, 1), 2, np.int32), x3, 1)[0, 0] == -(1 << 62)
+
+
+# ---------------------------------------------------------------------------
+# Pure fractional-LNS reduction (BitState brief §5.2): approximate, so no
+# end-to-end exact pin; its parts are pinned where the mathematics fixes them.
+# ---------------------------------------------------------------------------
+
+def _hp_log8(v, F):
+    """round-free 8 log2(v) 2^F in 50-digit decimal arithmetic."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    return Decimal(8) * (Decimal(v).ln() / Decimal(2).ln()) * (Decimal(2) ** F)
+
+
+@pytest.mark.parametrize("F", [1, 2, 3, 4, 5, 6])
+def test_lns_tables_are_the_rounded_closed_forms(F):
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    log8, kp, km = oracle.lns_tables(F)
+    one = Decimal(1)
+    assert log8[1] == 0 and kp[0] == 8 << F and kp[-1] == 0 and km[-1] == 0
+    for j in range(8):
+        assert log8[1 << j] == 8 * j << F            # powers of two are exact
+    for n in (3, 5, 7, 100, 127, 128):
+        assert abs(Decimal(int(log8[n])) - _hp_log8(n, F)) <= Decimal("0.5")
+    scale = Decimal(8) * (Decimal(2) ** F)
+    for i in list(range(1, 40)) + list(range(40, len(kp), max(1, len(kp) // 50))):
+        q = (-(Decimal(i) / scale) * Decimal(2).ln()).exp()     # 2^(-i / (8 2^F))
+        assert abs(Decimal(int(kp[i])) - _hp_log8(one + q, F)) <= Decimal("0.5")
+        assert abs(Decimal(int(km[i])) - _hp_log8(one - q, F)) <= Decimal("0.5")
+    assert np.all(np.diff(kp) <= 0) and np.all(np.diff(km[1:]) >= 0) and np.all(km[1:] <= 0)
+
+
+def _one_group(N, lanes):
+    """LNS8 weights with the given (row, lane, trit) nonzeros in one 128-lane group."""
+    t = np.zeros((N, 128), np.int8)
+    for r, i, v in lanes:
+        t[r, i] = v
+    return t
+
+
+@pytest.mark.parametrize("F", [1, 4, 6])
+def test_purelns_exact_cases(F):
+    xa = np.zeros(128, np.uint8)
+    xa[3] = 90                 # +2^(16/8)
+    xa[7] = 90                 # the same state
+    xa[9] = 0x80 | 60          # -2^(-14/8)
+    dcode = np.full((5, 1), 74, np.uint8)    # e = 0: k = a
+    t = _one_group(5, [(0, 3, 1),                  # one lane: (+, 90) exactly
+                       (1, 3, 1), (1, 7, 1),       # two lanes of one state: +8 codes exactly
+                       (2, 3, 1), (2, 7, -1),      # a state whose population cancels: zero
+                       (3, 9, 1),                  # one negative lane
+                       (4, 3, -1), (4, 7, -1)])    # two negative lanes of one state
+    s, lam, S = oracle.lns8_purelns(t, dcode, xa, F)
+    assert (s[0], lam[0]) == (1, 90 << F)
+    assert (s[1], lam[1]) == (1, 98 << F)
+    assert (s[2], lam[2]) == (0, 0) and S[2] == 0.0
+    assert (s[3], lam[3]) == (-1, 60 << F)
+    assert (s[4], lam[4]) == (-1, 98 << F)
+    assert S[0] == 4.0 and S[1] == 8.0          # 2^((90 - 74) / 8), doubled
+
+
+def test_purelns_opposite_equal_buckets_cancel_across_groups():
+    """The same magnitude with opposite signs in two groups meets in the group
+    tree and cancels to exact zero."""
+    xa = np.zeros(256, np.uint8)
+    xa[5] = 100
+    xa[128 + 5] = 100
+    t = np.zeros((1, 256), np.int8)
+    t[0, 5] = 1
+    t[0, 128 + 5] = -1
+    s, lam, S = oracle.lns8_purelns(t, np.full((1, 2), 74, np.uint8), xa, 3)
+    assert s[0] == 0 and S[0] == 0.0
+
+
+@pytest.mark.parametrize("F", [1, 2, 3, 4, 5, 6])
+def test_purelns_error_bound_without_cancellation(F):
+    """All terms positive: each table rounding moves L by at most 1/2 unit of
+    2^-F codes and positive sums do not amplify it, so along any path to the
+    root (one count fold, 4 band levels, log2(G) group levels, 3 phase levels)
+    |log error| <= (depth + 1) / 2 * 2^-F codes."""
+    N, K = 64, 1024
+    w = W.lns8(seed=F, N=N, K=K)
+    t = np.abs(w["t"])
+    xa = w["xa"] & 0x7F
+    s, lam, S = oracle.lns8_purelns(t, w["dcode"], xa, F)
+    exact = oracle.lns8_materialise(oracle.lns8_direct(t, w["dcode"], xa))
+    depth = 4 + int(np.log2(K // 128)) + 3
+    bound = 2.0 ** ((depth + 1) * 0.5 * 2.0 ** -F / 8) - 1
+    rel = np.abs(S / exact - 1)
+    assert np.all(s == 1) and np.all(rel <= bound * (1 + 1e-12)), (float(rel.max()), bound)
