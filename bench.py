@@ -68,7 +68,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row figures")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--quick", action="store_true", help="= --no-rows --no-cpu (for profiler runs)")
-    ap.add_argument("--sweep", default=None, choices=["lns8_routes", "gemv_m"],
+    ap.add_argument("--sweep", default=None, choices=["lns8_routes", "gemv_m", "lns8_purelns"],
                     help="run a measurement sweep instead of the bench and exit")
     ap.add_argument("--row", default=None,
                     help="time only these rows (comma list of lns8, lm_head, batched, q1, x64) and exit")
@@ -298,14 +298,17 @@ def row_lns8(tg, torch, stream, dev):
     S = torch.empty((L.N,), dtype=torch.float64, device="cuda")
     alg = L.mask_bytes + L.N * L.G + L.K + L.N * 8 * 8 + L.N * 8
     out = {}
-    for key, flags in (("lns8", 0), ("lns8_stateset", tg.TG_FLAG_LNS8_STATE_SET)):
+    for key, flags in (("lns8", 0), ("lns8_stateset", tg.TG_FLAG_LNS8_STATE_SET),
+                       ("lns8_purelns_f4", tg.TG_FLAG_LNS8_PURE_LNS)):
         Lr = tg.tg_layout.from_buffer_copy(L)
         Lr.flags = flags
+        Lr.frac = 4 if flags == tg.TG_FLAG_LNS8_PURE_LNS else 0
         g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(Lr, wd[i % R], xa, A, S, h), R)
         g.replay()
         t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
-        out[key] = {"workload": "N=4096 K=4096 LNS8 eight-phase, "
-                                + ("state-population route" if flags else "direct route"),
+        route = {0: "direct route", tg.TG_FLAG_LNS8_STATE_SET: "state-population route",
+                 tg.TG_FLAG_LNS8_PURE_LNS: "pure fractional-LNS route, F = 4 (approximate)"}[flags]
+        out[key] = {"workload": "N=4096 K=4096 LNS8 eight-phase, " + route,
                     "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
                     "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}
         del g
@@ -492,6 +495,56 @@ def run_sweep_lns8_routes(args):
         r = _lns8_route_point(tg, torch, stream, dev, w)
         print(json.dumps({"sweep": "zero_density", "N": 4096, "K": K, "zero_frac": round(z, 3), **r}),
               flush=True)
+        torch.cuda.empty_cache()
+
+
+def run_sweep_lns8_purelns(args):
+    """Error study of the pure fractional-LNS route against the exact direct
+    route by internal precision F, and its per-call time (N = K = 4096): the
+    LNS8 workload (signed sums) and the same rows with every term positive."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from bit_decode_gemv_gb300 import build as tgbuild
+    tgbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    for name in ("signed", "positive"):
+        w = W.lns8()
+        if name == "positive":
+            w["t"] = np.abs(w["t"])
+            w["xa"] = w["xa"] & 0x7F
+        blob, L = tg.tg_pack_weights(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+        R = min(_copies_for(blob.size), 128)
+        wd = [dev(blob) for _ in range(R)]
+        xa = dev(w["xa"])
+        A = torch.empty((L.N, 8), dtype=torch.int64, device="cuda")
+        S_exact = torch.empty((L.N,), dtype=torch.float64, device="cuda")
+        tg.tg_gemv_lns8_phase(L, wd[0], xa, A, S_exact)
+        S = torch.empty((L.N,), dtype=torch.float64, device="cuda")
+        for F in range(1, 7):
+            Lp = tg.tg_layout.from_buffer_copy(L)
+            Lp.flags = tg.TG_FLAG_LNS8_PURE_LNS
+            Lp.frac = F
+            g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(Lp, wd[i % R], xa, A, S, h), R)
+            g.replay()
+            t = event_time(torch, lambda i: g.replay(), 3, stream) / (3 * R)
+            del g
+            tg.tg_gemv_lns8_phase(Lp, wd[0], xa, A, S)
+            torch.cuda.synchronize()
+            se, sp = S_exact.cpu().numpy(), S.cpu().numpy()
+            nz = se != 0
+            rel = np.abs(sp[nz] / se[nz] - 1.0)
+            print(json.dumps({"sweep": "lns8_purelns", "terms": name, "F": F, "N": L.N, "K": L.K,
+                              "us": round(t * 1e6, 3),
+                              "rel_err_median": float(np.median(rel)), "rel_err_p90": float(np.quantile(rel, 0.9)),
+                              "rel_err_p99": float(np.quantile(rel, 0.99)), "rel_err_max": float(rel.max()),
+                              "sign_mismatch_rows": int(np.sum(np.sign(sp) != np.sign(se))),
+                              "rows": int(L.N)}), flush=True)
+        del wd
         torch.cuda.empty_cache()
 
 
@@ -709,6 +762,8 @@ def main():
         run_sweep_lns8_routes(args)
     elif args.sweep == "gemv_m":
         run_sweep_gemv_m(args)
+    elif args.sweep == "lns8_purelns":
+        run_sweep_lns8_purelns(args)
     elif args.row:
         run_row_only(args)
     elif args.impl == "reference":

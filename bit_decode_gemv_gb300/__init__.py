@@ -39,6 +39,7 @@ TG_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 TG_FLAG_CONST_WEIGHTS = 1
 TG_FLAG_LNS8_STATE_SET = 2
 TG_FLAG_X_INT64 = 4
+TG_FLAG_LNS8_PURE_LNS = 8
 
 # Every symbol include/tg.h declares.
 EXPORTS = (

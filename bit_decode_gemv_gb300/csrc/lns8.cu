@@ -319,8 +319,11 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
 {
     if (!L || !w || !xa || !A)
         return TG_ERR_ARG;
-    if (L->kind != TG_TERNARY_LNS8 || L->version != 1 || L->frac != 0)
+    const bool pure = (L->flags & TG_FLAG_LNS8_PURE_LNS) != 0;
+    if (L->kind != TG_TERNARY_LNS8 || L->version != 1)
         return TG_ERR_ARG;
+    if (pure ? (L->frac < 1 || L->frac > 6 || (L->flags & TG_FLAG_LNS8_STATE_SET)) : L->frac != 0)
+        return TG_ERR_ARG;   // frac is the pure route's internal precision, 0 otherwise
     if (!tgi::aligned(w, 256) || !tgi::aligned(xa, 16) || !tgi::aligned(A, 8) ||
         (S && !tgi::aligned(S, 8)))
         return TG_ERR_ARG;
@@ -340,6 +343,8 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
     const int G = (int)L->G, N = (int)L->N;
     if (L->flags & TG_FLAG_LNS8_STATE_SET)
         return tgi::lns8_stateset(masks, codes, xa, A, S, F.f, N, G, (int)L->tiles, s);
+    if (pure)
+        return tgi::lns8_purelns(masks, codes, xa, A, S, N, G, (int)L->frac, s);
     const int gpc = (G + kMaxCluster - 1) / kMaxCluster;   // groups per CTA
     const int csize = (G + gpc - 1) / gpc;                 // CTAs per cluster, <= 8
 

@@ -1,0 +1,293 @@
+// lns8_purelns.cu -- the pure fractional-LNS reduction of the LNS8 product
+// states (BitState brief §5.2), selected by TG_FLAG_LNS8_PURE_LNS on
+// tg_gemv_lns8_phase. Approximate by design: there is no linear accumulator,
+// every addition is a log-domain pairwise add with table corrections.
+//
+// Definition (this library's reading of §5.2; the oracle states the same):
+//   value (s, L): s in {-1, 0, +1}, L = log magnitude in code units held as
+//   the integer L * 2^F (F = internal fractional bits, 1..6); the value is
+//   s * 2^((L - 74) / 8).
+//   Count fold: a signed state population C != 0 of product code k becomes
+//   (sign C, k 2^F + LOG8[|C|]), LOG8[n] = round(8 log2 n 2^F).
+//   Pairwise add, hi = the operand with the larger L (the first on a tie),
+//   diff = L_hi - L_lo: same sign -> L_hi + KP[diff]; opposite sign -> zero
+//   if diff = 0, else L_hi + KM[diff]; KP[i] = round(8 log2(1 + 2^(-i/(8 2^F))) 2^F),
+//   KM[i] = round(8 log2(1 - 2^(-i/(8 2^F))) 2^F), both 0 from (8F + 40) 2^F on.
+//   Trees are balanced, left half first: per (group, phase p) over the sixteen
+//   band slots k = 8b + p, per phase over the groups padded with zeros to a
+//   power of two, then over the eight phases.
+//
+// Mapping: one warp per row, lane = group (or a run of groups when there are
+// more than 32: a lane's local tree over its run, then the warp tree). A lane
+// reads its row's four 16-byte LNS8 entries for the group, compacts them into
+// W_nonzero / W_negative words (the byte-permute conversion of the state-set
+// route), walks the set bits into a 128-bin population histogram in shared
+// memory, and folds each phase's sixteen band slots. The group tree is a
+// shuffle tree (lane i combines with lane i + 2^l, left operand first), and
+// lane 0 reduces the eight phases. The tables are computed on the host from
+// the definitions above and passed as a kernel parameter (23 KB at F = 6).
+//
+// Output: A[r][0] = s, A[r][1] = L * 2^F, A[r][2..7] = 0, and
+// S[r] = s * 2^((L - 74) / 8) in fp64.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "tg.h"
+#include "tg_internal.h"
+
+namespace {
+
+constexpr int kWarps = 8;             // rows per CTA (one warp each)
+constexpr int kMaxF = 6;
+constexpr int kLenMax = (8 * kMaxF + 40) << kMaxF;   // table length at F = 6
+constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int kLog8 = 136;   // LOG8 entries stored ([0..128] used; 136 keeps what follows 16-byte aligned)
+
+struct LnsTables {
+    int16_t log8[kLog8];
+    int16_t kp[kLenMax];
+    int16_t km[kLenMax];
+};
+static_assert(sizeof(LnsTables) < 30 * 1024, "kernel parameter space");
+
+struct Lv {
+    int s;     // -1, 0, +1
+    int lam;   // log magnitude * 2^F (meaningless when s = 0)
+};
+
+__device__ __forceinline__ Lv lns_add(Lv u, Lv v, const int16_t *kp, const int16_t *km, int len)
+{
+    if (u.s == 0)
+        return v;
+    if (v.s == 0)
+        return u;
+    const bool uhi = u.lam >= v.lam;
+    const Lv hi = uhi ? u : v, lo = uhi ? v : u;
+    const int diff = hi.lam - lo.lam;
+    Lv r = hi;
+    if (hi.s == lo.s)
+        r.lam = hi.lam + (diff < len ? kp[diff] : 0);
+    else if (diff == 0)
+        r = Lv{0, 0};
+    else
+        r.lam = hi.lam + (diff < len ? km[diff] : 0);
+    return r;
+}
+
+__device__ __forceinline__ Lv shfl_down(Lv v, int d)
+{
+    return Lv{__shfl_down_sync(kFull, v.s, d), __shfl_down_sync(kFull, v.lam, d)};
+}
+
+// Group lane held at bit `bit` of compact word j (as in the state-set route).
+__device__ __forceinline__ int lane_col(int j, int bit)
+{
+    const int x = 7 - (bit & 7);
+    const int c = (x >> 2) + 2 * ((bit >> 3) & 1) + 4 * (x & 1);
+    return 16 * c + 2 * j + 8 * ((x >> 1) & 1) + (bit >> 4);
+}
+
+// One 16-byte LNS8 entry -> compact W_nonzero / W_negative words of its two
+// rows (q: *0, q + 8: *1).
+__device__ __forceinline__ void convert_word(uint4 w, uint32_t &nz0, uint32_t &ng0, uint32_t &nz1, uint32_t &ng1)
+{
+    const uint32_t nza0 = __byte_perm(w.x, w.y, 0x6240), nga0 = __byte_perm(w.x, w.y, 0x7351);
+    const uint32_t nza1 = __byte_perm(w.z, w.w, 0x6240), nga1 = __byte_perm(w.z, w.w, 0x7351);
+    nz0 = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
+    nz1 = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
+    ng0 = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
+    ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
+}
+
+// The eight phase aggregates of one (row, group): population histogram, count
+// fold, a balanced tree over the sixteen band slots of each phase.
+__device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, short *bins,
+                             const int16_t *log8, const int16_t *kp, const int16_t *km, int len, int F, Lv (&ph)[8])
+{
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+        reinterpret_cast<uint4 *>(bins)[k] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        uint32_t nz0, ng0, nz1, ng1;
+        convert_word(tgi::ldg_stream(ent + j), nz0, ng0, nz1, ng1);
+        uint32_t nz = half ? nz1 : nz0;
+        const uint32_t ng = half ? ng1 : ng0;
+        while (nz) {
+            const int b = __ffs((int)nz) - 1;
+            nz &= nz - 1u;
+            const unsigned a = xg[lane_col(j, b)];
+            const int code = (int)(a & 0x7fu);
+            int k = code + e;
+            if (code == 0 || k <= 0)
+                continue;
+            k = min(k, 127);
+            bins[k] += (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
+        }
+    }
+#pragma unroll 1
+    for (int p = 0; p < 8; p++) {
+        Lv v[16];
+#pragma unroll
+        for (int b = 0; b < 16; b++) {
+            const int c = bins[8 * b + p];
+            v[b] = c == 0 ? Lv{0, 0} : Lv{c > 0 ? 1 : -1, ((8 * b + p) << F) + log8[c > 0 ? c : -c]};
+        }
+#pragma unroll
+        for (int w = 1; w < 16; w *= 2)
+#pragma unroll
+            for (int i = 0; i < 16; i += 2 * w)
+                v[i] = lns_add(v[i], v[i + w], kp, km, len);
+        ph[p] = v[0];
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
+                    const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S, int N, int G,
+                    int Gp, int F, int len, const __grid_constant__ LnsTables T)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    int16_t *log8 = reinterpret_cast<int16_t *>(smem);                  // [kLog8]
+    int16_t *kp = log8 + kLog8;                                         // [kLenMax]
+    int16_t *km = kp + kLenMax;                                         // [kLenMax]
+    short *bins_all = reinterpret_cast<short *>(km + kLenMax);          // [kWarps * 32][128]
+    uint8_t *xs = reinterpret_cast<uint8_t *>(bins_all + kWarps * 32 * 128);   // [G * 128], 16-byte aligned
+    static_assert(((kLog8 + 2 * kLenMax) * 2 + kWarps * 32 * 128 * 2) % 16 == 0, "xs alignment");
+
+    for (int i = threadIdx.x; i < kLog8; i += blockDim.x)
+        log8[i] = T.log8[i];
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+        kp[i] = T.kp[i];
+        km[i] = T.km[i];
+    }
+    for (int i = threadIdx.x; i < G * 128 / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(xa) + i);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + warp;
+    if (row >= N)
+        return;
+    short *bins = bins_all + (size_t)threadIdx.x * 128;
+    const int blk = row >> 4, q = row & 7, half = (row >> 3) & 1;
+    const int gpl = Gp > 32 ? Gp / 32 : 1;   // groups per lane
+
+    // this lane's phase aggregates: a tree over its run of groups
+    Lv ph[8];
+#pragma unroll
+    for (int p = 0; p < 8; p++)
+        ph[p] = Lv{0, 0};
+    if (lane * gpl < Gp) {
+        Lv run[8][8];   // [phase][level] partial trees of the run (gpl <= 2^7 groups)
+        int filled = 0;
+        for (int i = 0; i < gpl; i++) {
+            const int g = lane * gpl + i;
+            Lv cur[8];
+            if (g < G) {
+                const uint4 *ent = masks + ((size_t)blk * G + g) * 32 + 4 * q;
+                const int e = (int)codes[((size_t)blk * G + g) * 16 + (row & 15)] - 74;
+                group_phases(ent, half, xs + (size_t)g * 128, e, bins, log8, kp, km, len, F, cur);
+            } else {
+#pragma unroll
+                for (int p = 0; p < 8; p++)
+                    cur[p] = Lv{0, 0};
+            }
+            // binary-counter merge: after 2^m groups the level-m slot holds
+            // the balanced tree of those 2^m groups, left half first
+            int lvl = 0;
+            for (int c = i; c & 1; c >>= 1, lvl++)
+#pragma unroll
+                for (int p = 0; p < 8; p++)
+                    cur[p] = lns_add(run[p][lvl], cur[p], kp, km, len);
+#pragma unroll
+            for (int p = 0; p < 8; p++)
+                run[p][lvl] = cur[p];
+            filled = lvl;
+        }
+#pragma unroll
+        for (int p = 0; p < 8; p++)
+            ph[p] = run[p][filled];
+    }
+    // the tree over the lanes' runs, left operand first
+    for (int d = 1; d < 32 && d * gpl < Gp; d *= 2)
+#pragma unroll
+        for (int p = 0; p < 8; p++) {
+            const Lv o = shfl_down(ph[p], d);
+            if ((lane & (2 * d - 1)) == 0)
+                ph[p] = lns_add(ph[p], o, kp, km, len);
+        }
+    if (lane == 0) {
+#pragma unroll
+        for (int w = 1; w < 8; w *= 2)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2 * w)
+                ph[i] = lns_add(ph[i], ph[i + w], kp, km, len);
+        const Lv R = ph[0];
+        int64_t *a = A + (size_t)row * 8;
+        a[0] = R.s;
+        a[1] = R.s == 0 ? 0 : R.lam;
+#pragma unroll
+        for (int p = 2; p < 8; p++)
+            a[p] = 0;
+        if (S)
+            S[row] = R.s == 0 ? 0.0 : (double)R.s * exp2(((double)R.lam / (double)(1 << F) - 74.0) / 8.0);
+    }
+}
+
+// The tables of the definition above, on the host.
+void build_tables(int F, LnsTables &T, int &len)
+{
+    const double scale = std::ldexp(1.0, F);
+    len = (8 * F + 40) << F;
+    for (int i = 0; i < kLog8; i++)
+        T.log8[i] = 0;
+    for (int n = 1; n <= 128; n++)
+        T.log8[n] = (int16_t)std::llround(8.0 * std::log2((double)n) * scale);
+    for (int i = 0; i < kLenMax; i++) {
+        if (i >= len) {
+            T.kp[i] = T.km[i] = 0;
+            continue;
+        }
+        const double q = std::exp2(-(double)i / (8.0 * scale));
+        T.kp[i] = (int16_t)std::llround(8.0 * std::log2(1.0 + q) * scale);
+        T.km[i] = i == 0 ? (int16_t)0 : (int16_t)std::llround(8.0 * std::log2(1.0 - q) * scale);
+    }
+}
+
+}  // namespace
+
+namespace tgi {
+
+int lns8_purelns(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S, int N, int G,
+                 int F, cudaStream_t s)
+{
+    if (F < 1 || F > kMaxF)
+        return TG_ERR_ARG;
+    static LnsTables tables[kMaxF + 1];
+    static int lens[kMaxF + 1];
+    static std::once_flag once[kMaxF + 1];
+    std::call_once(once[F], [F] { build_tables(F, tables[F], lens[F]); });   // host tables, once per F
+    int Gp = 1;
+    while (Gp < G)
+        Gp *= 2;
+    if (Gp > 32 * 128)   // a lane's run of groups is at most 128 (the run's eight tree levels)
+        return TG_ERR_SHAPE;
+    const size_t smem = (kLog8 + 2 * (size_t)kLenMax) * 2 + (size_t)kWarps * 32 * 128 * 2 + (size_t)G * 128;
+    if (smem > 227 * 1024)
+        return TG_ERR_SHAPE;
+    cudaError_t e = cudaFuncSetAttribute(lns8_purelns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return TG_ERR_CUDA;
+    lns8_purelns_kernel<<<(N + kWarps - 1) / kWarps, kWarps * 32, smem, s>>>(masks, codes, xa, A, S, N, G, Gp, F,
+                                                                              lens[F], tables[F]);
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+}  // namespace tgi

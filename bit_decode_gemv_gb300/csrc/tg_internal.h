@@ -44,4 +44,9 @@ int gemv_i8_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int
 int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S,
                   const double F[8], int N, int G, int tiles, cudaStream_t s);
 
+// LNS8 by the pure fractional-LNS reduction (TG_FLAG_LNS8_PURE_LNS), F
+// internal fractional bits (1..6); arguments as checked by tg_gemv_lns8_phase.
+int lns8_purelns(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S, int N, int G,
+                 int F, cudaStream_t s);
+
 }  // namespace tgi

@@ -132,7 +132,8 @@ typedef struct tg_layout {
     int64_t max_abs_scale;  /* max |scale| seen when packing (0 from tg_layout_init) */
     int64_t flags;          /* TG_FLAG_* bits, 0 after packing; the caller may set them */
     int64_t frac;           /* per-group floor shift (TG_TERNARY_I8, TG_BINARY_Q1): 0..62;
-                               0 after packing; the caller may set it; 0 for other kinds */
+                               internal fractional bits of the pure-LNS route (TG_TERNARY_LNS8
+                               with TG_FLAG_LNS8_PURE_LNS): 1..6; otherwise 0. 0 after packing */
     int64_t reserved[2];
 } tg_layout;
 
@@ -167,6 +168,19 @@ typedef struct tg_layout {
  * activation needs.
  */
 #define TG_FLAG_X_INT64 4
+
+/*
+ * Layout flag (TG_TERNARY_LNS8): tg_gemv_lns8_phase takes the pure
+ * fractional-LNS reduction of the BitState brief §5.2 -- no linear
+ * accumulator; signed state populations are folded into log-domain buckets
+ * and summed by pairwise kappa+/kappa- adds from tables with layout->frac
+ * (1..6) internal fractional bits, in balanced trees over the bands, the
+ * groups and the eight phases. Approximate by design. Outputs: A[r][0] = sign
+ * (-1, 0, +1), A[r][1] = log magnitude in code units times 2^frac,
+ * A[r][2..7] = 0; S[r] (if not NULL) = sign * 2^((A[r][1] / 2^frac - 74) / 8).
+ * Not combinable with TG_FLAG_LNS8_STATE_SET.
+ */
+#define TG_FLAG_LNS8_PURE_LNS 8
 
 /* Static string naming a status code. Never NULL. */
 const char *tg_status_string(int status);

@@ -257,6 +257,17 @@ def test_lns8_argument_errors():
     fr = tg.tg_layout.from_buffer_copy(L)
     fr.frac = 3                                                                # no floor for LNS8
     assert status_of(f, fr, A256, A256, A256, None, 0) == tg.TG_ERR_ARG
+    # the pure-LNS route takes frac = 1..6 as its internal precision, and not
+    # together with the state-set route
+    for frac in (0, 7, -1):
+        pl = tg.tg_layout.from_buffer_copy(L)
+        pl.flags = tg.TG_FLAG_LNS8_PURE_LNS
+        pl.frac = frac
+        assert status_of(f, pl, A256, A256, A256, None, 0) == tg.TG_ERR_ARG
+    both = tg.tg_layout.from_buffer_copy(L)
+    both.flags = tg.TG_FLAG_LNS8_PURE_LNS | tg.TG_FLAG_LNS8_STATE_SET
+    both.frac = 3
+    assert status_of(f, both, A256, A256, A256, None, 0) == tg.TG_ERR_ARG
 
 
 def test_lmhead_argument_errors():
@@ -288,6 +299,6 @@ def test_lmhead_argument_errors():
 
 def test_layout_flags_are_distinct_bits():
     import bit_decode_gemv_gb300 as tg
-    flags = [tg.TG_FLAG_CONST_WEIGHTS, tg.TG_FLAG_LNS8_STATE_SET, tg.TG_FLAG_X_INT64]
+    flags = [tg.TG_FLAG_CONST_WEIGHTS, tg.TG_FLAG_LNS8_STATE_SET, tg.TG_FLAG_X_INT64, tg.TG_FLAG_LNS8_PURE_LNS]
     assert all(f & (f - 1) == 0 for f in flags)
-    assert len(set(flags)) == 3 and sum(flags) == (flags[0] | flags[1] | flags[2])
+    assert len(set(flags)) == len(flags) and sum(flags) == (flags[0] | flags[1] | flags[2] | flags[3])

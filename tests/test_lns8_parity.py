@@ -135,3 +135,56 @@ def test_routes_agree_bitwise_on_the_workload():
     A1, S1 = check(w, route="stateset")
     np.testing.assert_array_equal(A0, A1)
     np.testing.assert_array_equal(S0.view(np.int64), S1.view(np.int64))
+
+
+
+# ---------------------------------------------------------------------------
+# Pure fractional-LNS route (TG_FLAG_LNS8_PURE_LNS): approximate by design, so
+# the comparison is with the oracle's statement of the same reduction: sign
+# and log magnitude bit-exact, S within the rounding of the final fp64 exp2.
+# ---------------------------------------------------------------------------
+
+def check_pure(w, F, with_S=True):
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import lns8, pack_to_device
+    wd, L = pack_to_device(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    L.flags |= tg.TG_FLAG_LNS8_PURE_LNS
+    L.frac = F
+    A, S = lns8(wd, L, w["xa"], with_S)
+    s_ref, lam_ref, S_ref = oracle.lns8_purelns(w["t"], w["dcode"], w["xa"], F)
+    np.testing.assert_array_equal(A[:, 0], s_ref)
+    np.testing.assert_array_equal(A[:, 1], lam_ref)
+    assert not A[:, 2:].any()
+    if with_S:
+        np.testing.assert_allclose(S, S_ref, rtol=1e-14, atol=0)
+    return A, S
+
+
+@pytest.mark.parametrize("F", [1, 2, 3, 4, 5, 6])
+def test_purelns_workload_full_size(F):
+    check_pure(W.lns8(), F)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 384), (95, 4096), (40, 12800), (17, 32768)])
+def test_purelns_shapes_and_clamps(N, K):
+    """Ragged N; one group; more groups than lanes (a lane's run of groups,
+    K = 12800 and 32768); codes and scale codes over the whole byte range."""
+    check_pure(wide(N, N, K), 4)
+
+
+@pytest.mark.parametrize("F", [2, 6])
+@pytest.mark.parametrize("n_states", [1, 3, 127])
+def test_purelns_state_cardinality(n_states, F):
+    w = W.lns8(seed=n_states, N=130, K=2048)
+    w["xa"] = W.lns8_activations_states(n_states, 2048, n_states)
+    check_pure(w, F)
+
+
+def test_purelns_zero_rows_and_without_S():
+    w = W.lns8(seed=6, N=70, K=512)
+    w["t"][::3] = 0
+    A, _ = check_pure(w, 3, with_S=False)
+    assert not A[::3].any()
+    w["xa"] = np.where(np.arange(512) % 2 == 0, 0x80, 0x00).astype(np.uint8)
+    A, S = check_pure(w, 5)
+    assert not A.any() and not S.any()
