@@ -54,6 +54,60 @@ __device__ __forceinline__ int warp_sum_i32(int v) { return __reduce_add_sync(0x
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// Warp-level MMAs (16x8x16, fp32 accumulate) used where a few tokens, or the
+// LNS8 class sums, make a contraction too small for the tensor-memory MMA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Exact fp32 integer of magnitude at most 2^22 -> int (through the 1.5 * 2^23
+// magic number, so no conversion instruction is needed).
+__device__ __forceinline__ int int_of_f32(float v) { return __float_as_int(v + 12582912.0f) - 0x4B400000; }
+
+// ---------------------------------------------------------------------------
+// LNS8 fragment layout -> compact mask words. Entry j (16 bytes) of a row pair
+// (q, q + 8) of a 16-row block holds, in words u = 0..3, the W_nonzero bits of
+// both rows in bytes 0 and 2 and the W_negative bits in bytes 1 and 3 (see
+// tg.h). Two byte permutes and two shift-and-merge steps give one 32-lane
+// W_nonzero and one W_negative word per row; lns8_lane_col names the group
+// lane of each bit, the same for both rows.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int lns8_lane_col(int j, int bit)
+{
+    const int x = 7 - (bit & 7);
+    const int c = (x >> 2) + 2 * ((bit >> 3) & 1) + 4 * (x & 1);
+    return 16 * c + 2 * j + 8 * ((x >> 1) & 1) + (bit >> 4);
+}
+
+__device__ __forceinline__ void lns8_compact_words(uint4 w, uint32_t &nz0, uint32_t &ng0, uint32_t &nz1,
+                                                   uint32_t &ng1)
+{
+    const uint32_t nza0 = __byte_perm(w.x, w.y, 0x6240), nga0 = __byte_perm(w.x, w.y, 0x7351);
+    const uint32_t nza1 = __byte_perm(w.z, w.w, 0x6240), nga1 = __byte_perm(w.z, w.w, 0x7351);
+    nz0 = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
+    nz1 = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
+    ng0 = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
+    ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
+}
+
 }  // namespace tgi
 
 // Each translation unit holds one device error word, set by a kernel that

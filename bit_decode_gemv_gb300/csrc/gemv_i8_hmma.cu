@@ -55,16 +55,6 @@ using tgi::kTileRows;
 constexpr int kWarps = 8;
 constexpr size_t kFragBudget = 200 * 1024;   // shared memory for the B fragments of one chunk
 
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // fp16 pair selected by the 2-bit codes in selector nibbles 1 and 3.
 __device__ __forceinline__ uint32_t tern_pair(uint32_t sel) { return __byte_perm(0xBC003C00u, 0u, sel); }
 __device__ __forceinline__ uint32_t q1_pair(uint32_t sel) { return __byte_perm(0x3C00BC00u, 0u, sel); }
@@ -88,9 +78,6 @@ __device__ __forceinline__ void fp16_of_s8x16(uint4 v, uint4 &lo, uint4 &hi)
     hi = make_uint4(fp16x2_of_s8(v.z, 0x5140u), fp16x2_of_s8(v.z, 0x7362u), fp16x2_of_s8(v.w, 0x5140u),
                     fp16x2_of_s8(v.w, 0x7362u));
 }
-
-// Exact fp32 integer of magnitude at most 2^22 -> int.
-__device__ __forceinline__ int int_of_f32(float v) { return __float_as_int(v + 12582912.0f) - 0x4B400000; }
 
 template <bool kQ1, int NT>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -194,7 +181,7 @@ gemv_i8_hmma_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__
 #pragma unroll
                 for (int nt = 0; nt < NT; nt++) {
                     const unsigned char *xr = xk + (size_t)8 * nt * stride;
-                    mma_f16_16816((s & 1) ? e[nt] : d[nt], a0, a1, a2, a3, *reinterpret_cast<const uint32_t *>(xr),
+                    tgi::mma_f16_16816((s & 1) ? e[nt] : d[nt], a0, a1, a2, a3, *reinterpret_cast<const uint32_t *>(xr),
                                   *reinterpret_cast<const uint32_t *>(xr + 16));
                 }
             }
@@ -206,10 +193,10 @@ gemv_i8_hmma_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__
             // d[nt] = P of (row r0: tokens 8 nt + 2t, + 1), (row r0 + 8: same)
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
-                acc[nt][0] += (da * int_of_f32(d[nt][0])) >> frac;
-                acc[nt][1] += (da * int_of_f32(d[nt][1])) >> frac;
-                acc[nt][2] += (db * int_of_f32(d[nt][2])) >> frac;
-                acc[nt][3] += (db * int_of_f32(d[nt][3])) >> frac;
+                acc[nt][0] += (da * tgi::int_of_f32(d[nt][0])) >> frac;
+                acc[nt][1] += (da * tgi::int_of_f32(d[nt][1])) >> frac;
+                acc[nt][2] += (db * tgi::int_of_f32(d[nt][2])) >> frac;
+                acc[nt][3] += (db * tgi::int_of_f32(d[nt][3])) >> frac;
             }
         }
 #pragma unroll

@@ -75,16 +75,6 @@ __device__ __forceinline__ uint32_t frag_pair(uint32_t w)
     return ((w & (0x00800080u >> RP)) * (0x7Fu << RP)) | ((w << RP) & 0x80008000u);
 }
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // One V value: (a != 0 and a & 7 == q) ? bf16(+-2^(a >> 3)) : 0.
 __device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
 {
@@ -224,8 +214,8 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 for (int kc = 0; kc < 8; kc += 2) {
                     const uint32_t w = w4[kc >> 1];
                     const uint2 b0 = vfrag[gl][kc][lane], b1 = vfrag[gl][kc + 1][lane];
-                    mma_bf16_16816(d, frag_pair<0>(w), frag_pair<1>(w), frag_pair<2>(w), frag_pair<3>(w), b0.x, b0.y);
-                    mma_bf16_16816(d1, frag_pair<4>(w), frag_pair<5>(w), frag_pair<6>(w), frag_pair<7>(w), b1.x, b1.y);
+                    tgi::mma_bf16_16816(d, frag_pair<0>(w), frag_pair<1>(w), frag_pair<2>(w), frag_pair<3>(w), b0.x, b0.y);
+                    tgi::mma_bf16_16816(d1, frag_pair<4>(w), frag_pair<5>(w), frag_pair<6>(w), frag_pair<7>(w), b1.x, b1.y);
                 }
 #pragma unroll
                 for (int i = 0; i < 4; i++)

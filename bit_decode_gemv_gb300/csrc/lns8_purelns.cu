@@ -85,26 +85,6 @@ __device__ __forceinline__ Lv shfl_down(Lv v, int d)
     return Lv{__shfl_down_sync(kFull, v.s, d), __shfl_down_sync(kFull, v.lam, d)};
 }
 
-// Group lane held at bit `bit` of compact word j (as in the state-set route).
-__device__ __forceinline__ int lane_col(int j, int bit)
-{
-    const int x = 7 - (bit & 7);
-    const int c = (x >> 2) + 2 * ((bit >> 3) & 1) + 4 * (x & 1);
-    return 16 * c + 2 * j + 8 * ((x >> 1) & 1) + (bit >> 4);
-}
-
-// One 16-byte LNS8 entry -> compact W_nonzero / W_negative words of its two
-// rows (q: *0, q + 8: *1).
-__device__ __forceinline__ void convert_word(uint4 w, uint32_t &nz0, uint32_t &ng0, uint32_t &nz1, uint32_t &ng1)
-{
-    const uint32_t nza0 = __byte_perm(w.x, w.y, 0x6240), nga0 = __byte_perm(w.x, w.y, 0x7351);
-    const uint32_t nza1 = __byte_perm(w.z, w.w, 0x6240), nga1 = __byte_perm(w.z, w.w, 0x7351);
-    nz0 = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
-    nz1 = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
-    ng0 = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
-    ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
-}
-
 // The eight phase aggregates of one (row, group): population histogram, count
 // fold, a balanced tree over the sixteen band slots of each phase.
 __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, short *bins,
@@ -116,13 +96,13 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         uint32_t nz0, ng0, nz1, ng1;
-        convert_word(tgi::ldg_stream(ent + j), nz0, ng0, nz1, ng1);
+        tgi::lns8_compact_words(tgi::ldg_stream(ent + j), nz0, ng0, nz1, ng1);
         uint32_t nz = half ? nz1 : nz0;
         const uint32_t ng = half ? ng1 : ng0;
         while (nz) {
             const int b = __ffs((int)nz) - 1;
             nz &= nz - 1u;
-            const unsigned a = xg[lane_col(j, b)];
+            const unsigned a = xg[tgi::lns8_lane_col(j, b)];
             const int code = (int)(a & 0x7fu);
             int k = code + e;
             if (code == 0 || k <= 0)

@@ -72,28 +72,6 @@ constexpr int kListStride = 36;     // entries per word list: 32 + 4, so the fou
 constexpr int kMaxCluster = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Group lane held at bit `bit` of compact word j (the order convert_word
-// produces for both rows of a lane).
-__device__ __forceinline__ int lane_col(int j, int bit)
-{
-    const int x = 7 - (bit & 7);
-    const int c = (x >> 2) + 2 * ((bit >> 3) & 1) + 4 * (x & 1);
-    return 16 * c + 2 * j + 8 * ((x >> 1) & 1) + (bit >> 4);
-}
-
-// One 16-byte LNS8 entry (words u = 0..3, both rows of a lane) -> the compact
-// W_nonzero and W_negative words of rows q and q + 8.
-__device__ __forceinline__ void convert_word(uint4 w, uint32_t &nz0, uint32_t &ng0, uint32_t &nz1,
-                                             uint32_t &ng1)
-{
-    const uint32_t nza0 = __byte_perm(w.x, w.y, 0x6240), nga0 = __byte_perm(w.x, w.y, 0x7351);
-    const uint32_t nza1 = __byte_perm(w.z, w.w, 0x6240), nga1 = __byte_perm(w.z, w.w, 0x7351);
-    nz0 = (nza0 & 0xAAAAAAAAu) | ((nza1 >> 1) & 0x55555555u);
-    nz1 = ((nza0 << 1) & 0xAAAAAAAAu) | (nza1 & 0x55555555u);
-    ng0 = (nga0 & 0xAAAAAAAAu) | ((nga1 >> 1) & 0x55555555u);
-    ng1 = ((nga0 << 1) & 0xAAAAAAAAu) | (nga1 & 0x55555555u);
-}
-
 struct WordMeta {
     int n, n_multi;    // entries, and of them those with several lanes
     int amin, amax;    // smallest and largest nonzero code of the word (amax = 0: none)
@@ -108,19 +86,6 @@ __device__ __forceinline__ uint32_t bf16x2_int(int lo, int hi)
     const float flo = __int_as_float(0x4B400000 + lo) - 12582912.0f;
     const float fhi = __int_as_float(0x4B400000 + hi) - 12582912.0f;
     return __byte_perm(__float_as_uint(flo), __float_as_uint(fhi), 0x7632);
-}
-
-// Exact fp32 integer of magnitude at most 2^22 -> int.
-__device__ __forceinline__ int int_of_f32(float v) { return __float_as_int(v + 12582912.0f) - 0x4B400000; }
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Signed population of an entry in one row. kSingle: the mask has one lane.
@@ -156,7 +121,7 @@ __device__ __forceinline__ void tile_step(const uint2 *L, int t, uint32_t nz0, u
     const uint32_t b0 = v_of(y[0], gq) | (v_of(y[1], gq) << 16);
     const uint32_t b1 = v_of(y[2], gq) | (v_of(y[3], gq) << 16);
     if constexpr (kSingle && !kChecked) {
-        mma_bf16_16816(d, single_bf16(nz0, ne0, m[0]) | (single_bf16(nz0, ne0, m[1]) << 16),
+        tgi::mma_bf16_16816(d, single_bf16(nz0, ne0, m[0]) | (single_bf16(nz0, ne0, m[1]) << 16),
                        single_bf16(nz1, ne1, m[0]) | (single_bf16(nz1, ne1, m[1]) << 16),
                        single_bf16(nz0, ne0, m[2]) | (single_bf16(nz0, ne0, m[3]) << 16),
                        single_bf16(nz1, ne1, m[2]) | (single_bf16(nz1, ne1, m[3]) << 16), b0, b1);
@@ -179,7 +144,7 @@ __device__ __forceinline__ void tile_step(const uint2 *L, int t, uint32_t nz0, u
                 }
             }
         }
-        mma_bf16_16816(d, bf16x2_int(c0[0], c0[1]), bf16x2_int(c1[0], c1[1]), bf16x2_int(c0[2], c0[3]),
+        tgi::mma_bf16_16816(d, bf16x2_int(c0[0], c0[1]), bf16x2_int(c1[0], c1[1]), bf16x2_int(c0[2], c0[3]),
                        bf16x2_int(c1[2], c1[3]), b0, b1);
     }
 }
@@ -281,7 +246,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
         // entry lists: one (group, word) item per warp at a time
         for (int item = warp; item < 4 * ng; item += kWarps) {
             const int gl = item >> 2, j = item & 3;
-            const unsigned a = xa[(size_t)(c0 + gl) * TG_GROUP + lane_col(j, lane)];
+            const unsigned a = xa[(size_t)(c0 + gl) * TG_GROUP + tgi::lns8_lane_col(j, lane)];
             build_word(a, lane, lists[gl][j], meta[gl][j]);
         }
         __syncthreads();
@@ -303,7 +268,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                 amax = max(amax, M[j].amax);
             }
             uint32_t nz0, ng0, nz1, ng1;
-            convert_word(w, nz0, ng0, nz1, ng1);
+            tgi::lns8_compact_words(w, nz0, ng0, nz1, ng1);
             const uint32_t sg = M[tq].sg;
             const uint32_t ne0 = nz0 & (ng0 ^ sg), ne1 = nz1 & (ng1 ^ sg);
             const int e0 = d0 - 74, e1 = d1 - 74;
@@ -332,7 +297,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                 const int delta = e & 7, beta = e >> 3;
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
-                    const int v = int_of_f32(d[2 * r + c]);
+                    const int v = tgi::int_of_f32(d[2 * r + c]);
                     if (v != 0) {
                         const int q = 2 * (int)tq + c;
                         const int sh = beta + ((q + delta) >> 3);
