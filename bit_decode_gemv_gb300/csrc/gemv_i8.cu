@@ -261,14 +261,14 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
     const int G = (int)L->G, N = (int)L->N;
     const int tiles = (int)L->tiles;
 
+    const bool pdl = (L->flags & TG_FLAG_CONST_WEIGHTS) != 0;
     if (x64)   // int64 activations: the digit-plane dp4a kernel for every M
         return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, true,
-                               (int)L->frac, s);
+                               (int)L->frac, pdl, s);
 
     if (M == 1) {
         if (m1_smem_bytes(G, 32) > 200 * 1024)
             return TG_ERR_SHAPE;
-        const bool pdl = (L->flags & TG_FLAG_CONST_WEIGHTS) != 0;
         // One group per warp up to K = 4096 (32 warps), then two per warp up to
         // K = 8192; beyond that 16 warps loop over batches of four groups each.
         const int frac = (int)L->frac;
@@ -292,10 +292,10 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
             return TG_ERR_CUDA;
     } else if (M <= kDp4aMaxTokens) {
         return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, false,
-                               (int)L->frac, s);
+                               (int)L->frac, pdl, s);
     } else if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G)) {
         return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1,
-                                 (int)L->frac, s);
+                                 (int)L->frac, pdl, s);
     } else {
         return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale,
                                 L->kind == TG_BINARY_Q1, (int)L->frac, s);

@@ -53,6 +53,7 @@ namespace {
 using tgi::kTileRows;
 
 constexpr int kWarps = 8;
+constexpr int kStageLoads = 8;               // activation loads per thread in flight while staging
 constexpr size_t kFragBudget = 200 * 1024;   // shared memory for the B fragments of one chunk
 
 // fp16 pair selected by the 2-bit codes in selector nibbles 1 and 3.
@@ -120,17 +121,38 @@ gemv_i8_hmma_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__
         ndb = __ldg(tscale + (size_t)(gg) * kTileRows + r0 + 8);                            \
     }
         TG_HMMA_LOAD_GROUP(warp >> 1)
-        // the chunk's activations as fp16 rows; rows past M are zero
+        if (m0 == 0) {
+            // launched as a programmatic dependent (constant weights): the next
+            // kernel may start now; x and y are touched only after the wait
+            tgi::pdl_launch_dependents();
+            tgi::pdl_wait();
+        }
+        // the chunk's activations as fp16 rows (rows past M are zero): eight
+        // 16-byte loads per thread in flight at a time, then their conversion
         const int per_row = K / 16;
-#pragma unroll 4
-        for (int i = threadIdx.x; i < 8 * NT * per_row; i += blockDim.x) {
-            const int tok = i / per_row, c = i - tok * per_row;
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (tok < mc)
-                fp16_of_s8x16(__ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + tok) * K) + c), lo, hi);
-            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)tok * stride + 32 * c);
-            dst[0] = lo;
-            dst[1] = hi;
+        const int items = 8 * NT * per_row;
+        for (int base = threadIdx.x; base < items; base += kStageLoads * blockDim.x) {
+            uint4 raw[kStageLoads];
+#pragma unroll
+            for (int u = 0; u < kStageLoads; u++) {
+                const int i = base + u * blockDim.x;
+                const int tok = i / per_row, c = i - tok * per_row;
+                raw[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < items && tok < mc)
+                    raw[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + tok) * K) + c);
+            }
+#pragma unroll
+            for (int u = 0; u < kStageLoads; u++) {
+                const int i = base + u * blockDim.x;
+                if (i < items) {
+                    const int tok = i / per_row, c = i - tok * per_row;
+                    uint4 lo, hi;
+                    fp16_of_s8x16(raw[u], lo, hi);
+                    uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)tok * stride + 32 * c);
+                    dst[0] = lo;
+                    dst[1] = hi;
+                }
+            }
         }
         for (int i = threadIdx.x; i < 32 * 8 * NT; i += blockDim.x)
             ysum[i] = 0ull;
@@ -223,28 +245,37 @@ size_t hmma_smem_bytes(int G, int NT) { return (size_t)8 * NT * (2 * 128 * (size
 
 template <bool kQ1, int NT>
 cudaError_t launch_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                        int tiles, int M, int frac, cudaStream_t s)
+                        int tiles, int M, int frac, bool pdl, cudaStream_t s)
 {
     auto kern = gemv_i8_hmma_kernel<kQ1, NT>;
     const size_t smem = hmma_smem_bytes(G, NT);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<tiles, kWarps * 32, smem, s>>>(masks, scales, x, y, N, G, M, frac);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, M, frac);
 }
 
 template <bool kQ1>
 cudaError_t dispatch_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                          int tiles, int M, int frac, cudaStream_t s)
+                          int tiles, int M, int frac, bool pdl, cudaStream_t s)
 {
     // token tiles per chunk: as many as M needs, as far as the fragments fit
     const int need = (M + 7) / 8;
     if (need >= 4 && hmma_smem_bytes(G, 4) <= kFragBudget)
-        return launch_hmma<kQ1, 4>(masks, scales, x, y, N, G, tiles, M, frac, s);
+        return launch_hmma<kQ1, 4>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
     if (need >= 2 && hmma_smem_bytes(G, 2) <= kFragBudget)
-        return launch_hmma<kQ1, 2>(masks, scales, x, y, N, G, tiles, M, frac, s);
-    return launch_hmma<kQ1, 1>(masks, scales, x, y, N, G, tiles, M, frac, s);
+        return launch_hmma<kQ1, 2>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
+    return launch_hmma<kQ1, 1>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
 }
 
 }  // namespace
@@ -254,12 +285,12 @@ namespace tgi {
 bool gemv_i8_hmma_fits(int G) { return hmma_smem_bytes(G, 1) <= kFragBudget; }
 
 int gemv_i8_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
-                 int M, bool q1, int frac, cudaStream_t s)
+                 int M, bool q1, int frac, bool pdl, cudaStream_t s)
 {
     if (!gemv_i8_hmma_fits(G))
         return TG_ERR_SHAPE;
-    const cudaError_t e = q1 ? dispatch_hmma<true>(masks, scales, x, y, N, G, tiles, M, frac, s)
-                             : dispatch_hmma<false>(masks, scales, x, y, N, G, tiles, M, frac, s);
+    const cudaError_t e = q1 ? dispatch_hmma<true>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s)
+                             : dispatch_hmma<false>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

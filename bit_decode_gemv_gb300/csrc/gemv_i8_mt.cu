@@ -166,6 +166,12 @@ gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
             }
         };
         load_batch(warp);
+        if (m0 == 0) {
+            // launched as a programmatic dependent (constant weights): the next
+            // kernel may start now; x and y are touched only after the wait
+            tgi::pdl_launch_dependents();
+            tgi::pdl_wait();
+        }
 
         // stage the chunk's activations (row t * planes + l holds digit plane l
         // of token t), their group totals, zero the row sums
@@ -270,7 +276,7 @@ size_t mt_smem_bytes(int G, int chunk, int planes)
 
 template <int GPW, bool kQ1, bool kX64>
 cudaError_t launch_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G,
-                      int tiles, int M, int frac, cudaStream_t s)
+                      int tiles, int M, int frac, bool pdl, cudaStream_t s)
 {
     auto kern = gemv_i8_mt_kernel<GPW, kQ1, kX64>;
     constexpr int kPlanes = planes_max<kX64>();
@@ -286,19 +292,28 @@ cudaError_t launch_mt(const uint4 *masks, const int32_t *scales, const void *x, 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    kern<<<tiles, warps * 32, smem, s>>>(masks, scales, x, y, N, G, M, chunk, frac);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, M, chunk, frac);
 }
 
 template <bool kX64>
 cudaError_t dispatch_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G,
-                        int tiles, int M, bool q1, int frac, cudaStream_t s)
+                        int tiles, int M, bool q1, int frac, bool pdl, cudaStream_t s)
 {
     if (q1)
-        return G <= 32 ? launch_mt<2, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s)
-                       : launch_mt<4, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s);
-    return G <= 32 ? launch_mt<2, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s)
-                   : launch_mt<4, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, s);
+        return G <= 32 ? launch_mt<2, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s)
+                       : launch_mt<4, true, kX64>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
+    return G <= 32 ? launch_mt<2, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s)
+                   : launch_mt<4, false, kX64>(masks, scales, x, y, N, G, tiles, M, frac, pdl, s);
 }
 
 }  // namespace
@@ -306,13 +321,13 @@ cudaError_t dispatch_mt(const uint4 *masks, const int32_t *scales, const void *x
 namespace tgi {
 
 int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G, int tiles,
-               int M, bool q1, bool x64, int frac, cudaStream_t s)
+               int M, bool q1, bool x64, int frac, bool pdl, cudaStream_t s)
 {
     const size_t planes = x64 ? 8 : 1;
     if (planes * ((size_t)G * 128 + 4 * (size_t)G) + 256 > kStageBytes)
         return TG_ERR_SHAPE;   // one token's activation planes must fit
-    const cudaError_t e = x64 ? dispatch_mt<true>(masks, scales, x, y, N, G, tiles, M, q1, frac, s)
-                              : dispatch_mt<false>(masks, scales, x, y, N, G, tiles, M, q1, frac, s);
+    const cudaError_t e = x64 ? dispatch_mt<true>(masks, scales, x, y, N, G, tiles, M, q1, frac, pdl, s)
+                              : dispatch_mt<false>(masks, scales, x, y, N, G, tiles, M, q1, frac, pdl, s);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 

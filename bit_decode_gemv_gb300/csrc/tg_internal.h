@@ -28,16 +28,17 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
                 int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s);
 
 // Ternary / Q1_0 GEMV for a few tokens on the CUDA cores; x is int8 [M][K], or
-// int64 [M][K] when x64 (sums modulo 2^64). Arguments as checked by
-// tg_gemv_i8. Returns a tg_status.
+// int64 [M][K] when x64 (sums modulo 2^64); pdl: launch as a programmatic
+// dependent (constant weights). Arguments as checked by tg_gemv_i8. Returns a
+// tg_status.
 int gemv_i8_mt(const uint4 *masks, const int32_t *scales, const void *x, int64_t *y, int N, int G, int tiles,
-               int M, bool q1, bool x64, int frac, cudaStream_t s);
+               int M, bool q1, bool x64, int frac, bool pdl, cudaStream_t s);
 
 // Ternary / Q1_0 GEMV for a few tokens through warp-level fp16 MMAs; the token
 // activations' fragments must fit in shared memory (gemv_i8_hmma_fits(G)).
 bool gemv_i8_hmma_fits(int G);
 int gemv_i8_hmma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G, int tiles,
-                 int M, bool q1, int frac, cudaStream_t s);
+                 int M, bool q1, int frac, bool pdl, cudaStream_t s);
 
 // LNS8 eight-phase GEMV by the state-population route (TG_FLAG_LNS8_STATE_SET);
 // arguments as checked by tg_gemv_lns8_phase. Returns a tg_status.

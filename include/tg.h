@@ -139,12 +139,12 @@ typedef struct tg_layout {
 
 /*
  * Layout flag: the packed weights are constant -- no device work on the stream
- * of an apply call writes them. A batch-1 tg_gemv_i8 call on such weights is
- * launched as a programmatic dependent of the previous kernel on the stream: it
- * may start streaming its weights while that kernel is still running, and it
- * waits for that kernel to finish (and its writes to be visible) before it
- * reads x or writes y. Without the flag every call starts after the previous
- * work on the stream has finished.
+ * of an apply call writes them. A tg_gemv_i8 call on such weights with up to 16
+ * tokens (or int64 activations) is launched as a programmatic dependent of the
+ * previous kernel on the stream: it may start streaming its weights while that
+ * kernel is still running, and it waits for that kernel to finish (and its
+ * writes to be visible) before it reads x or writes y. Without the flag every
+ * call starts after the previous work on the stream has finished.
  */
 #define TG_FLAG_CONST_WEIGHTS 1
 

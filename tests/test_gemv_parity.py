@@ -108,11 +108,12 @@ def test_output_untouched_on_argument_error():
 
 
 @pytest.mark.parametrize("N,K", [(6912, 2560), (1000, 6912)])
-def test_const_weights_back_to_back(N, K):
-    # With TG_FLAG_CONST_WEIGHTS a batch-1 call may start streaming its weights
-    # while the previous kernel runs; x and y must still be ordered after it.
-    # Several calls in a row on one stream: each on other weights, all writing
-    # the same y, with x rewritten by a torch kernel between some of them.
+@pytest.mark.parametrize("M", [1, 3, 8, 12])
+def test_const_weights_back_to_back(N, K, M):
+    # With TG_FLAG_CONST_WEIGHTS a call with up to 16 tokens may start streaming
+    # its weights while the previous kernel runs; x and y must still be ordered
+    # after it. Several calls in a row on one stream: each on other weights, all
+    # writing the same y, with x rewritten by a torch kernel between some of them.
     import torch
     import bit_decode_gemv_gb300 as tg
     from gpu_helpers import dev, pack_to_device
@@ -122,15 +123,15 @@ def test_const_weights_back_to_back(N, K):
         wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
         L.flags |= tg.TG_FLAG_CONST_WEIGHTS
         packed.append((wd, L))
-    xs = [dev(W.x_normal40(200 + i, (1, K))) for i in range(4)]
-    x = torch.empty((1, K), dtype=torch.int8, device="cuda")
-    y = torch.empty((1, N), dtype=torch.int64, device="cuda")
-    outs = [torch.empty((1, N), dtype=torch.int64, device="cuda") for _ in range(8)]
+    xs = [dev(W.x_normal40(200 + i, (M, K))) for i in range(4)]
+    x = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.int64, device="cuda")
+    outs = [torch.empty((M, N), dtype=torch.int64, device="cuda") for _ in range(8)]
     for rep in range(2):
         for i, (wd, L) in enumerate(packed):
             torch.add(xs[(i + rep) % 4], 0, out=x)          # a kernel writes x
-            tg.tg_gemv_i8(L, wd, x, 1, y)
-            tg.tg_gemv_i8(L, wd, x, 1, y)                    # same y again, back to back
+            tg.tg_gemv_i8(L, wd, x, M, y)
+            tg.tg_gemv_i8(L, wd, x, M, y)                    # same y again, back to back
             outs[rep * 4 + i].copy_(y)
     torch.cuda.synchronize()
     for rep in range(2):

@@ -109,3 +109,29 @@ def test_int8_range_values_equal_the_int8_call():
     y64 = run_x64(tg.TG_TERNARY_I8, w["t"], w["d"], w["x"].astype(np.int64))
     wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
     np.testing.assert_array_equal(y64, gemv(wd, L, w["x"]))
+
+
+def test_const_weights_back_to_back_int64():
+    """Programmatic dependent launch on the int64 path: a torch kernel rewrites
+    x between calls that all write the same y."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import dev, pack_to_device
+    N, K, M = 300, 1024, 2
+    cases = [W.batched(seed=300 + i, M=M, N=N, K=K) for i in range(3)]
+    packed = []
+    for w in cases:
+        wd, L = pack_to_device(tg.TG_TERNARY_I8, w["t"], w["d"])
+        L.flags |= tg.TG_FLAG_CONST_WEIGHTS | tg.TG_FLAG_X_INT64
+        packed.append((wd, L))
+    xs = [dev(W.x_fixed64(400 + i, (M, K), frac_bits=12)) for i in range(3)]
+    x = torch.empty((M, K), dtype=torch.int64, device="cuda")
+    y = torch.empty((M, N), dtype=torch.int64, device="cuda")
+    outs = [torch.empty((M, N), dtype=torch.int64, device="cuda") for _ in range(3)]
+    for i, (wd, L) in enumerate(packed):
+        torch.add(xs[i], 0, out=x)
+        tg.tg_gemv_i8(L, wd, x, M, y)
+        outs[i].copy_(y)
+    torch.cuda.synchronize()
+    for i, w in enumerate(cases):
+        np.testing.assert_array_equal(outs[i].cpu().numpy(), oracle.gemv_x64(w["t"], w["d"], xs[i].cpu().numpy()))
