@@ -10,14 +10,18 @@
  *          y[m][r] = sum_g d[r][g] * ( sum_{i in group g} t[r][i] * x[m][i] ).
  *      Groups are 128 weights; the per-group partial is an int32, the sum over
  *      groups an int64. The same call takes binary Q1_0 weights {-1, +1}
- *      (§4.1, one sign bit per weight) and the per-group floor arshift(., frac)
- *      of §4.1/§4.2 (layout field frac, 0 by default).
+ *      (§4.1, one sign bit per weight), the per-group floor arshift(., frac)
+ *      of §4.1/§4.2 (layout field frac, 0 by default), 1 to 64 tokens, and
+ *      int64 fixed-point activations (§4.4, sums modulo 2^64; TG_FLAG_X_INT64).
  *
  *   2. LNS8 S1|E4|L3 eight-phase accumulation (BitState brief §3, §3.1 and the
  *      generic variant of §4): every nonzero product state
  *          k = a + d - 74   (k <= 0 -> exact zero, k > 127 -> 127)
  *      adds sign * (1 << (k >> 3)) into A[k & 7], and
  *          S = 2^-9 * sum_p A[p] * 2^((p - 2) / 8)        (fp64).
+ *      Besides the direct per-lane route, the same result by signed state
+ *      populations (§4 with §6; TG_FLAG_LNS8_STATE_SET), and an approximate
+ *      pure fractional-LNS reduction (§5.2; TG_FLAG_LNS8_PURE_LNS).
  *
  *   3. Vocab-scale lm_head over 8 base-3 planes (SKaiNET-transformers issue
  *      #337, BITNET_PLANES and BitNetTwoStageDecode): the integer weight is
@@ -37,7 +41,9 @@
  *     argument error no output buffer is touched.
  *   - The library keeps no state between calls, apart from one device error
  *     word that a kernel sets if a bounded wait of its own runs out
- *     (tg_device_error()).
+ *     (tg_device_error()), the fixed device scratch of
+ *     tg_lmhead_argmax_topk_noalloc, and the constant host tables of the
+ *     pure-LNS route (computed on first use for each precision).
  *   - Packing (tg_pack_weights) runs synchronously on the host, from host
  *     arrays into a host buffer; the caller copies that buffer to the device.
  */
