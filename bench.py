@@ -744,7 +744,10 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "gemvs_per_step": GEMVS_PER_STEP, "weight_copies": R,
+        "config": {"workload": WORKLOAD, "seed": rank,
+                   "inputs_sha256_16": hashlib.sha256(blob.tobytes() + np.ascontiguousarray(w["x"]).tobytes())
+                   .hexdigest()[:16],
+                   "gemvs_per_step": GEMVS_PER_STEP, "weight_copies": R,
                    "weight_copy_bytes": int(blob.size),
                    "l2": f"weights rotated over {R} copies ({R * blob.size / 2**20:.0f} MiB > 4x L2)",
                    "launch": "each step's calls replayed from one CUDA graph; weights flagged "
