@@ -226,6 +226,9 @@ lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
+    // the rescoring kernel may launch now; it waits for this grid before it
+    // reads anything this grid writes
+    tgi::pdl_launch_dependents();
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
     const int64_t sum_abs = warp_sum_abs_regs<CPL>(xr);
@@ -316,9 +319,14 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
     const int C16 = K / 16;
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
-    // every warp derives the bound's sum |x| and the threshold itself: no block barrier
-    const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
     const int64_t sum_abs = warp_sum_abs_regs<CPL>(xr);
+    // launched as a programmatic dependent of stage 1: x (complete before stage
+    // 1 started) is read above; the histogram and the stage-1 sums only after
+    // stage 1 has finished. The final selection may launch now.
+    tgi::pdl_launch_dependents();
+    tgi::pdl_wait();
+    // every warp derives the threshold itself: no block barrier
+    const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
 
     for (int base = wg * 32; base < N; base += NW * 32) {
@@ -524,6 +532,7 @@ __global__ void __launch_bounds__(kSelThreads)
 lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32_t *__restrict__ ids,
                  int64_t *__restrict__ scores, int32_t *__restrict__ ncand)
 {
+    tgi::pdl_wait();   // launched as a programmatic dependent of the rescoring / collecting kernel
     extern __shared__ __align__(16) unsigned char dyn[];
     uint64_t *sel = reinterpret_cast<uint64_t *>(dyn);                                 // [kFilterMax]
     RadixSmem &rs = *reinterpret_cast<RadixSmem *>(dyn + kFilterMax * sizeof(uint64_t));
@@ -629,10 +638,19 @@ void launch_scan(bool full, int grid, cudaStream_t st, const int8_t *hi, const i
 }
 
 template <int CPL>
-void launch_rescore(int grid, cudaStream_t st, const int8_t *lo, const int32_t *s, const uint8_t *m,
+cudaError_t launch_rescore(int grid, cudaStream_t st, const int8_t *lo, const int32_t *s, const uint8_t *m,
                     const int8_t *x, Ws ws, int N, int K, int k, int idx_bits)
 {
-    lmh_rescore_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(lo, s, m, x, ws, N, K, k, idx_bits);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kScanWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lmh_rescore_kernel<CPL>, lo, s, m, x, ws, N, K, k, idx_bits);
 }
 
 }  // namespace
@@ -709,28 +727,42 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
     }
 #undef TGI_CPL_CASE
 
+    cudaError_t re = cudaSuccess;
     if (full) {
         const int cgrid = (int)((N + 255) / 256 < nsm * 4 ? (N + 255) / 256 : nsm * 4);
         lmh_collect_kernel<<<cgrid, 256, 0, st>>>(logits, wsp, n, k, idx_bits);
     } else {
 #define TGI_CPL_CASE(C)                                                                            \
     case C:                                                                                        \
-        launch_rescore<C>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);                         \
+        re = launch_rescore<C>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);                    \
         break;
         switch (cpl) {
             TGI_CPL_CASE(1) TGI_CPL_CASE(2) TGI_CPL_CASE(3) TGI_CPL_CASE(4) TGI_CPL_CASE(5)
             TGI_CPL_CASE(6) TGI_CPL_CASE(7) TGI_CPL_CASE(8)
         default:
-            launch_rescore<16>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);
+            re = launch_rescore<16>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);
             break;
         }
 #undef TGI_CPL_CASE
     }
+    if (re != cudaSuccess)
+        return TG_ERR_CUDA;
     const size_t final_smem = kFilterMax * sizeof(uint64_t) + sizeof(RadixSmem);
     if (cudaFuncSetAttribute(lmh_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)final_smem) != cudaSuccess)
         return TG_ERR_CUDA;
-    lmh_final_kernel<<<1, kSelThreads, final_smem, st>>>(wsp, k, idx_bits, argmax, ids, scores, ncand);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = final_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, lmh_final_kernel, wsp, k, idx_bits, argmax, ids, scores, ncand) != cudaSuccess)
+        return TG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
