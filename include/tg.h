@@ -171,7 +171,8 @@ typedef struct tg_layout {
  * §5: the base-256 limb decomposition is exact modulo 2^64): the result is
  * exact whenever no step leaves the int64 range, and there is no TG_ERR_BOUND
  * check. Computed by signed base-256 digit planes of x, as many as the largest
- * activation needs.
+ * activation needs; eight planes of one token must fit the kernel's staging
+ * area, so K is at most 17,792 (TG_ERR_SHAPE beyond).
  */
 #define TG_FLAG_X_INT64 4
 

@@ -135,3 +135,9 @@ def test_const_weights_back_to_back_int64():
     torch.cuda.synchronize()
     for i, w in enumerate(cases):
         np.testing.assert_array_equal(outs[i].cpu().numpy(), oracle.gemv_x64(w["t"], w["d"], xs[i].cpu().numpy()))
+
+
+def test_largest_k():
+    """K = 17792, the largest K whose eight digit planes fit the staging area."""
+    w = W.batched(seed=17, M=2, N=40, K=17792)
+    check(w["t"], w["d"], W.x_int64_full(17, (2, 17792)))
