@@ -14,11 +14,14 @@
 // the result is exact modulo 2^64 and therefore exact, since y fits in int64
 // (checked on the host).
 //
-// Mapping. A CTA owns 128 rows (four 32-row mask tiles) for all groups and all
-// tokens. 16 compute warps, two MMA warps and a copy warp hand work to each other through
-// mbarrier rings, with no CTA-wide barrier inside the group loop.
+// Mapping. A CTA owns one to four 32-row mask tiles (the MMA's M stays 128;
+// the host picks the fewest tiles per CTA that still fill one wave) for all
+// groups and all tokens. 16 compute warps, two MMA warps and a copy warp hand
+// work to each other through mbarrier rings, with no CTA-wide barrier inside
+// the group loop.
 //   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
-//     rows of mask tile w%4) and handles part p = w/4. In its iteration for
+//     rows of mask tile w%4; a warp whose tile the CTA does not own only
+//     converts activations) and handles part p = w/4. In its iteration for
 //     group g it first reads back group g-2's D buffer for tokens
 //     16p..16p+15, accumulates it, and refills that buffer with the offset for
 //     group g+2; then expands its 32 weights of group g (group lanes
@@ -166,7 +169,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Wait for this thread's tensor-memory loads, with the loaded registers passed
+// through the wait so that the compiler places no use of them before it (other
+// work may sit between the load and the wait).
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15])
+                 :
+                 : "memory");
+}
 
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -309,7 +323,7 @@ template <bool kQ1, int kFold>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char *__restrict__ scales,
                    const __grid_constant__ CUtensorMap xmap, int64_t *__restrict__ y, int N, int G, int tiles,
-                   int M, int frac)
+                   int M, int frac, int ctiles)
 {
     constexpr bool kNarrow = kFold == kFoldNarrow;
     constexpr uint32_t kMaskBytes = kQ1 ? 512u : 1024u;   // mask bytes of one (tile, group)
@@ -319,7 +333,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t nmma = (uint32_t)((M + 15) & ~15);
-    const int tiles_here = min(4, tiles - (int)blockIdx.x * 4);
+    const int tiles_here = min(ctiles, tiles - (int)blockIdx.x * ctiles);
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bars = sbase + kOffBar;
@@ -377,7 +391,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 mbar_expect_tx(b, tx);
             __syncwarp();
             if (lane < tiles_here) {
-                const size_t unit = (size_t)(blockIdx.x * 4 + lane) * G + g;
+                const size_t unit = (size_t)(blockIdx.x * ctiles + lane) * G + g;
                 bulk_copy(sdst + kStageMask + lane * 1024, masks + unit * kMaskBytes, kMaskBytes, b);
                 bulk_copy(sdst + kStageScale + lane * 128, scales + unit * 128, 128, b);
             } else if (lane == 31) {
@@ -422,11 +436,14 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
     } else {
         // ---------------- compute warps ----------------
         const int q = warp & 3, p = warp >> 2;
-        const int tile = blockIdx.x * 4 + q;
-        const bool tile_ok = tile < tiles;
+        // a warp whose quarter q >= ctiles has no rows: it converts activations and keeps
+        // the barrier protocol, and its tensor-memory lanes hold nothing that is read
+        const bool rows_q = q < ctiles;
+        const int tile = blockIdx.x * ctiles + q;
+        const bool tile_ok = rows_q && tile < tiles;
         const int row = tile * tgi::kTileRows + lane;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const bool epi = 16 * p < M;   // warp-uniform: this warp's tokens exist
+        const bool epi = rows_q && 16 * p < M;   // warp-uniform: this warp's rows and tokens exist
         // int64 accumulators of tokens 16p + j (j = 0..15) for this row: [token][row] layout, + 128 j
         int64_t *accs = reinterpret_cast<int64_t *>(smem + kOffAcc) + 16 * p * kRowsPerCta + 32 * q + lane;
 
@@ -486,15 +503,19 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         // B position of chunks 2 j16 and 2 j16 + 1 of token xn: K-step j16, core matrices 0 and 1
         unsigned char *bdst = smem + kOffB + j16 * kKStepBytes + (xn >> 3) * 256 + (xn & 7) * 16;
 
-        // read back group gp's D buffer (db_e), accumulate, and refill it with the offset
-        auto epilogue = [&](int dgp, bool refill) {
+        // read back group gp's D buffer (db_e) -- issued by epi_load, consumed by
+        // epi_fold once the group's other work has been issued -- accumulate it,
+        // and refill the buffer with the offset
+        auto epi_load = [&](uint32_t (&v)[16]) {
             wait(kBarDFull + db_e, db_par);
             fence_after_sync();
+            if (epi)
+                tmem_ld16(dbase + (uint32_t)(kMaxN * db_e), v);
+        };
+        auto epi_fold = [&](uint32_t (&v)[16], int dgp, bool refill) {
             const uint32_t dcol = dbase + (uint32_t)(kMaxN * db_e);
             if (epi) {
-                uint32_t v[16];
-                tmem_ld16(dcol, v);
-                tmem_wait_ld();
+                tmem_wait_ld(v);
                 if (refill)
                     tmem_st16_same(dcol, kOffsetBits);
                 if (kNarrow) {
@@ -535,31 +556,38 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 if (g >= G)
                     break;
                 const bool refill = g >= kLag && g - kLag + kDBufs < G;
-                if (g >= kLag)
-                    epilogue(d_lag[bb], refill);   // group g - 2 has the same parity as g
                 if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
                     wait(kBarABEmpty + sl, sl_par ^ 1u);
                 wait(kBarMFull + st, st_par);
-                {
+                // this group's inputs from the stage, then group g - 2's D buffer (same
+                // parity as g), both in flight while the weights are expanded
+                uint2 mw = make_uint2(0, 0);
+                if (tile_ok)
+                    mw = kQ1 ? make_uint2(*reinterpret_cast<const uint32_t *>(mrow + st * kStageBytes), 0u)
+                             : *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes);
+                const uint4 xv = x_ok ? *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes)
+                                      : make_uint4(0, 0, 0, 0);
+                const int dg = tile_ok ? *reinterpret_cast<const int *>(srow + st * kStageBytes) : 0;
+                uint32_t v[16];
+                if (g >= kLag)
+                    epi_load(v);
+                if (rows_q) {
                     uint32_t a[16];
                     if (kQ1) {
-                        const uint32_t mw = tile_ok ? *reinterpret_cast<const uint32_t *>(mrow + st * kStageBytes) : 0u;
-                        expand_word_q1(mw, a);
+                        expand_word_q1(mw.x, a);
                     } else {
-                        const uint2 mw = tile_ok ? *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes)
-                                                 : make_uint2(0, 0);
                         expand_word(mw.x, a);
                         expand_word(mw.y, a + 8);
                     }
                     tmem_st16(abase + 64u * (uint32_t)sl, a);
                 }
                 if (x_ok) {
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes);
                     unsigned char *B = bdst + sl * kBBytes;
                     *reinterpret_cast<uint4 *>(B) = fp16_of_int8x8(make_uint2(xv.x, xv.y));
                     *reinterpret_cast<uint4 *>(B + 128) = fp16_of_int8x8(make_uint2(xv.z, xv.w));
                 }
-                const int dg = tile_ok ? *reinterpret_cast<const int *>(srow + st * kStageBytes) : 0;
+                if (g >= kLag)
+                    epi_fold(v, d_lag[bb], refill);
                 dsum += (uint64_t)(int64_t)dg;
                 tmem_wait_st();   // A of group g and the refilled D buffer
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -585,7 +613,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             }
         }
         for (int gp = max(0, G - kLag); gp < G; gp++) {
-            epilogue((gp & 1) ? d_lag[1] : d_lag[0], false);
+            uint32_t v[16];
+            epi_load(v);
+            epi_fold(v, (gp & 1) ? d_lag[1] : d_lag[0], false);
             next_db();
         }
         if (kNarrow && epi)
@@ -637,7 +667,7 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
         }
         if (!attr_set) {
             void (*kernels[6])(const unsigned char *, const unsigned char *, const CUtensorMap, int64_t *, int, int,
-                               int, int, int) = {
+                               int, int, int, int) = {
                 gemv_i8_mma_kernel<false, kFoldNarrow>, gemv_i8_mma_kernel<false, kFoldWide>,
                 gemv_i8_mma_kernel<false, kFoldFloor>,  gemv_i8_mma_kernel<true, kFoldNarrow>,
                 gemv_i8_mma_kernel<true, kFoldWide>,    gemv_i8_mma_kernel<true, kFoldFloor>};
@@ -657,10 +687,24 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return TG_ERR_CUDA;
-    const int grid = (tiles + 3) / 4;
+    // Tiles per CTA: the fewest that still fit every CTA in one wave (one CTA per SM),
+    // so that a shape with fewer than 4 x #SMs tiles spreads over more SMs; a CTA's
+    // per-group work shrinks with its tiles, the activation conversion does not.
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TG_ERR_CUDA;
+    int ctiles = 4;
+    for (int c = 1; c < 4; c++)
+        if ((tiles + c - 1) / c <= nsm) {
+            ctiles = c;
+            break;
+        }
+    const int grid = (tiles + ctiles - 1) / ctiles;
     const auto *mk = reinterpret_cast<const unsigned char *>(masks);
     const auto *sc = reinterpret_cast<const unsigned char *>(scales);
-#define TGI_MMA_LAUNCH(Q, F) gemv_i8_mma_kernel<Q, F><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M, frac)
+#define TGI_MMA_LAUNCH(Q, F) \
+    gemv_i8_mma_kernel<Q, F><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M, frac, ctiles)
     if (q1) {
         if (fold == kFoldNarrow)
             TGI_MMA_LAUNCH(true, kFoldNarrow);

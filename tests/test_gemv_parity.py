@@ -260,3 +260,16 @@ def test_every_token_count_path(M, K):
     check_frac(W.batched(seed=M * K + 1, M=M, N=N, K=K), 5)
     check_q1(W.ffn_up_q1(seed=M * K + 2, N=N, K=K, M=M))
     check_q1(W.ffn_up_q1(seed=M * K + 3, N=N, K=K, M=M), 11)
+
+
+# The tensor-memory kernel gives a CTA one to four 32-row tiles, the fewest that
+# still fit one wave on the device's SMs. On a 152-SM part these row counts take
+# two, three and four tiles per CTA, each with a last CTA that owns fewer tiles;
+# K = 1024 cycles the input ring (eight groups, six stages).
+@pytest.mark.parametrize("N", [6939, 12807, 15043])
+@pytest.mark.parametrize("M", [17, 64])
+def test_tiles_per_cta(N, M):
+    check(W.batched(seed=N + M, M=M, N=N, K=1024))
+    if M == 64:
+        check_frac(W.batched(seed=N + 1, M=M, N=N, K=1024), 6)
+        check_q1(W.ffn_up_q1(seed=N + 2, N=N, K=1024, M=M))
