@@ -215,6 +215,18 @@ __device__ __forceinline__ int row_dot(const int8_t *row, int C16, int lane, con
     return acc;
 }
 
+// 0. Zero the candidate count and both histograms. Launched as a programmatic
+// dependent of whatever precedes the call on the stream, it waits for that
+// work to finish (x may be its output), then lets the scan launch; the scan
+// waits for the clearing before it touches the workspace.
+__global__ void __launch_bounds__(256) lmh_clear_kernel(uint4 *__restrict__ p, int n16)
+{
+    tgi::pdl_wait();
+    tgi::pdl_launch_dependents();
+    for (int i = threadIdx.x; i < n16; i += blockDim.x)
+        p[i] = make_uint4(0, 0, 0, 0);
+}
+
 // 1. Stage-1 scan over planes 0-3; two rows per warp iteration keep 2 * CPL
 // 16-byte loads per lane in flight. Each warp counts its largest lower bound.
 template <int CPL>
@@ -232,6 +244,11 @@ lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
     const int64_t sum_abs = warp_sum_abs_regs<CPL>(xr);
+    // the clearing kernel (tiny) has long finished. Waiting for it here rather
+    // than before the first count lets the rescoring CTAs launch while the scan
+    // runs (measured: with the wait at the end they launched only as the scan's
+    // CTAs exited).
+    tgi::pdl_wait();
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += 2 * NW) {
@@ -268,8 +285,10 @@ lmh_full_kernel(const int8_t *__restrict__ hi, const int8_t *__restrict__ lo,
     const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     const int NW = gridDim.x * kScanWarps;
     const int C16 = K / 16;
+    tgi::pdl_launch_dependents();   // the collecting kernel waits for this grid before it reads anything
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
+    tgi::pdl_wait();   // the clearing kernel (as in stage 1)
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += NW) {
@@ -307,15 +326,28 @@ __device__ __forceinline__ void append_key(Ws ws, bool take, uint64_t key, int64
 }
 
 // 2. Rescore every row whose upper bound reaches tau, exactly, with planes 4-7.
+// One CTA per SM: at 64 registers it fits beside the scan's CTAs, so every
+// rescoring CTA is resident (and has read x) before the scan ends. A CTA owns a
+// contiguous range of rows and filters it in passes of kRescorePass rows (four
+// per thread; the first pass's bounds load while one warp finds tau); the
+// candidates of a pass are gathered in shared memory and shared out over the
+// CTA's warps, two rows per warp at a time so that both rows' loads are in
+// flight together.
+constexpr int kRescorePass = kScanWarps * 32 * 4;
+
 template <int CPL>
-__global__ void __launch_bounds__(kScanWarps * 32)
+__global__ void __launch_bounds__(kScanWarps * 32, CPL <= 5 ? 4 : 1)
 lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
                    const uint8_t *__restrict__ m, const int8_t *__restrict__ x, Ws ws, int N, int K,
                    int k, int idx_bits)
 {
-    const int lane = threadIdx.x & 31;
-    const int wg = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
-    const int NW = gridDim.x * kScanWarps;
+    __shared__ int64_t sh_tau;
+    __shared__ int sh_n;
+    __shared__ unsigned long long sh_base;
+    __shared__ int c_row[kRescorePass];
+    __shared__ int c_sc[kRescorePass];
+    __shared__ int64_t c_s1[kRescorePass];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int C16 = K / 16;
     uint4 xr[CPL];
     load_x<CPL>(x, C16, lane, xr);
@@ -325,30 +357,47 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
     // stage 1 has finished. The final selection may launch now.
     tgi::pdl_launch_dependents();
     tgi::pdl_wait();
-    // every warp derives the threshold itself: no block barrier
-    const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
+    const int per = (N + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int r_begin = (int)blockIdx.x * per;
+    const int r_end = min(N, r_begin + per);
 
-    for (int base = wg * 32; base < N; base += NW * 32) {
-        const int r = base + lane;
-        bool cand = false;
-        int64_t sc = 0, s1 = 0;
-        if (r < N) {
-            sc = __ldg(s + r);
-            s1 = ws.s1[r];
-            cand = sc * s1 + sc * (int64_t)__ldg(m + r) * sum_abs >= tau;
+    for (int c0 = r_begin; c0 < r_end; c0 += kRescorePass) {
+        int scv[4];
+        int64_t s1v[4], mv[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int r = c0 + (int)threadIdx.x + kScanWarps * 32 * i;
+            const bool ok = r < r_end;
+            scv[i] = ok ? __ldg(s + r) : 0;
+            s1v[i] = ok ? __ldcg(ws.s1 + r) : 0;
+            mv[i] = ok ? (int64_t)__ldg(m + r) : 0;
         }
-        // candidates of this block of 32 rows, two at a time so that both rows'
-        // loads are in flight together
-        unsigned todo = __ballot_sync(0xffffffffu, cand);
-        while (todo) {
-            const int src0 = __ffs(todo) - 1;
-            todo &= todo - 1;
-            const int src1 = todo ? __ffs(todo) - 1 : src0;
-            const bool two = todo != 0;
-            if (two)
-                todo &= todo - 1;
-            const int r0 = base + src0, r1 = base + src1;
+        if (c0 == r_begin && warp == 0) {
+            const int64_t t = warp_kth_bin_edge(ws.hist_row, k);
+            if (lane == 0)
+                sh_tau = t;
+        }
+        if (threadIdx.x == 0)
+            sh_n = 0;
+        __syncthreads();
+        const int64_t tau = sh_tau;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int r = c0 + (int)threadIdx.x + kScanWarps * 32 * i;
+            const int64_t sc = scv[i];
+            if (r < r_end && sc * s1v[i] + sc * mv[i] * sum_abs >= tau) {
+                const int slot = atomicAdd(&sh_n, 1);
+                c_row[slot] = r;
+                c_sc[slot] = scv[i];
+                c_s1[slot] = s1v[i];
+            }
+        }
+        __syncthreads();
+        const int nc = sh_n;
+        for (int i = 2 * warp; i < nc; i += 2 * kScanWarps) {
+            const bool two = i + 1 < nc;
+            const int r0 = c_row[i], r1 = two ? c_row[i + 1] : r0;
             uint4 h0[CPL], h1[CPL];
 #pragma unroll
             for (int j = 0; j < CPL; j++) {
@@ -371,15 +420,23 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
             }
             const int t0 = tgi::warp_sum_i32(a0);
             const int t1 = tgi::warp_sum_i32(a1);
-            const int64_t sc0 = __shfl_sync(0xffffffffu, sc, src0), s10 = __shfl_sync(0xffffffffu, s1, src0);
-            const int64_t sc1 = __shfl_sync(0xffffffffu, sc, src1), s11 = __shfl_sync(0xffffffffu, s1, src1);
-            // lane 0 appends the first row, lane 1 the second
-            const int64_t e0 = sc0 * (s10 + (int64_t)t0), e1 = sc1 * (s11 + (int64_t)t1);
-            const bool take = lane == 0 || (two && lane == 1);
-            const int64_t e = lane == 0 ? e0 : e1;
-            const int rr = lane == 0 ? r0 : r1;
-            append_key(ws, take, to_ordered(e * (low_mask + 1) + (low_mask - rr)), e);
+            // lane 0 finishes the first row, lane 1 the second: the exact logit is
+            // counted, and its key replaces the row's stage-1 sum in the list
+            if (lane == 0 || (two && lane == 1)) {
+                const int src = i + lane;
+                const int64_t e = (int64_t)c_sc[src] * (c_s1[src] + (int64_t)(lane == 1 ? t1 : t0));
+                c_s1[src] = (int64_t)to_ordered(e * (low_mask + 1) + (low_mask - c_row[src]));
+                count_score(ws.hist_cand, e);
+            }
         }
+        // the pass's keys go out together: one counter update per CTA
+        __syncthreads();
+        if (threadIdx.x == 0 && nc > 0)
+            sh_base = atomicAdd(ws.count, (unsigned long long)nc);
+        __syncthreads();
+        for (int i = (int)threadIdx.x; i < nc; i += (int)blockDim.x)
+            ws.cand[sh_base + i] = (uint64_t)c_s1[i];
+        __syncthreads();   // the list is read before the next pass refills it
     }
 }
 
@@ -388,6 +445,8 @@ __global__ void __launch_bounds__(256)
 lmh_collect_kernel(const int64_t *__restrict__ logits, Ws ws, int N, int k, int idx_bits)
 {
     __shared__ int64_t sh_tau;
+    tgi::pdl_launch_dependents();
+    tgi::pdl_wait();   // launched as a programmatic dependent of the full scan
     if (threadIdx.x < 32) {
         const int64_t tau = warp_kth_bin_edge(ws.hist_row, k);
         if (threadIdx.x == 0)
@@ -532,6 +591,9 @@ __global__ void __launch_bounds__(kSelThreads)
 lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32_t *__restrict__ ids,
                  int64_t *__restrict__ scores, int32_t *__restrict__ ncand)
 {
+    // the next kernel on the stream may launch now (it waits for this grid before
+    // it touches anything this call reads or writes)
+    tgi::pdl_launch_dependents();
     tgi::pdl_wait();   // launched as a programmatic dependent of the rescoring / collecting kernel
     extern __shared__ __align__(16) unsigned char dyn[];
     uint64_t *sel = reinterpret_cast<uint64_t *>(dyn);                                 // [kFilterMax]
@@ -540,6 +602,10 @@ lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32
     __shared__ int nsel;
     const int n = (int)*ws.count;
     const int64_t low_mask = ((int64_t)1 << idx_bits) - 1;
+    // this thread's first two candidate keys load while warp 0 finds tau2
+    const int i0 = (int)threadIdx.x, i1 = (int)threadIdx.x + kSelThreads;
+    const uint64_t u0 = i0 < n ? __ldcg(ws.cand + i0) : 0ull;
+    const uint64_t u1 = i1 < n ? __ldcg(ws.cand + i1) : 0ull;
     if (threadIdx.x < 32) {
         const int64_t tau = warp_kth_bin_edge(ws.hist_cand, k);
         if (threadIdx.x == 0) {
@@ -564,8 +630,10 @@ lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32
         if (take && slot < kFilterMax)
             sel[slot] = u;
     };
-    for (int b = 0; b < n; b += blockDim.x) {   // uniform over the block: full warps in append_sel
-        const int i = b + threadIdx.x;
+    append_sel(i0 < n && (from_ordered(u0) >> idx_bits) >= tau, u0);
+    append_sel(i1 < n && (from_ordered(u1) >> idx_bits) >= tau, u1);
+    for (int b = 2 * kSelThreads; b < n; b += kSelThreads) {   // uniform over the block: full warps in append_sel
+        const int i = b + (int)threadIdx.x;
         const uint64_t u = i < n ? ws.cand[i] : 0ull;
         append_sel(i < n && (from_ordered(u) >> idx_bits) >= tau, u);
     }
@@ -586,11 +654,54 @@ lmh_final_kernel(Ws ws, int k, int idx_bits, int32_t *__restrict__ argmax, int32
         m = nsel < kFilterMax ? nsel : kFilterMax;
     }
     const int kout = m < k ? m : k;
+    // Rank of key i = the number of larger keys (all keys are distinct). Each
+    // run of 32 keys is sorted (descending) by one warp, which gives every key
+    // its count within its run; the counts in the other runs come from binary
+    // searches, one (key, run) pair per thread, summed in shared memory (the
+    // radix select's bins are free by now).
+    unsigned *rank_of = &rs.hist[0][0];
+    static_assert(sizeof(rs.hist) >= kFilterMax * sizeof(unsigned), "rank array");
+    const int runs = (m + 31) >> 5;
+    {
+        const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+        for (int rr = warp; rr < runs; rr += kSelThreads / 32) {
+            const int i = rr * 32 + lane;
+            uint64_t u = i < m ? sel[i] : 0ull;   // padding sorts below every key
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const uint64_t o = __shfl_xor_sync(0xffffffffu, u, stride);
+                    const bool lower = (lane & stride) == 0, rising = (lane & size) == 0;
+                    u = (lower != rising) ? (u < o ? u : o) : (u > o ? u : o);
+                }
+            }
+            sel[i] = u;
+            rank_of[i] = (unsigned)lane;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < m * runs; t += blockDim.x) {
+        const int i = t / runs, rr = t - i * runs;
+        if (rr == (i >> 5))
+            continue;
+        const uint64_t u = sel[i];
+        const uint64_t *run = sel + rr * 32;
+        int lo = 0, hi = m - rr * 32 < 32 ? m - rr * 32 : 32;
+        while (lo < hi) {   // first position of the run holding a key below u
+            const int mid = (lo + hi) >> 1;
+            if (run[mid] > u)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        if (lo)
+            atomicAdd(rank_of + i, (unsigned)lo);
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < m; i += blockDim.x) {
         const uint64_t u = sel[i];
-        int rank = 0;
-        for (int j = 0; j < m; j++)
-            rank += sel[j] > u;
+        const int rank = (int)rank_of[i];
         if (rank < kout) {
             const int64_t key = from_ordered(u);
             ids[rank] = (int32_t)(low_mask - (key & low_mask));
@@ -627,30 +738,50 @@ Ws carve(void *ws, int64_t N)
     return w;
 }
 
+// Launch config of a programmatic dependent of the previous kernel on the stream.
+struct PdlLaunch {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    PdlLaunch(int grid, int threads, size_t smem, cudaStream_t st)
+    {
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+};
+
 template <int CPL>
-void launch_scan(bool full, int grid, cudaStream_t st, const int8_t *hi, const int8_t *lo,
-                 const int32_t *s, const uint8_t *m, const int8_t *x, int64_t *logits, Ws ws, int N, int K)
+cudaError_t launch_scan(bool full, int grid, cudaStream_t st, const int8_t *hi, const int8_t *lo,
+                        const int32_t *s, const uint8_t *m, const int8_t *x, int64_t *logits, Ws ws, int N, int K)
 {
+    // The scans use no shared memory; ask for an SM configuration with room for
+    // the rescoring or collecting CTAs that launch beside them.
+    static const cudaError_t carve = [] {
+        cudaError_t e = cudaFuncSetAttribute(lmh_stage1_kernel<CPL>,
+                                             cudaFuncAttributePreferredSharedMemoryCarveout, 25);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(lmh_full_kernel<CPL>, cudaFuncAttributePreferredSharedMemoryCarveout, 25);
+        return e;
+    }();
+    if (carve != cudaSuccess)
+        return carve;
+    PdlLaunch l(grid, kScanWarps * 32, 0, st);
     if (full)
-        lmh_full_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(hi, lo, s, x, logits, ws, N, K);
-    else
-        lmh_stage1_kernel<CPL><<<grid, kScanWarps * 32, 0, st>>>(hi, s, m, x, ws, N, K);
+        return cudaLaunchKernelEx(&l.cfg, lmh_full_kernel<CPL>, hi, lo, s, x, logits, ws, N, K);
+    return cudaLaunchKernelEx(&l.cfg, lmh_stage1_kernel<CPL>, hi, s, m, x, ws, N, K);
 }
 
 template <int CPL>
 cudaError_t launch_rescore(int grid, cudaStream_t st, const int8_t *lo, const int32_t *s, const uint8_t *m,
-                    const int8_t *x, Ws ws, int N, int K, int k, int idx_bits)
+                           const int8_t *x, Ws ws, int N, int K, int k, int idx_bits)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kScanWarps * 32);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lmh_rescore_kernel<CPL>, lo, s, m, x, ws, N, K, k, idx_bits);
+    PdlLaunch l(grid, kScanWarps * 32, 0, st);
+    return cudaLaunchKernelEx(&l.cfg, lmh_rescore_kernel<CPL>, lo, s, m, x, ws, N, K, k, idx_bits);
 }
 
 }  // namespace
@@ -711,36 +842,48 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
     const int n = (int)N, kk = (int)K;
 
     // the candidate count and both histograms start at zero every call
-    if (cudaMemsetAsync(ws, 0, kClearedBytes, st) != cudaSuccess)
-        return TG_ERR_CUDA;
+    static_assert(kClearedBytes % 16 == 0, "cleared region in 16-byte words");
+    {
+        PdlLaunch cl(1, 256, 0, st);
+        if (cudaLaunchKernelEx(&cl.cfg, lmh_clear_kernel, static_cast<uint4 *>(ws), (int)(kClearedBytes / 16)) !=
+            cudaSuccess)
+            return TG_ERR_CUDA;
+    }
 
+    cudaError_t re = cudaSuccess;
 #define TGI_CPL_CASE(C)                                                                            \
     case C:                                                                                        \
-        launch_scan<C>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);                       \
+        re = launch_scan<C>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);                  \
         break;
     switch (cpl) {
         TGI_CPL_CASE(1) TGI_CPL_CASE(2) TGI_CPL_CASE(3) TGI_CPL_CASE(4) TGI_CPL_CASE(5)
         TGI_CPL_CASE(6) TGI_CPL_CASE(7) TGI_CPL_CASE(8)
     default:
-        launch_scan<16>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);
+        re = launch_scan<16>(full, grid, st, hi, lo, s, m, x, logits, wsp, n, kk);
         break;
     }
 #undef TGI_CPL_CASE
+    if (re != cudaSuccess)
+        return TG_ERR_CUDA;
 
-    cudaError_t re = cudaSuccess;
     if (full) {
         const int cgrid = (int)((N + 255) / 256 < nsm * 4 ? (N + 255) / 256 : nsm * 4);
-        lmh_collect_kernel<<<cgrid, 256, 0, st>>>(logits, wsp, n, k, idx_bits);
+        PdlLaunch cl(cgrid, 256, 0, st);
+        re = cudaLaunchKernelEx(&cl.cfg, lmh_collect_kernel, static_cast<const int64_t *>(logits), wsp, n, (int)k,
+                                idx_bits);
     } else {
+        // one rescoring CTA per SM (it fits beside the scan's CTAs), none without rows
+        const int64_t rows_cta = kScanWarps * 32;
+        const int rgrid = (int)((N + rows_cta - 1) / rows_cta < nsm ? (N + rows_cta - 1) / rows_cta : nsm);
 #define TGI_CPL_CASE(C)                                                                            \
     case C:                                                                                        \
-        re = launch_rescore<C>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);                    \
+        re = launch_rescore<C>(rgrid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);                   \
         break;
         switch (cpl) {
             TGI_CPL_CASE(1) TGI_CPL_CASE(2) TGI_CPL_CASE(3) TGI_CPL_CASE(4) TGI_CPL_CASE(5)
             TGI_CPL_CASE(6) TGI_CPL_CASE(7) TGI_CPL_CASE(8)
         default:
-            re = launch_rescore<16>(grid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);
+            re = launch_rescore<16>(rgrid, st, lo, s, m, x, wsp, n, kk, k, idx_bits);
             break;
         }
 #undef TGI_CPL_CASE
@@ -751,17 +894,8 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
     if (cudaFuncSetAttribute(lmh_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)final_smem) != cudaSuccess)
         return TG_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = final_smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, lmh_final_kernel, wsp, k, idx_bits, argmax, ids, scores, ncand) != cudaSuccess)
+    PdlLaunch fl(1, kSelThreads, final_smem, st);
+    if (cudaLaunchKernelEx(&fl.cfg, lmh_final_kernel, wsp, k, idx_bits, argmax, ids, scores, ncand) != cudaSuccess)
         return TG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
