@@ -37,6 +37,25 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
     return v;
 }
 
+// L2 policy for data read once per call (a weight stream larger than L2): its
+// lines are the first evicted, so the stream recycles a small part of L2 and the
+// rest -- kernel code, activations, per-row sums, histograms -- stays resident.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ int64_t warp_sum_i64(int64_t v)
 {
 #pragma unroll
