@@ -3,8 +3,10 @@
 // BitNetTwoStageDecode; lowest-index tie-break from integer_engine.md §3.3).
 //
 // Weights arrive as two balanced base-3 digit groups per weight (tg.h):
-// hi = planes 0-3 and lo = planes 4-7, both int8 in [-40, 40], W = 81 hi + lo.
-// A row's dot products with x are plain signed-byte dp4a sums.
+// hi = planes 0-3 and lo = planes 4-7, both int8 in [-40, 40], W = 81 hi + lo,
+// in rows of 2K bytes (the row's hi, then its lo; the pointers hi and lo below
+// point at row 0's and advance by 2K per row). A row's dot products with x are
+// plain signed-byte dp4a sums.
 //
 // Two-stage path (logits == NULL), all on one stream, no host round trip:
 //   1. scan     every row: s1 = 81 * sum hi*x. Its planes 4-7 residual is at
@@ -69,6 +71,9 @@ constexpr int kHistWords = kHistBins + kCoarseBins;   // one histogram: fine bin
 constexpr size_t kClearedBytes = 256 + 2 * (size_t)kHistWords * sizeof(unsigned);
 
 __device__ __forceinline__ uint64_t to_ordered(int64_t v) { return (uint64_t)v ^ kSignBit; }
+
+// Byte offset of row r's digit group (hi or lo) from row 0's: rows of 2K bytes.
+__device__ __forceinline__ size_t row_off(int r, int K) { return (size_t)r * 2 * (size_t)K; }
 __device__ __forceinline__ int64_t from_ordered(uint64_t u) { return (int64_t)(u ^ kSignBit); }
 
 __device__ __forceinline__ int score_bin(int64_t v)
@@ -260,8 +265,8 @@ lmh_stage1_kernel(const int8_t *__restrict__ hi, const int32_t *__restrict__ s,
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += 2 * NW) {
         const int r2 = r + NW;
-        const int d1 = row_dot<CPL, true>(hi + (size_t)r * K, C16, lane, xr);
-        const int d2 = r2 < N ? row_dot<CPL, true>(hi + (size_t)r2 * K, C16, lane, xr) : 0;
+        const int d1 = row_dot<CPL, true>(hi + row_off(r, K), C16, lane, xr);
+        const int d2 = r2 < N ? row_dot<CPL, true>(hi + row_off(r2, K), C16, lane, xr) : 0;
         const int t1 = tgi::warp_sum_i32(d1);
         const int t2 = tgi::warp_sum_i32(d2);
         if (lane == 0) {
@@ -299,8 +304,8 @@ lmh_full_kernel(const int8_t *__restrict__ hi, const int8_t *__restrict__ lo,
 
     int64_t best = INT64_MIN;
     for (int r = wg; r < N; r += NW) {
-        const int dh = row_dot<CPL, false>(hi + (size_t)r * K, C16, lane, xr);
-        const int dl = row_dot<CPL, false>(lo + (size_t)r * K, C16, lane, xr);
+        const int dh = row_dot<CPL, false>(hi + row_off(r, K), C16, lane, xr);
+        const int dl = row_dot<CPL, false>(lo + row_off(r, K), C16, lane, xr);
         const int th = tgi::warp_sum_i32(dh);
         const int tl = tgi::warp_sum_i32(dl);
         if (lane == 0) {
@@ -410,9 +415,9 @@ lmh_rescore_kernel(const int8_t *__restrict__ lo, const int32_t *__restrict__ s,
 #pragma unroll
             for (int j = 0; j < CPL; j++) {
                 const int c = lane + 32 * j;
-                h0[j] = c < C16 ? tgi::ldg_stream(lo + (size_t)r0 * K + (size_t)c * 16, pol)
+                h0[j] = c < C16 ? tgi::ldg_stream(lo + row_off(r0, K) + (size_t)c * 16, pol)
                                 : make_uint4(0, 0, 0, 0);
-                h1[j] = (two && c < C16) ? tgi::ldg_stream(lo + (size_t)r1 * K + (size_t)c * 16, pol)
+                h1[j] = (two && c < C16) ? tgi::ldg_stream(lo + row_off(r1, K) + (size_t)c * 16, pol)
                                          : make_uint4(0, 0, 0, 0);
             }
             int a0 = 0, a1 = 0;

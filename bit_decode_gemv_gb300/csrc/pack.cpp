@@ -92,12 +92,13 @@ extern "C" int tg_layout_init(int kind, int64_t N, int64_t K, tg_layout *out)
     L.K = K;
     L.G = K / TG_GROUP;
     if (kind == TG_PLANES8) {
+        // rows of 2K bytes: planes 0-3 (K bytes) then planes 4-7 (K bytes)
         L.tiles = 0;
         L.mask_off = 0;
         L.mask_bytes = N * K;
-        L.aux_off = align_up(L.mask_off + L.mask_bytes);
+        L.aux_off = K;
         L.aux_bytes = N * K;
-        L.scale_off = align_up(L.aux_off + L.aux_bytes);
+        L.scale_off = align_up(2 * N * K);
         L.scale_bytes = N * 4;
         L.aux2_off = align_up(L.scale_off + L.scale_bytes);
         L.aux2_bytes = N;
@@ -336,8 +337,8 @@ extern "C" int tg_pack_weights(int kind, int64_t N, int64_t K, const int8_t *tri
                         else
                             lo = lo * 3 + v;
                     }
-                    out[L.mask_off + r * K + i] = (uint8_t)(int8_t)hi;
-                    out[L.aux_off + r * K + i] = (uint8_t)(int8_t)lo;
+                    out[L.mask_off + 2 * r * K + i] = (uint8_t)(int8_t)hi;
+                    out[L.aux_off + 2 * r * K + i] = (uint8_t)(int8_t)lo;
                     m = std::max(m, lo < 0 ? -lo : lo);
                 }
                 out[L.aux2_off + r] = (uint8_t)m;

@@ -115,11 +115,15 @@ enum {
  *          W_negative bits at 7-r' and 15-r', the second's at 23-r' and 31-r'.
  *   scales [tiles][G][16]: uint8 LNS8 code of row 16*tile + i.
  *   Rows N..16*tiles-1 are padding: zero masks, zero codes.
- * TG_PLANES8:
- *   masks  [N][K] int8, planes 0-3 as one balanced base-3 number per weight,
- *          hi = 27 t0 + 9 t1 + 3 t2 + t3 in [-40, 40];
- *   aux    [N][K] int8, planes 4-7 the same way, lo = 27 t4 + 9 t5 + 3 t6 + t7,
- *          so W = 81 hi + lo;
+ * TG_PLANES8: rows of 2K bytes, row r at byte 2rK of the blob (mask_off = 0):
+ *   masks  the row's first K bytes (hi at mask_off + 2rK), int8, planes 0-3 as
+ *          one balanced base-3 number per weight, hi = 27 t0 + 9 t1 + 3 t2 + t3
+ *          in [-40, 40];
+ *   aux    its next K bytes (lo at aux_off + 2rK, aux_off = K), int8, planes
+ *          4-7 the same way, lo = 27 t4 + 9 t5 + 3 t6 + t7, so W = 81 hi + lo
+ *          (one row's two digit groups are adjacent: the full scan then reads
+ *          one contiguous stream, measured 13% faster than two regions);
+ *          mask_bytes = aux_bytes = N * K;
  *   scales [N] int32 row scale s[r] >= 1;
  *   aux2   [N] uint8, m[r] = max_i |lo[r][i]| (<= 40), the row's own bound on
  *          the planes 4-7 residual (0 for an exactly-ternary row).

@@ -175,8 +175,11 @@ def test_pack_planes_layout():
     w = W.lm_head(seed=2, N=37, K=256)
     blob, L = tg.tg_pack_weights(tg.TG_PLANES8, w["planes"], w["s"])
     N, K = 37, 256
-    hi = blob[L.mask_off:L.mask_off + N * K].view(np.int8).reshape(N, K).astype(np.int64)
-    lo = blob[L.aux_off:L.aux_off + N * K].view(np.int8).reshape(N, K).astype(np.int64)
+    # rows of 2K bytes: the row's planes 0-3 digits, then its planes 4-7 digits
+    assert L.mask_off == 0 and L.aux_off == K and L.mask_bytes == L.aux_bytes == N * K
+    assert L.scale_off >= 2 * N * K and L.scale_off % 256 == 0
+    rows = blob[:2 * N * K].view(np.int8).reshape(N, 2 * K).astype(np.int64)
+    hi, lo = rows[:, :K], rows[:, K:]
     pw = np.array([3 ** (7 - p) for p in range(8)], dtype=np.int64)
     Wint = np.tensordot(pw, w["planes"].astype(np.int64), axes=(0, 0))
     np.testing.assert_array_equal(81 * hi + lo, Wint)
