@@ -18,30 +18,31 @@
 // the host picks the fewest tiles per CTA that still fill one wave) for all
 // groups and all tokens. 16 compute warps, two MMA warps and a copy warp hand
 // work to each other through mbarrier rings, with no CTA-wide barrier inside
-// the group loop.
+// the group loop; work moves between them in pairs of groups, so that each
+// wait, fence and arrival serves two groups.
 //   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
 //     rows of mask tile w%4; a warp whose tile the CTA does not own only
 //     converts activations) and handles part p = w/4. In its iteration for
-//     group g it first reads back group g-2's D buffer for tokens
-//     16p..16p+15, accumulates it, and refills that buffer with the offset for
-//     group g+2; then expands its 32 weights of group g (group lanes
-//     32p..32p+31, from the input ring) to fp16, one byte permute per two
-//     weights, into A slot g%3 in tensor memory (row = lane, K along the
-//     columns), converts two 8-byte activation chunks (from the input ring)
-//     into B slot g%3 in shared memory, in the canonical K-major layout of
-//     8-row x 16-byte core matrices, and arrives on the slot's "full" barrier.
-//     The compute warps issue no global loads at all.
-//   - Two MMA warps take the even and the odd groups. When A/B slot g%3 is full
-//     and D buffer g%4 has been refilled, one thread issues the eight K=16
-//     steps of group g and commits them to the slot's "empty" and the buffer's
-//     "full" barriers. (One thread issues an MMA only every ~70 cycles, so two
-//     issuers keep the tensor core busier.)
-//   - A copy warp fills a 6-deep ring of input stages with bulk and tensor
-//     (TMA) copies: per group the mask bytes and scales of the four tiles and
-//     the 64 x 128 activation box (128-byte swizzle, so the compute warps'
-//     16-byte reads of eight token rows hit eight different bank groups); it
-//     refills the stage of group g with group g+6 once every compute warp has
-//     arrived on that stage's "empty" barrier.
+//     pair P it expands its 32 weights of each group (group lanes 32p..32p+31,
+//     from the input ring) to fp16, one byte permute per two weights, into A
+//     slot P%2 in tensor memory (row = lane, K along the columns), converts
+//     two 8-byte activation chunks per group (from the input ring) into B slot
+//     P%2 in shared memory, in the canonical K-major layout of 8-row x 16-byte
+//     core matrices, and arrives on the slot's "full" barrier; then it reads
+//     back pair P-1's D buffer for tokens 16p..16p+15 (those MMAs ran while
+//     pair P was prepared), accumulates it, and refills the buffer with the
+//     offset for pair P+1. The compute warps issue no global loads at all.
+//   - MMA warp w takes the pairs P = w mod 2, with A/B slot w and D buffer w.
+//     When the slot is full and the buffer refilled, one thread issues the
+//     sixteen K=16 steps of the pair and commits them to the slot's "empty" and
+//     the buffer's "full" barriers.
+//   - A copy warp fills a 3-deep ring of input stages with bulk and tensor
+//     (TMA) copies: per pair the mask bytes and scales of the tiles (a tile's
+//     two groups are adjacent in the blob) and one 64 x 128 activation box per
+//     group (128-byte swizzle, so the compute warps' 16-byte reads of eight
+//     token rows hit eight different bank groups); it refills the stage of pair
+//     P with pair P+3 once every compute warp has arrived on that stage's
+//     "empty" barrier.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -58,30 +59,32 @@ TGI_DEFINE_DEVICE_ERROR(gemv_mma_take_device_error)
 namespace {
 
 constexpr int kComputeWarps = 16;   // 4 row quarters x 4 parts (32 weights and 16 tokens each)
-constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd groups)
+constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd pairs)
 constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
 constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
 constexpr int kMaxN = 64;                 // tokens, the MMA's N at most
-constexpr int kStages = 6;                // input ring stages (masks, scales, activations of one group)
-constexpr int kSlots = 3;                 // A/B slots
-constexpr int kDBufs = 4;                 // D buffers
-constexpr int kLag = 2;                   // the epilogue of group g runs after the inputs of group g + kLag
+constexpr int kPair = 2;                  // groups per handshake: work moves between warps in pairs
+constexpr int kStages = 3;                // input ring stages (masks, scales, activations of one pair)
+constexpr int kSlots = 2;                 // A/B slots, one pair each
+constexpr int kDBufs = 2;                 // D buffers, one pair each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0;             // A slots: 64 columns each (128 fp16 of K per row)
-constexpr uint32_t kColD = 64 * kSlots;   // D buffers: kMaxN columns each
-static_assert(kColD + kDBufs * kMaxN <= kTmemCols, "tensor memory plan");
-static_assert(kMaxN == 64, "each compute warp reads and refills 32 D columns");
+constexpr uint32_t kColA = 0;                       // A slots: 128 columns each (2 x 128 fp16 of K per row)
+constexpr uint32_t kColD = 128 * kSlots;            // D buffers: 2 x kMaxN columns each
+static_assert(kColD + kDBufs * kPair * kMaxN <= kTmemCols, "tensor memory plan");
+static_assert(kMaxN == 64, "each compute warp reads and refills 16 D columns of each group");
+static_assert(kSlots == kMmaWarps && kDBufs == kMmaWarps, "MMA warp w owns A/B slot w and D buffer w");
 constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^23
 
 // Shared-memory plan (dynamic), byte offsets.
 constexpr int kKStepBytes = (kMaxN / 8) * 256;         // one K=16 step of B: token octets x 256 B
 constexpr int kBBytes = 8 * kKStepBytes;               // one group of B
-constexpr int kOffB = 0;                               // kSlots B slots
-constexpr int kOffStages = kOffB + kSlots * kBBytes;   // 1024-aligned: the activation box is swizzled
-constexpr int kStageMask = 0;                          // masks of 4 tiles, 1 KB each
-constexpr int kStageScale = 4096;                      // scales of 4 tiles, 128 B each
-constexpr int kStageX = 5120;                          // activations: 64 tokens x 128 B, 128-byte swizzle
-constexpr int kStageBytes = kStageX + kMaxN * TG_GROUP;
+constexpr int kOffB = 0;                               // kSlots B slots of a pair each
+constexpr int kOffStages = kOffB + kSlots * kPair * kBBytes;   // 1024-aligned: the activation box is swizzled
+constexpr int kStageMask = 0;                          // masks [tile][group of the pair]: 2 KB per tile
+constexpr int kStageScale = 8192;                      // scales [tile][group]: 256 B per tile
+constexpr int kStageX = 9216;                          // activations [group]: 64 tokens x 128 B, 128-byte swizzle
+constexpr int kStageXBytes = kMaxN * TG_GROUP;
+constexpr int kStageBytes = kStageX + kPair * kStageXBytes;
 // mbarriers: input stage full/empty, A/B slot full/empty, D buffer full/empty. Every
 // waiter of a barrier is also needed for that barrier's next phase to complete, so no
 // waiter can see a phase completed twice over (which would make it wait forever).
@@ -91,8 +94,8 @@ constexpr int kOffAcc = kOffStages + kStages * kStageBytes;   // int64 accumulat
 constexpr int kOffBar = kOffAcc + kMaxN * kRowsPerCta * 8;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;   // + slack to align the base to 1024 bytes
-static_assert(kStageBytes % 1024 == 0 && kOffStages % 1024 == 0 && kStageX % 1024 == 0,
-              "bulk copies need 16-byte and the swizzled activation box 1024-byte alignment");
+static_assert(kStageBytes % 1024 == 0 && kOffStages % 1024 == 0 && kStageX % 1024 == 0 && kStageXBytes % 1024 == 0,
+              "bulk copies need 16-byte and the swizzled activation boxes 1024-byte alignment");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -380,56 +383,63 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         }
     };
 
+    const int npairs = (G + kPair - 1) / kPair;
     if (warp == kComputeWarps + kMmaWarps) {
-        // ---------------- copy warp: inputs of group g -> stage g % kStages ----------------
-        const uint32_t tx = (uint32_t)tiles_here * (kMaskBytes + 128u) + (uint32_t)(kMaxN * TG_GROUP);
-        auto copy_inputs = [&](int g) {
-            const int st = g % kStages;
+        // ---------------- copy warp: inputs of pair P -> stage P % kStages ----------------
+        auto copy_inputs = [&](int P) {
+            const int st = P % kStages, g0 = kPair * P;
+            const int ng = min(kPair, G - g0);
             const uint32_t sdst = sbase + kOffStages + st * kStageBytes;
             const uint32_t b = bar(kBarMFull + st);
             if (lane == 0)
-                mbar_expect_tx(b, tx);
+                mbar_expect_tx(b, (uint32_t)(tiles_here * ng) * (kMaskBytes + 128u) + (uint32_t)(ng * kStageXBytes));
             __syncwarp();
             if (lane < tiles_here) {
-                const size_t unit = (size_t)(blockIdx.x * ctiles + lane) * G + g;
-                bulk_copy(sdst + kStageMask + lane * 1024, masks + unit * kMaskBytes, kMaskBytes, b);
-                bulk_copy(sdst + kStageScale + lane * 128, scales + unit * 128, 128, b);
-            } else if (lane == 31) {
-                // 64 token rows x 128 bytes of group g (rows from M on read as zero)
-                tensor_copy_2d(sdst + kStageX, &xmap, g * TG_GROUP, 0, b);
+                // the pair's groups of one tile are adjacent in the blob
+                const size_t unit = (size_t)(blockIdx.x * ctiles + lane) * G + g0;
+                bulk_copy(sdst + kStageMask + lane * 2048, masks + unit * kMaskBytes, (uint32_t)ng * kMaskBytes, b);
+                bulk_copy(sdst + kStageScale + lane * 256, scales + unit * 128, (uint32_t)ng * 128u, b);
+            } else if (lane >= 32 - ng) {
+                // 64 token rows x 128 bytes of group g0 + h (rows from M on read as zero)
+                const int h = 31 - lane;
+                tensor_copy_2d(sdst + kStageX + h * kStageXBytes, &xmap, (g0 + h) * TG_GROUP, 0, b);
             }
             __syncwarp();
         };
-        for (int g = 0; g < min(G, kStages); g++)
-            copy_inputs(g);
-        for (int g = 0; g + kStages < G; g++) {
-            // every compute warp has read stage g % kStages
+        for (int P = 0; P < min(npairs, kStages); P++)
+            copy_inputs(P);
+        for (int P = 0; P + kStages < npairs; P++) {
+            // every compute warp has read stage P % kStages
             if (lane == 0)
-                wait(kBarMEmpty + g % kStages, (uint32_t)(g / kStages) & 1u);
+                wait(kBarMEmpty + P % kStages, (uint32_t)(P / kStages) & 1u);
             __syncwarp();
             if (__shfl_sync(0xffffffffu, abort_flag, 0))
                 break;
-            copy_inputs(g + kStages);
+            copy_inputs(P + kStages);
         }
     } else if (warp >= kComputeWarps) {
-        // ---------------- MMA warps: groups g = (warp - kComputeWarps) mod 2 ----------------
+        // ---------------- MMA warp w: pairs P = w mod 2, A/B slot and D buffer w ----------------
         const uint32_t idesc = instr_desc(nmma);
+        const int w = warp - kComputeWarps;
         if (lane == 0) {
-            for (int g = warp - kComputeWarps; g < G && !abort_flag; g += kMmaWarps) {
-                const int sl = g % kSlots, db = g % kDBufs;
-                wait(kBarABFull + sl, (uint32_t)(g / kSlots) & 1u);
-                wait(kBarDEmpty + db, (uint32_t)(g / kDBufs) & 1u);   // refilled with the offset
+            for (int P = w; P < npairs && !abort_flag; P += kMmaWarps) {
+                const uint32_t par = (uint32_t)(P / kMmaWarps) & 1u;
+                wait(kBarABFull + w, par);
+                wait(kBarDEmpty + w, par);   // refilled with the offset
                 if (abort_flag)
                     break;
                 fence_after_sync();
-                const uint32_t dt = tmem + kColD + (uint32_t)(kMaxN * db);
-                const uint32_t Bs = sbase + kOffB + sl * kBBytes;
+                const int ng = min(kPair, G - kPair * P);
+                for (int h = 0; h < ng; h++) {
+                    const uint32_t dt = tmem + kColD + (uint32_t)(kPair * kMaxN * w + kMaxN * h);
+                    const uint32_t at = tmem + kColA + (uint32_t)(128 * w + 64 * h);
+                    const uint32_t Bs = sbase + kOffB + (uint32_t)((kPair * w + h) * kBBytes);
 #pragma unroll
-                for (int ks = 0; ks < 8; ks++)
-                    mma_a_tmem(dt, tmem + kColA + 64u * (uint32_t)sl + 8u * ks, smem_desc(Bs + ks * kKStepBytes),
-                               idesc, 1u);
-                mma_commit(bar(kBarABEmpty + sl));
-                mma_commit(bar(kBarDFull + db));
+                    for (int ks = 0; ks < 8; ks++)
+                        mma_a_tmem(dt, at + 8u * ks, smem_desc(Bs + ks * kKStepBytes), idesc, 1u);
+                }
+                mma_commit(bar(kBarABEmpty + w));
+                mma_commit(bar(kBarDFull + w));
             }
         }
         __syncwarp();
@@ -454,11 +464,11 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         const bool x_ok = xn < M;
         const int xoff = kStageX + xn * TG_GROUP + ((j16 ^ (xn & 7)) << 4);
 
-        // D buffers of groups 0..kDBufs-1 start at the offset 1.5 * 2^23
+        // D buffers (both groups of a pair) start at the offset 1.5 * 2^23
         const uint32_t dbase = tmem + lane_off + kColD + 16u * (uint32_t)p;
 #pragma unroll 1
-        for (int db = 0; db < kDBufs; db++)
-            tmem_st16_same(dbase + (uint32_t)(kMaxN * db), kOffsetBits);
+        for (int c = 0; c < kDBufs * kPair; c++)
+            tmem_st16_same(dbase + (uint32_t)(kMaxN * c), kOffsetBits);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
@@ -485,139 +495,129 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             dblk = 0;
             nblk = 0;
         };
-        int d_lag[2] = {0, 0};   // scale of group g, kept for its epilogue kLag groups later
+        // accumulate one group's D (tokens 16p..16p+15 of this warp's rows) scaled by dgp
+        auto fold = [&](uint32_t (&v)[16], int dgp) {
+            if (kNarrow) {
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                    acc32[j] += v[j] * (uint32_t)dgp;
+                dblk += (uint32_t)dgp;
+                if (++nblk == kBlock)
+                    flush();
+            } else if (kFold == kFoldWide) {
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                    accs[128 * j] = (int64_t)mad_wide(v[j], dgp, (uint64_t)accs[128 * j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int32_t P = (int32_t)(v[j] - kOffsetBits);
+                    accs[128 * j] += ((int64_t)P * dgp) >> frac;   // the group's floor
+                }
+            }
+        };
+        // read back pair P's D buffer db (ng groups), accumulate it, and refill it
+        // with the offset for pair P + kDBufs if there is one
+        auto epilogue = [&](int db, uint32_t par, int ng, const int (&dprev)[kPair], bool refill) {
+            if (!epi)
+                return;
+            wait(kBarDFull + db, par);
+            fence_after_sync();
+            const uint32_t dcol = dbase + (uint32_t)(kPair * kMaxN * db);
+            uint32_t v0[16], v1[16];
+            tmem_ld16(dcol, v0);
+            if (ng > 1)
+                tmem_ld16(dcol + kMaxN, v1);
+            tmem_wait_ld(v0);
+            if (ng > 1)
+                tmem_wait_ld(v1);
+            if (refill) {
+                tmem_st16_same(dcol, kOffsetBits);
+                tmem_st16_same(dcol + kMaxN, kOffsetBits);
+            }
+            fold(v0, dprev[0]);
+            if (ng > 1)
+                fold(v1, dprev[1]);
+        };
 
-        // ring positions of group g, advanced by counters
-        int sl = 0, st = 0;              // A/B slot, input stage
-        uint32_t sl_par = 0, st_par = 0;  // phase parities of those uses
-        int db_e = 0;                    // D buffer of group g - kLag
-        uint32_t db_par = 0;
-        // this thread's 32 weights: group lanes 32p..32p+31 = words 2(p%2), 2(p%2)+1 of half p/2
-        // Q1: word p of the row's 16 bytes (group lanes 32p..32p+31)
-        const unsigned char *mrow = kQ1 ? smem + kOffStages + kStageMask + q * 1024 + lane * 16 + 4 * p
-                                        : smem + kOffStages + kStageMask + q * 1024 + (p >> 1) * 512 + lane * 16 +
+        int dprev[kPair] = {0, 0};   // scales of the previous pair, for its epilogue
+        // this thread's 32 weights of a group: group lanes 32p..32p+31 = words 2(p%2), 2(p%2)+1
+        // of half p/2; Q1: word p of the row's 16 bytes (group lanes 32p..32p+31)
+        const unsigned char *mrow = kQ1 ? smem + kOffStages + kStageMask + q * 2048 + lane * 16 + 4 * p
+                                        : smem + kOffStages + kStageMask + q * 2048 + (p >> 1) * 512 + lane * 16 +
                                               (p & 1) * 8;
-        const unsigned char *srow = smem + kOffStages + kStageScale + q * 128 + lane * 4;
+        const unsigned char *srow = smem + kOffStages + kStageScale + q * 256 + lane * 4;
         const unsigned char *xrow = smem + kOffStages + xoff;
         const uint32_t abase = tmem + lane_off + kColA + 16u * (uint32_t)p;
         // B position of chunks 2 j16 and 2 j16 + 1 of token xn: K-step j16, core matrices 0 and 1
         unsigned char *bdst = smem + kOffB + j16 * kKStepBytes + (xn >> 3) * 256 + (xn & 7) * 16;
 
-        // read back group gp's D buffer (db_e) -- issued by epi_load, consumed by
-        // epi_fold once the group's other work has been issued -- accumulate it,
-        // and refill the buffer with the offset
-        auto epi_load = [&](uint32_t (&v)[16]) {
-            wait(kBarDFull + db_e, db_par);
-            fence_after_sync();
-            if (epi)
-                tmem_ld16(dbase + (uint32_t)(kMaxN * db_e), v);
-        };
-        auto epi_fold = [&](uint32_t (&v)[16], int dgp, bool refill) {
-            const uint32_t dcol = dbase + (uint32_t)(kMaxN * db_e);
-            if (epi) {
-                tmem_wait_ld(v);
-                if (refill)
-                    tmem_st16_same(dcol, kOffsetBits);
-                if (kNarrow) {
-#pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        acc32[j] += v[j] * (uint32_t)dgp;
-                    dblk += (uint32_t)dgp;
-                    if (++nblk == kBlock)
-                        flush();
-                } else if (kFold == kFoldWide) {
-#pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        accs[128 * j] = (int64_t)mad_wide(v[j], dgp, (uint64_t)accs[128 * j]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const int32_t P = (int32_t)(v[j] - kOffsetBits);
-                        accs[128 * j] += ((int64_t)P * dgp) >> frac;   // the group's floor
-                    }
-                }
-            } else if (refill) {
-                tmem_st16_same(dcol, kOffsetBits);
-            }
-        };
-        auto next_db = [&]() {
-            if (++db_e == kDBufs) {
-                db_e = 0;
-                db_par ^= 1u;
-            }
-        };
-
-        static_assert(kLag == 2, "the scale history below keeps two groups");
+        int st = 0;
+        uint32_t st_par = 0;
 #pragma unroll 1
-        for (int g0 = 0; g0 < G; g0 += 2) {
+        for (int P = 0; P < npairs; P++) {
+            const int sl = P & 1;                        // A/B slot and D buffer of pair P (= its MMA warp)
+            const uint32_t sl_par = (uint32_t)(P >> 1) & 1u;
+            const int ng = min(kPair, G - kPair * P);
+            if (P >= kSlots)   // A/B slot free: the MMAs of pair P - 2 are done
+                wait(kBarABEmpty + sl, sl_par ^ 1u);
+            wait(kBarMFull + st, st_par);
+            int dg[kPair] = {0, 0};
 #pragma unroll
-            for (int bb = 0; bb < 2; bb++) {   // g & 1: which scale history register, static
-                const int g = g0 + bb;
-                if (g >= G)
-                    break;
-                const bool refill = g >= kLag && g - kLag + kDBufs < G;
-                if (g >= kSlots)   // A/B slot free: the MMAs of group g - kSlots are done
-                    wait(kBarABEmpty + sl, sl_par ^ 1u);
-                wait(kBarMFull + st, st_par);
-                // this group's inputs from the stage, then group g - 2's D buffer (same
-                // parity as g), both in flight while the weights are expanded
-                uint2 mw = make_uint2(0, 0);
-                if (tile_ok)
-                    mw = kQ1 ? make_uint2(*reinterpret_cast<const uint32_t *>(mrow + st * kStageBytes), 0u)
-                             : *reinterpret_cast<const uint2 *>(mrow + st * kStageBytes);
-                const uint4 xv = x_ok ? *reinterpret_cast<const uint4 *>(xrow + st * kStageBytes)
-                                      : make_uint4(0, 0, 0, 0);
-                const int dg = tile_ok ? *reinterpret_cast<const int *>(srow + st * kStageBytes) : 0;
-                uint32_t v[16];
-                if (g >= kLag)
-                    epi_load(v);
-                if (rows_q) {
-                    uint32_t a[16];
-                    if (kQ1) {
-                        expand_word_q1(mw.x, a);
-                    } else {
-                        expand_word(mw.x, a);
-                        expand_word(mw.y, a + 8);
+            for (int h = 0; h < kPair; h++) {
+                if (h < ng) {
+                    uint2 mw = make_uint2(0, 0);
+                    if (tile_ok) {
+                        const unsigned char *mp = mrow + (size_t)st * kStageBytes + h * kMaskBytes;
+                        mw = kQ1 ? make_uint2(*reinterpret_cast<const uint32_t *>(mp), 0u)
+                                 : *reinterpret_cast<const uint2 *>(mp);
+                        dg[h] = *reinterpret_cast<const int *>(srow + (size_t)st * kStageBytes + h * 128);
                     }
-                    tmem_st16(abase + 64u * (uint32_t)sl, a);
-                }
-                if (x_ok) {
-                    unsigned char *B = bdst + sl * kBBytes;
-                    *reinterpret_cast<uint4 *>(B) = fp16_of_int8x8(make_uint2(xv.x, xv.y));
-                    *reinterpret_cast<uint4 *>(B + 128) = fp16_of_int8x8(make_uint2(xv.z, xv.w));
-                }
-                if (g >= kLag)
-                    epi_fold(v, d_lag[bb], refill);
-                dsum += (uint64_t)(int64_t)dg;
-                tmem_wait_st();   // A of group g and the refilled D buffer
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(kBarMEmpty + st));   // this warp is done with input stage st
-                    mbar_arrive(bar(kBarABFull + sl));
-                    if (refill)
-                        mbar_arrive(bar(kBarDEmpty + db_e));
-                }
-                if (g >= kLag)
-                    next_db();
-                d_lag[bb] = dg;
-                if (++sl == kSlots) {
-                    sl = 0;
-                    sl_par ^= 1u;
-                }
-                if (++st == kStages) {
-                    st = 0;
-                    st_par ^= 1u;
+                    if (rows_q) {
+                        uint32_t a[16];
+                        if (kQ1) {
+                            expand_word_q1(mw.x, a);
+                        } else {
+                            expand_word(mw.x, a);
+                            expand_word(mw.y, a + 8);
+                        }
+                        tmem_st16(abase + 128u * (uint32_t)sl + 64u * (uint32_t)h, a);
+                    }
+                    if (x_ok) {
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + (size_t)st * kStageBytes +
+                                                                          h * kStageXBytes);
+                        unsigned char *B = bdst + (sl * kPair + h) * kBBytes;
+                        *reinterpret_cast<uint4 *>(B) = fp16_of_int8x8(make_uint2(xv.x, xv.y));
+                        *reinterpret_cast<uint4 *>(B + 128) = fp16_of_int8x8(make_uint2(xv.z, xv.w));
+                    }
                 }
             }
+            dsum += (uint64_t)(int64_t)dg[0] + (uint64_t)(int64_t)dg[1];
+            // hand pair P to its MMA warp: A and B written (and the refill of its D buffer,
+            // done at the end of the previous iteration, complete)
+            tmem_wait_st();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(kBarMEmpty + st));   // this warp is done with input stage st
+                mbar_arrive(bar(kBarABFull + sl));
+                if (P >= kDBufs)   // D buffer sl, read back and refilled for pair P
+                    mbar_arrive(bar(kBarDEmpty + sl));
+            }
+            // then pair P - 1: its MMAs ran while this pair was prepared
+            if (P >= 1)
+                epilogue(sl ^ 1, (uint32_t)((P - 1) >> 1) & 1u, kPair, dprev, P - 1 + kDBufs < npairs);
+            dprev[0] = dg[0];
+            dprev[1] = dg[1];
+            if (++st == kStages) {
+                st = 0;
+                st_par ^= 1u;
+            }
         }
-        for (int gp = max(0, G - kLag); gp < G; gp++) {
-            uint32_t v[16];
-            epi_load(v);
-            epi_fold(v, (gp & 1) ? d_lag[1] : d_lag[0], false);
-            next_db();
-        }
+        if (npairs >= 1)
+            epilogue((npairs - 1) & 1, (uint32_t)((npairs - 1) >> 1) & 1u, min(kPair, G - kPair * (npairs - 1)),
+                     dprev, false);
         if (kNarrow && epi)
             flush();
         // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); otherwise acc_m
