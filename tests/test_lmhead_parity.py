@@ -104,3 +104,42 @@ def test_row_shards_merge_to_global_topk():
     np.testing.assert_array_equal(got_ids, ref_ids)
     np.testing.assert_array_equal(got_scores, ref_scores)
     assert got_ids[0] == oracle.argmax(logits_ref)
+
+
+def test_back_to_back_calls_read_x_written_just_before():
+    """Calls on one stream with no host synchronisation between them: before each
+    call a device copy rewrites x, and every call reuses one workspace. The call's
+    first kernel is a programmatic dependent of whatever precedes it, so it must
+    wait for that copy; each result must be the one for the x just written."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import dev, pack_to_device
+    w = W.lm_head(seed=11, N=20000, K=2560)
+    wd, L = pack_to_device(tg.TG_PLANES8, w["planes"], w["s"])
+    k = 50
+    xs = [W.lm_head(seed=20 + i, N=64, K=2560)["x"] for i in range(4)]
+    src = [dev(x) for x in xs]
+    xd = torch.empty_like(src[0])
+    wsb = tg.tg_lmhead_workspace_bytes(L, k)
+    ws = torch.full((wsb,), 0xAB, dtype=torch.uint8, device="cuda")
+    calls = []
+    for i in range(len(xs)):
+        for full in (False, True):
+            o = dict(logits=torch.full((L.N,), -7, dtype=torch.int64, device="cuda") if full else None,
+                     argmax=torch.full((1,), -7, dtype=torch.int32, device="cuda"),
+                     ids=torch.full((k,), -7, dtype=torch.int32, device="cuda"),
+                     scores=torch.full((k,), -7, dtype=torch.int64, device="cuda"),
+                     ncand=torch.full((1,), -7, dtype=torch.int32, device="cuda"))
+            xd.copy_(src[i])
+            tg.tg_lmhead_argmax_topk(L, wd, xd, k, o["logits"], o["argmax"], o["ids"], o["scores"], o["ncand"],
+                                     ws, wsb)
+            calls.append((i, full, o))
+    torch.cuda.synchronize()
+    for i, full, o in calls:
+        logits_ref = oracle.lmhead_logits(w["planes"], w["s"], xs[i])
+        ids_ref, top_ref = oracle.topk(logits_ref, k)
+        if full:
+            np.testing.assert_array_equal(o["logits"].cpu().numpy(), logits_ref)
+        np.testing.assert_array_equal(o["ids"].cpu().numpy(), ids_ref)
+        np.testing.assert_array_equal(o["scores"].cpu().numpy(), top_ref)
+        assert int(o["argmax"].item()) == oracle.argmax(logits_ref)
