@@ -89,43 +89,60 @@ __device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
 // contributes is returned: +-2^15 into phase 7 for k > 127, nothing for k <= 0.
 // With those lanes removed every remaining lane has k in 1..127 and the
 // factorised add is exact again.
+// The flagged lanes of chunk KC (raw: its four activation bytes of this quad
+// thread, w: the thread's mask word holding them).
+template <int KC>
+__device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, uint32_t T, uint32_t U, int e,
+                                            int *gcorr, int &clamp)
+{
+    const uint32_t a4 = raw & 0x7f7f7f7fu;
+    uint32_t m = (__vcmpgtu4(a4, T) | (__vcmpltu4(a4, U) & __vcmpne4(a4, 0u))) & 0x80808080u;
+    while (m) {
+        const int bi = (__ffs((int)m) - 1) >> 3;
+        m &= m - 1u;
+        const int rp = 4 * (KC & 1) + half + 2 * (bi >> 1);
+        const int h = bi & 1;
+        if (((w >> (16 * h + 7 - rp)) & 1u) == 0u)
+            continue;
+        const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
+        const uint32_t xab = (raw >> (8 * bi)) & 0xffu;
+        const int a = (int)(xab & 0x7fu);
+        const bool minus = ((xab >> 7) ^ neg) != 0u;
+        const int v = 1 << (a >> 3);
+        atomicAdd(gcorr + (a & 7), minus ? v : -v);
+        if (a + e > 127)
+            clamp += minus ? -(1 << 15) : (1 << 15);
+    }
+}
+
 __device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg, int *gcorr)
 {
     const uint32_t T = (uint32_t)min(max(127 - e, 0), 127) * 0x01010101u;   // a > 127 - e saturates
     const uint32_t U = (uint32_t)min(max(1 - e, 1), 128) * 0x01010101u;     // 0 < a < 1 - e is zero
     const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xg);
+    // chunk kc: lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1} (byte bi = 2 * rr + h).
+    // All sixteen loads are issued first, so that they are in flight together
+    // (inside the scan, behind its shared-memory atomics, they went one by one).
+    auto ld = [&](int kc) {
+        return (uint32_t)__ldg(x16 + 8 * kc + tq) | ((uint32_t)__ldg(x16 + 8 * kc + 4 + tq) << 16);
+    };
+    const uint32_t r0 = ld(0), r1 = ld(1), r2 = ld(2), r3 = ld(3), r4 = ld(4), r5 = ld(5), r6 = ld(6), r7 = ld(7);
     int clamp = 0;
-#pragma unroll
-    for (int kc = 0; kc < 8; kc++) {
-        // lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1}: byte bi = 2 * rr + h
-        const uint32_t raw = (uint32_t)__ldg(x16 + 8 * kc + tq) | ((uint32_t)__ldg(x16 + 8 * kc + 4 + tq) << 16);
-        const uint32_t a4 = raw & 0x7f7f7f7fu;
-        uint32_t m = (__vcmpgtu4(a4, T) | (__vcmpltu4(a4, U) & __vcmpne4(a4, 0u))) & 0x80808080u;
-        const uint32_t w = w4[kc >> 1];
-        while (m) {
-            const int bi = (__ffs((int)m) - 1) >> 3;
-            m &= m - 1u;
-            const int rp = 4 * (kc & 1) + half + 2 * (bi >> 1);
-            const int h = bi & 1;
-            if (((w >> (16 * h + 7 - rp)) & 1u) == 0u)
-                continue;
-            const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
-            const uint32_t xab = (raw >> (8 * bi)) & 0xffu;
-            const int a = (int)(xab & 0x7fu);
-            const bool minus = ((xab >> 7) ^ neg) != 0u;
-            const int v = 1 << (a >> 3);
-            atomicAdd(gcorr + (a & 7), minus ? v : -v);
-            if (a + e > 127)
-                clamp += minus ? -(1 << 15) : (1 << 15);
-        }
-    }
+    clamp_chunk<0>(r0, w4[0], half, T, U, e, gcorr, clamp);
+    clamp_chunk<1>(r1, w4[0], half, T, U, e, gcorr, clamp);
+    clamp_chunk<2>(r2, w4[1], half, T, U, e, gcorr, clamp);
+    clamp_chunk<3>(r3, w4[1], half, T, U, e, gcorr, clamp);
+    clamp_chunk<4>(r4, w4[2], half, T, U, e, gcorr, clamp);
+    clamp_chunk<5>(r5, w4[2], half, T, U, e, gcorr, clamp);
+    clamp_chunk<6>(r6, w4[3], half, T, U, e, gcorr, clamp);
+    clamp_chunk<7>(r7, w4[3], half, T, U, e, gcorr, clamp);
     return clamp;
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
 lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                 const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
-                PhaseF F, int N, int G, int gpc)
+                const __grid_constant__ PhaseF F, int N, int G, int gpc)
 {
     __shared__ uint2 vfrag[kChunkGroups][8][32];   // V fragments (b0, b1) per group, chunk, lane
     __shared__ unsigned gmin[kChunkGroups], gmax[kChunkGroups];
@@ -204,7 +221,6 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
             for (int gl = 0; gl < kChunkGroups; gl++) {
                 if (gl >= ng)
                     break;
-                const int grp = c0 + gl;
                 const uint32_t w4[4] = {wv[gl].x, wv[gl].y, wv[gl].z, wv[gl].w};
                 // two independent accumulation chains (even and odd chunks);
                 // each partial is an integer of magnitude below 2^23, so the
@@ -234,7 +250,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                     if (!clamp_free) {
                         int *gc = gcorr[warp][gq + 8 * half];
                         const unsigned qmask = 0xfu << (lane & ~3);
-                        clamp = clamp_lanes(w4, half, tq, e, xa + (size_t)grp * TG_GROUP, gc);
+                        clamp = clamp_lanes(w4, half, tq, e, xa + (size_t)(c0 + gl) * TG_GROUP, gc);
                         __syncwarp(qmask);
                         d[2 * half] += (float)gc[2 * tq];
                         d[2 * half + 1] += (float)gc[2 * tq + 1];
@@ -287,7 +303,16 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
             A[(size_t)row * 8 + p] = a;
     }
     if (S) {
-        // S: one thread per row, the eight terms in the order p = 0..7
+        // S: the products A[p] * F[p], one thread per (row, phase), written over A
+        // in shared memory (fp64 is slow on this part: a thread per row doing all
+        // eight measured ~2000 cycles), then one thread per row adds the eight
+        // terms in the order p = 0..7
+        __syncthreads();
+        double *prod = reinterpret_cast<double *>(&arow[0][0]);
+        static_assert(kWarps * 32 % 8 == 0, "a thread's phase p = tid & 7 is the same for all its items");
+        const double fp = F.f[tid & 7];   // F is a grid constant: indexed in place, not copied
+        for (int item = tid; item < rows_here * 8; item += blockDim.x)
+            prod[item] = __dmul_rn((double)arow[item >> 3][item & 7], fp);
         __syncthreads();
         for (int i = tid; i < rows_here; i += blockDim.x) {
             const int row = blockIdx.x * kRows + rank * slice + i;
@@ -295,7 +320,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 double sum = 0.0;
 #pragma unroll
                 for (int p = 0; p < 8; p++)
-                    sum = __dadd_rn(sum, __dmul_rn((double)arow[i][p], F.f[p]));
+                    sum = __dadd_rn(sum, prod[i * 8 + p]);
                 S[row] = __dmul_rn(sum, 0x1p-9);
             }
         }
