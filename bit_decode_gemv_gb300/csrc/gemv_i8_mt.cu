@@ -181,17 +181,30 @@ gemv_i8_mt_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
             if (threadIdx.x == 0)
                 top_plane = 0;
             __syncthreads();
+            // (loads in batches of kScanBatch per thread, issued before they are used:
+            // one at a time they were a chain of L2 round trips)
             int top = 0;
-            for (int i = threadIdx.x; i < mc * K; i += blockDim.x) {
-                const uint64_t dv = signed_digits(__ldg(reinterpret_cast<const unsigned long long *>(xc) + i));
-                if (dv)
-                    top = max(top, (63 - __clzll((long long)dv)) >> 3);
+            constexpr int kScanBatch = 4;
+            for (int base = threadIdx.x; base < mc * K; base += kScanBatch * blockDim.x) {
+                uint64_t raw[kScanBatch];
+#pragma unroll
+                for (int u = 0; u < kScanBatch; u++) {
+                    const int i = base + u * blockDim.x;
+                    raw[u] = i < mc * K ? __ldg(reinterpret_cast<const unsigned long long *>(xc) + i) : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < kScanBatch; u++) {
+                    const uint64_t dv = signed_digits(raw[u]);   // 0 for x = 0
+                    if (dv)
+                        top = max(top, (63 - __clzll((long long)dv)) >> 3);
+                }
             }
             top = (int)__reduce_max_sync(0xffffffffu, (unsigned)top);
             if (lane == 0)
                 atomicMax(&top_plane, top);
             __syncthreads();
             planes = top_plane + 1;
+#pragma unroll 2
             for (int i = threadIdx.x; i < mc * (K / 4); i += blockDim.x) {
                 const int t = i / (K / 4), c = i - t * (K / 4);
                 const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(xc + (size_t)t * K + 4 * c);
