@@ -187,13 +187,30 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         __syncthreads();
         // V fragments: thread (q, j) of chunk kc holds V rows 2j, 2j+1 (b0) and
         // 2j+8, 2j+9 (b1) of column q
-        for (int idx = tid; idx < ng * 256; idx += blockDim.x) {
-            const int gl = idx >> 8, kc = (idx >> 5) & 7, ln = idx & 31;
+        // (thread tid builds entry (kc, ln) = (tid / 32, tid % 32) of every group of
+        // the chunk; the activation bytes of all groups are loaded first, so that
+        // they are in flight together)
+        static_assert(kWarps * 32 == 256, "one V entry (chunk, lane) per thread and group");
+        {
+            const int kc = tid >> 5, ln = tid & 31;
             const uint32_t q = (uint32_t)(ln >> 2);
-            const uint8_t *xg = xa + (size_t)(c0 + gl) * TG_GROUP + 16 * kc + 2 * (ln & 3);
-            const uint32_t b0 = v_entry(xg[0], q) | (v_entry(xg[1], q) << 16);
-            const uint32_t b1 = v_entry(xg[8], q) | (v_entry(xg[9], q) << 16);
-            vfrag[gl][kc][ln] = make_uint2(b0, b1);
+            uint32_t xb[kChunkGroups][4];
+#pragma unroll
+            for (int gl = 0; gl < kChunkGroups; gl++) {
+                const uint8_t *xg = xa + (size_t)(c0 + min(gl, ng - 1)) * TG_GROUP + 16 * kc + 2 * (ln & 3);
+                xb[gl][0] = xg[0];
+                xb[gl][1] = xg[1];
+                xb[gl][2] = xg[8];
+                xb[gl][3] = xg[9];
+            }
+#pragma unroll
+            for (int gl = 0; gl < kChunkGroups; gl++) {
+                if (gl < ng) {
+                    const uint32_t b0 = v_entry(xb[gl][0], q) | (v_entry(xb[gl][1], q) << 16);
+                    const uint32_t b1 = v_entry(xb[gl][2], q) | (v_entry(xb[gl][3], q) << 16);
+                    vfrag[gl][kc][ln] = make_uint2(b0, b1);
+                }
+            }
         }
         // smallest and largest nonzero activation code of each group
         for (int gl = warp; gl < ng; gl += kWarps) {
