@@ -208,7 +208,7 @@ struct PhaseF {
 __global__ void __launch_bounds__(kWarps * 32)
 lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                      const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
-                     PhaseF F, int N, int G, int tiles, int gpc)
+                     const __grid_constant__ PhaseF F, int N, int G, int tiles, int gpc)
 {
     __shared__ __align__(16) uint2 lists[kChunk][4][kListStride];
     __shared__ WordMeta meta[kChunk][4];
@@ -244,10 +244,20 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
             dn = dc[gq] | (dc[gq + 8] << 8);
         }
         // entry lists: one (group, word) item per warp at a time
-        for (int item = warp; item < 4 * ng; item += kWarps) {
-            const int gl = item >> 2, j = item & 3;
-            const unsigned a = xa[(size_t)(c0 + gl) * TG_GROUP + tgi::lns8_lane_col(j, lane)];
-            build_word(a, lane, lists[gl][j], meta[gl][j]);
+        // (the warp's activation bytes are loaded first, so that they are in flight together)
+        static_assert(4 * kChunk % kWarps == 0, "the same number of items per warp");
+        constexpr int kItems = 4 * kChunk / kWarps;
+        unsigned av[kItems];
+#pragma unroll
+        for (int u = 0; u < kItems; u++) {
+            const int item = min(warp + u * kWarps, 4 * ng - 1);
+            av[u] = xa[(size_t)(c0 + (item >> 2)) * TG_GROUP + tgi::lns8_lane_col(item & 3, lane)];
+        }
+#pragma unroll
+        for (int u = 0; u < kItems; u++) {
+            const int item = warp + u * kWarps;
+            if (item < 4 * ng)
+                build_word(av[u], lane, lists[item >> 2][item & 3], meta[item >> 2][item & 3]);
         }
         __syncthreads();
         for (int gl = 0; gl < ng; gl++) {
@@ -338,6 +348,15 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
             A[(size_t)row * 8 + p] = a;
     }
     if (S) {
+        // S: the products A[p] * F[p], one thread per (row, phase), written over A in
+        // shared memory, then one thread per row adds the eight terms in the order
+        // p = 0..7 (fp64 is slow on this part: eight products per thread serialise)
+        __syncthreads();
+        static_assert(kWarps * 32 % 8 == 0, "a thread's phase p = tid & 7 is the same for all its items");
+        double *prod = reinterpret_cast<double *>(&arow[0][0]);
+        const double fp = F.f[tid & 7];   // F is a grid constant: indexed in place, not copied
+        for (int item = tid; item < rows_here * 8; item += blockDim.x)
+            prod[item] = __dmul_rn((double)arow[item >> 3][item & 7], fp);
         __syncthreads();
         for (int i = tid; i < rows_here; i += blockDim.x) {
             const int row = blockIdx.x * kRows + rank * slice + i;
@@ -345,7 +364,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
                 double sum = 0.0;
 #pragma unroll
                 for (int p = 0; p < 8; p++)
-                    sum = __dadd_rn(sum, __dmul_rn((double)arow[i][p], F.f[p]));
+                    sum = __dadd_rn(sum, prod[i * 8 + p]);
                 S[row] = __dmul_rn(sum, 0x1p-9);
             }
         }
