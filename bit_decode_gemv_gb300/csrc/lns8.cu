@@ -92,11 +92,17 @@ __device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
 // The flagged lanes of chunk KC (raw: its four activation bytes of this quad
 // thread, w: the thread's mask word holding them).
 template <int KC>
-__device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, uint32_t T, uint32_t U, int e,
+__device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, uint32_t TH, uint32_t UL, int e,
                                             int *gcorr, int &clamp)
 {
+    // per byte, on 7-bit codes a (no sum below carries out of its byte):
+    // a > T is bit 7 of a + (127 - T); a < U is bit 7 clear in a + (128 - U);
+    // a != 0 is bit 7 of a + 127
     const uint32_t a4 = raw & 0x7f7f7f7fu;
-    uint32_t m = (__vcmpgtu4(a4, T) | (__vcmpltu4(a4, U) & __vcmpne4(a4, 0u))) & 0x80808080u;
+    const uint32_t hi_f = (a4 + TH) & 0x80808080u;
+    const uint32_t lo_f = ~(a4 + UL) & 0x80808080u;
+    const uint32_t nz_f = (a4 + 0x7f7f7f7fu) & 0x80808080u;
+    uint32_t m = hi_f | (lo_f & nz_f);
     while (m) {
         const int bi = (__ffs((int)m) - 1) >> 3;
         m &= m - 1u;
@@ -117,8 +123,9 @@ __device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, 
 
 __device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg, int *gcorr)
 {
-    const uint32_t T = (uint32_t)min(max(127 - e, 0), 127) * 0x01010101u;   // a > 127 - e saturates
-    const uint32_t U = (uint32_t)min(max(1 - e, 1), 128) * 0x01010101u;     // 0 < a < 1 - e is zero
+    const uint32_t T = (uint32_t)min(max(127 - e, 0), 127);   // a > T = 127 - e saturates
+    const uint32_t U = (uint32_t)min(max(1 - e, 1), 128);     // 0 < a < U = 1 - e is zero
+    const uint32_t TH = (127u - T) * 0x01010101u, UL = (128u - U) * 0x01010101u;
     const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xg);
     // chunk kc: lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1} (byte bi = 2 * rr + h).
     // All sixteen loads are issued first, so that they are in flight together
@@ -128,14 +135,14 @@ __device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, con
     };
     const uint32_t r0 = ld(0), r1 = ld(1), r2 = ld(2), r3 = ld(3), r4 = ld(4), r5 = ld(5), r6 = ld(6), r7 = ld(7);
     int clamp = 0;
-    clamp_chunk<0>(r0, w4[0], half, T, U, e, gcorr, clamp);
-    clamp_chunk<1>(r1, w4[0], half, T, U, e, gcorr, clamp);
-    clamp_chunk<2>(r2, w4[1], half, T, U, e, gcorr, clamp);
-    clamp_chunk<3>(r3, w4[1], half, T, U, e, gcorr, clamp);
-    clamp_chunk<4>(r4, w4[2], half, T, U, e, gcorr, clamp);
-    clamp_chunk<5>(r5, w4[2], half, T, U, e, gcorr, clamp);
-    clamp_chunk<6>(r6, w4[3], half, T, U, e, gcorr, clamp);
-    clamp_chunk<7>(r7, w4[3], half, T, U, e, gcorr, clamp);
+    clamp_chunk<0>(r0, w4[0], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<1>(r1, w4[0], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<2>(r2, w4[1], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<3>(r3, w4[1], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<4>(r4, w4[2], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<5>(r5, w4[2], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<6>(r6, w4[3], half, TH, UL, e, gcorr, clamp);
+    clamp_chunk<7>(r7, w4[3], half, TH, UL, e, gcorr, clamp);
     return clamp;
 }
 
