@@ -652,7 +652,11 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
     static std::mutex mu;
     static encode_fn encode = nullptr;
-    static bool attr_set = false;
+    static uint64_t attr_set = 0;   // bit d: the kernels' shared-memory limit is raised on device d
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TG_ERR_CUDA;
     const int fold = frac > 0 ? kFoldFloor : max_abs_scale <= kNarrowMaxScale ? kFoldNarrow : kFoldWide;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -665,7 +669,8 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
                 return TG_ERR_CUDA;
             encode = reinterpret_cast<encode_fn>(fn);
         }
-        if (!attr_set) {
+        const uint64_t dev_bit = dev < 64 ? 1ull << dev : 0ull;   // (devices past 64: set every call)
+        if (!(attr_set & dev_bit)) {
             void (*kernels[6])(const unsigned char *, const unsigned char *, const CUtensorMap, int64_t *, int, int,
                                int, int, int, int) = {
                 gemv_i8_mma_kernel<false, kFoldNarrow>, gemv_i8_mma_kernel<false, kFoldWide>,
@@ -674,7 +679,7 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
             for (auto k : kernels)
                 if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
                     return TG_ERR_CUDA;
-            attr_set = true;
+            attr_set |= dev_bit;
         }
     }
     // x as a 2D tensor [M rows][K bytes]; boxes of 64 rows x 128 bytes, 128-byte swizzle
@@ -690,10 +695,6 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
     // Tiles per CTA: the fewest that still fit every CTA in one wave (one CTA per SM),
     // so that a shape with fewer than 4 x #SMs tiles spreads over more SMs; a CTA's
     // per-group work shrinks with its tiles, the activation conversion does not.
-    int dev = 0, nsm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return TG_ERR_CUDA;
     int ctiles = 4;
     for (int c = 1; c < 4; c++)
         if ((tiles + c - 1) / c <= nsm) {

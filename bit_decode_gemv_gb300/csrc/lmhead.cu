@@ -774,14 +774,11 @@ cudaError_t launch_scan(bool full, int grid, cudaStream_t st, const int8_t *hi, 
                         const int32_t *s, const uint8_t *m, const int8_t *x, int64_t *logits, Ws ws, int N, int K)
 {
     // The scans use no shared memory; ask for an SM configuration with room for
-    // the rescoring or collecting CTAs that launch beside them.
-    static const cudaError_t carve = [] {
-        cudaError_t e = cudaFuncSetAttribute(lmh_stage1_kernel<CPL>,
-                                             cudaFuncAttributePreferredSharedMemoryCarveout, 25);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(lmh_full_kernel<CPL>, cudaFuncAttributePreferredSharedMemoryCarveout, 25);
-        return e;
-    }();
+    // the rescoring or collecting CTAs that launch beside them (set on every call:
+    // a function attribute belongs to the current device).
+    cudaError_t carve = cudaFuncSetAttribute(lmh_stage1_kernel<CPL>, cudaFuncAttributePreferredSharedMemoryCarveout, 25);
+    if (carve == cudaSuccess)
+        carve = cudaFuncSetAttribute(lmh_full_kernel<CPL>, cudaFuncAttributePreferredSharedMemoryCarveout, 25);
     if (carve != cudaSuccess)
         return carve;
     PdlLaunch l(grid, kScanWarps * 32, 0, st);
