@@ -121,11 +121,22 @@ __device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, 
     }
 }
 
-__device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, const uint8_t *xg, int *gcorr)
+// Both rows of a quad (halves 0 and 1: rows q and q + 8) hold the same 32 lanes,
+// so one call loads their activation bytes once and scans them for each row
+// that needs it (need[h]), with that row's e[h], corrections gcorr[h] and
+// saturation term clamp[h].
+__device__ void clamp_lanes(const uint32_t (&w4)[4], int tq, const int (&e)[2], const bool (&need)[2],
+                            const uint8_t *xg, int *const (&gcorr)[2], int (&clamp)[2])
 {
-    const uint32_t T = (uint32_t)min(max(127 - e, 0), 127);   // a > T = 127 - e saturates
-    const uint32_t U = (uint32_t)min(max(1 - e, 1), 128);     // 0 < a < U = 1 - e is zero
-    const uint32_t TH = (127u - T) * 0x01010101u, UL = (128u - U) * 0x01010101u;
+    uint32_t TH[2], UL[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const uint32_t T = (uint32_t)min(max(127 - e[h], 0), 127);   // a > T = 127 - e saturates
+        const uint32_t U = (uint32_t)min(max(1 - e[h], 1), 128);     // 0 < a < U = 1 - e is zero
+        TH[h] = (127u - T) * 0x01010101u;
+        UL[h] = (128u - U) * 0x01010101u;
+        clamp[h] = 0;
+    }
     const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xg);
     // chunk kc: lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1} (byte bi = 2 * rr + h).
     // All sixteen loads are issued first, so that they are in flight together
@@ -133,17 +144,20 @@ __device__ int clamp_lanes(const uint32_t (&w4)[4], int half, int tq, int e, con
     auto ld = [&](int kc) {
         return (uint32_t)__ldg(x16 + 8 * kc + tq) | ((uint32_t)__ldg(x16 + 8 * kc + 4 + tq) << 16);
     };
-    const uint32_t r0 = ld(0), r1 = ld(1), r2 = ld(2), r3 = ld(3), r4 = ld(4), r5 = ld(5), r6 = ld(6), r7 = ld(7);
-    int clamp = 0;
-    clamp_chunk<0>(r0, w4[0], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<1>(r1, w4[0], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<2>(r2, w4[1], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<3>(r3, w4[1], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<4>(r4, w4[2], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<5>(r5, w4[2], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<6>(r6, w4[3], half, TH, UL, e, gcorr, clamp);
-    clamp_chunk<7>(r7, w4[3], half, TH, UL, e, gcorr, clamp);
-    return clamp;
+    const uint32_t r[8] = {ld(0), ld(1), ld(2), ld(3), ld(4), ld(5), ld(6), ld(7)};
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        if (!need[h])
+            continue;
+        clamp_chunk<0>(r[0], w4[0], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<1>(r[1], w4[0], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<2>(r[2], w4[1], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<3>(r[3], w4[1], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<4>(r[4], w4[2], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<5>(r[5], w4[2], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<6>(r[6], w4[3], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        clamp_chunk<7>(r[7], w4[3], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+    }
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -261,37 +275,43 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 for (int i = 0; i < 4; i++)
                     d[i] += d1[i];
                 const int lo = (int)gmin[gl], hi = (int)gmax[gl];
+                // quad-uniform: the four threads of a quad hold the same two rows.
+                // Rows past N (zero weights, scale code 0) never need the clamp
+                // correction.
+                const int e[2] = {ec[gl][0], ec[gl][1]};
+                bool need[2];
+#pragma unroll
+                for (int half = 0; half < 2; half++)
+                    need[half] = !(lo > 127 || (lo + e[half] >= 1 && hi + e[half] <= 127) ||
+                                   rb * 16 + gq + 8 * half >= N);
+                int clamp[2] = {0, 0};
+                if (need[0] || need[1]) {
+                    int *const gc[2] = {gcorr[warp][gq], gcorr[warp][gq + 8]};
+                    const unsigned qmask = 0xfu << (lane & ~3);
+                    clamp_lanes(w4, tq, e, need, xa + (size_t)(c0 + gl) * TG_GROUP, gc, clamp);
+                    __syncwarp(qmask);
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {   // this thread's two classes of each row
+                        d[2 * half] += (float)gc[half][2 * tq];
+                        d[2 * half + 1] += (float)gc[half][2 * tq + 1];
+                        gc[half][2 * tq] = 0;
+                        gc[half][2 * tq + 1] = 0;
+                        clamp[half] += __shfl_xor_sync(qmask, clamp[half], 1);
+                        clamp[half] += __shfl_xor_sync(qmask, clamp[half], 2);
+                    }
+                }
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
-                    const int e = ec[gl][half];
                     int *acc_row = acc[warp * 16 + gq + 8 * half];
-                    // quad-uniform: the four threads of a quad hold the same row.
-                    // Rows past N (zero weights, scale code 0) never need the
-                    // clamp correction.
-                    const bool clamp_free = lo > 127 || (lo + e >= 1 && hi + e <= 127) ||
-                                            rb * 16 + gq + 8 * half >= N;
-                    int clamp = 0;
-                    if (!clamp_free) {
-                        int *gc = gcorr[warp][gq + 8 * half];
-                        const unsigned qmask = 0xfu << (lane & ~3);
-                        clamp = clamp_lanes(w4, half, tq, e, xa + (size_t)(c0 + gl) * TG_GROUP, gc);
-                        __syncwarp(qmask);
-                        d[2 * half] += (float)gc[2 * tq];
-                        d[2 * half + 1] += (float)gc[2 * tq + 1];
-                        gc[2 * tq] = 0;
-                        gc[2 * tq + 1] = 0;
-                        clamp += __shfl_xor_sync(qmask, clamp, 1);
-                        clamp += __shfl_xor_sync(qmask, clamp, 2);
-                    }
 #pragma unroll
                     for (int j = 0; j < 2; j++) {
                         const int q = 2 * tq + j;
                         const int v = __float2int_rn(d[2 * half + j]);
-                        const int sidx = q + (e & 7);
-                        const int sh = max(-31, min(31, (e >> 3) + (sidx >> 3)));
+                        const int sidx = q + (e[half] & 7);
+                        const int sh = max(-31, min(31, (e[half] >> 3) + (sidx >> 3)));
                         int add = sh >= 0 ? (v << sh) : (v >> -sh);
                         if ((sidx & 7) == 7)
-                            add += clamp;
+                            add += clamp[half];
                         acc_row[sidx & 7] += add;
                     }
                 }
