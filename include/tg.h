@@ -37,6 +37,13 @@
  *     cudaStream_t passed as void* (NULL = the legacy default stream); they
  *     only enqueue work on that stream and return at once. The library
  *     allocates no memory; the lm_head takes a caller-owned device workspace.
+ *   - Stream order holds as usual: a call's kernels start after the work
+ *     enqueued before it has finished (or, for kernels launched as
+ *     programmatic dependents, wait for it before touching x, y or the
+ *     workspace). Some of the library's kernels let the next kernel on the
+ *     stream launch early; a caller's kernel launched with programmatic stream
+ *     serialisation right after a call must wait (griddepcontrol.wait /
+ *     cudaGridDependencySynchronize) before it reads that call's outputs.
  *   - Arguments are validated on the host before anything is enqueued; on an
  *     argument error no output buffer is touched.
  *   - The library keeps no state between calls, apart from one device error
