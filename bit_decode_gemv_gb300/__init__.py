@@ -118,11 +118,14 @@ def _ptr(t):
     """Device (or host) address of a torch tensor, an int, or None."""
     if t is None:
         return None
-    if isinstance(t, int):
+    if type(t) is int:
         return t
-    if hasattr(t, "data_ptr"):
-        return t.data_ptr()
-    raise TypeError(f"expected a tensor or an address, got {type(t).__name__}")
+    try:
+        return t.data_ptr()   # (the common case first: this runs once per argument of every call)
+    except AttributeError:
+        if isinstance(t, int):
+            return int(t)
+        raise TypeError(f"expected a tensor or an address, got {type(t).__name__}") from None
 
 
 def _stream(stream):
