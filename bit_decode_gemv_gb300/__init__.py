@@ -184,9 +184,30 @@ def tg_pack_weights(kind: int, trits: np.ndarray, scales: np.ndarray):
     return out, L
 
 
+_FAST_UNSET = object()
+_fast_mod = _FAST_UNSET
+
+
+def _fast():
+    """The compiled call path to tg_gemv_i8 (csrc/tgpy.c), or None if it was not built."""
+    global _fast_mod
+    if _fast_mod is _FAST_UNSET:
+        lib()   # the same libtg.so, loaded first
+        try:
+            from . import _tgpy
+            _fast_mod = _tgpy
+        except ImportError:
+            _fast_mod = None
+    return _fast_mod
+
+
 def tg_gemv_i8(layout: tg_layout, w, x, M: int, y, stream=None) -> None:
-    _check(lib().tg_gemv_i8(C.byref(layout), _ptr(w), _ptr(x), int(M), _ptr(y), _stream(stream)),
-           "tg_gemv_i8")
+    f = _fast_mod if _fast_mod is not _FAST_UNSET else _fast()
+    if f is not None:
+        st = f.gemv_i8(C.addressof(layout), _ptr(w) or 0, _ptr(x) or 0, int(M), _ptr(y) or 0, _stream(stream) or 0)
+    else:
+        st = lib().tg_gemv_i8(C.byref(layout), _ptr(w), _ptr(x), int(M), _ptr(y), _stream(stream))
+    _check(st, "tg_gemv_i8")
 
 
 def tg_gemv_lns8_phase(layout: tg_layout, w, xa, A, S=None, stream=None) -> None:

@@ -46,7 +46,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > t for p in sources() + headers() + [__file__])
+    return any(os.path.getmtime(p) > t for p in sources() + headers() + [__file__, os.path.join(CSRC, "tgpy.c")])
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
@@ -77,7 +77,30 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("link failed")
     os.replace(tmp, LIB)
+    _build_tgpy()
     return LIB
+
+
+def _build_tgpy() -> None:
+    """The optional CPython call path to tg_gemv_i8 (csrc/tgpy.c), linked against the
+    in-tree libtg.so; skipped with a note if there is no C compiler or no Python headers
+    (the binding then calls through ctypes)."""
+    import sysconfig
+    src = os.path.join(CSRC, "tgpy.c")
+    out = os.path.join(PKG, "_tgpy" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+    inc = sysconfig.get_paths().get("include", "")
+    cc = os.environ.get("CC") or shutil.which("gcc") or shutil.which("cc")
+    if not cc or not os.path.exists(os.path.join(inc, "Python.h")):
+        sys.stderr.write("note: _tgpy not built (no C compiler or Python headers); the binding uses ctypes\n")
+        return
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-shared", "-fPIC", "-I", inc, "-I", INCLUDE, src, "-o", tmp, "-L", PKG, "-l:libtg.so",
+           "-Wl,-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode:
+        sys.stderr.write("note: _tgpy not built; the binding uses ctypes\n" + " ".join(cmd) + "\n" + r.stderr[-2000:])
+        return
+    os.replace(tmp, out)
 
 
 if __name__ == "__main__":

@@ -315,3 +315,22 @@ def test_int64_activations_k_limit():
     _, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, np.zeros((1, K), np.int8), np.ones((1, K // 128), np.int32))
     L.flags |= tg.TG_FLAG_X_INT64
     assert status_of(tg.tg_gemv_i8, L, A256, A256, 1, A256, 0) == tg.TG_ERR_SHAPE
+
+
+def test_compiled_and_ctypes_call_paths_agree():
+    """tg_gemv_i8 has two marshalling paths (the compiled module when it was built,
+    ctypes otherwise): both must pass the same arguments to the library, so every
+    argument error comes back with the same status."""
+    import ctypes as C
+    f = tg._fast()
+    if f is None:
+        pytest.skip("the compiled call path was not built")
+    w = W.tiny(seed=3, N=64, K=256)
+    blob, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
+    lib = tg.lib()
+    cases = [(0, 0, 0, 1, 0, 0), (C.addressof(L), 0, 0, 1, 0, 0), (C.addressof(L), 256, 16, 0, 8, 0),
+             (C.addressof(L), 256, 16, tg.TG_MAX_M + 1, 8, 0), (C.addressof(L), 257, 16, 1, 8, 0),
+             (C.addressof(L), 256, 15, 1, 8, 0)]
+    for args in cases:
+        lp = C.cast(args[0], C.POINTER(tg.tg_layout)) if args[0] else None
+        assert f.gemv_i8(*args) == lib.tg_gemv_i8(lp, *args[1:]), args
