@@ -669,7 +669,7 @@ int oracle_lns8_materialise(int64_t N, const int64_t *A, const double *F, double
 /*
  * The same materialisation in long double with F from exp2l, rounded to double
  * at the end: a higher-precision reference for S. S_abs receives
- * 2^-9 * sum_p |A[p]| * F[p], the scale against which rounding error is judged.
+ * 2^-9 * sum_p |A[p]| * F[p], the scale against which rounding error is measured.
  */
 int oracle_lns8_materialise_hi(int64_t N, const int64_t *A, double *S_hi, double *S_abs)
 {

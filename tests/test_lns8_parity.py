@@ -5,7 +5,7 @@ the direct per-lane route and the state-population route
 A[r][p] must be bit-exact. S is compared within 1e-12 relative error, the
 tolerance for the fp64 materialisation; the denominator is max(|S|, 2^-40 *
 2^-9 sum_p |A[p]| F[p]) so that rows whose eight terms cancel to near zero
-are judged against the size of the terms, not of the near-zero result.
+are measured against the size of the terms, not of the near-zero result.
 """
 
 import numpy as np
