@@ -22,7 +22,11 @@
 // reads its row's four 16-byte LNS8 entries for the group, compacts them into
 // W_nonzero / W_negative words (the byte-permute conversion of the state-set
 // route), walks the set bits into a 128-bin population histogram in shared
-// memory, and folds each phase's sixteen band slots. The group tree is a
+// memory, and folds each phase's sixteen band slots, clearing each bin as it
+// reads it. The histograms are stored bin-major ([bin][thread]), so the lanes
+// of a warp reading the same bin touch consecutive halfwords, and the staged
+// activation groups are 132 bytes apart, so lanes of different groups reading
+// the same column fall in different banks. The group tree is a
 // shuffle tree (lane i combines with lane i + 2^l, left operand first), and
 // lane 0 reduces the eight phases. The tables are computed on the host from
 // the definitions above and passed as a kernel parameter (23 KB at F = 6).
@@ -33,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <mutex>
 
@@ -43,18 +48,22 @@
 namespace {
 
 constexpr int kWarps = 8;             // rows per CTA (one warp each)
+constexpr int kThreads = kWarps * 32;
+constexpr int kXStride = 132;         // bytes between staged activation groups (33 words)
 constexpr int kMaxF = 6;
 constexpr int kLenMax = (8 * kMaxF + 40) << kMaxF;   // table length at F = 6
 constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int kLog8 = 136;   // LOG8 entries stored ([0..128] used; 136 keeps what follows 16-byte aligned)
 
-struct LnsTables {
+// 16-byte aligned so that the kernel can copy it to shared memory in 16-byte loads
+struct alignas(16) LnsTables {
     int16_t log8[kLog8];
     int16_t kp[kLenMax];
     int16_t km[kLenMax];
 };
 static_assert(sizeof(LnsTables) < 30 * 1024, "kernel parameter space");
+static_assert(offsetof(LnsTables, kp) % 16 == 0 && offsetof(LnsTables, km) % 16 == 0, "16-byte table rows");
 
 struct Lv {
     int s;     // -1, 0, +1
@@ -86,13 +95,12 @@ __device__ __forceinline__ Lv shfl_down(Lv v, int d)
 }
 
 // The eight phase aggregates of one (row, group): population histogram, count
-// fold, a balanced tree over the sixteen band slots of each phase.
+// fold, a balanced tree over the sixteen band slots of each phase. bins is the
+// thread's histogram column (bin k at bins[k * kThreads]); it is all zero on
+// entry and is left all zero.
 __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, short *bins,
                              const int16_t *log8, const int16_t *kp, const int16_t *km, int len, int F, Lv (&ph)[8])
 {
-#pragma unroll
-    for (int k = 0; k < 16; k++)
-        reinterpret_cast<uint4 *>(bins)[k] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         uint32_t nz0, ng0, nz1, ng1;
@@ -108,7 +116,7 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
             if (code == 0 || k <= 0)
                 continue;
             k = min(k, 127);
-            bins[k] += (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
+            bins[k * kThreads] += (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
         }
     }
 #pragma unroll 1
@@ -116,7 +124,9 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
         Lv v[16];
 #pragma unroll
         for (int b = 0; b < 16; b++) {
-            const int c = bins[8 * b + p];
+            short *slot = bins + (8 * b + p) * kThreads;
+            const int c = *slot;
+            *slot = 0;
             v[b] = c == 0 ? Lv{0, 0} : Lv{c > 0 ? 1 : -1, ((8 * b + p) << F) + log8[c > 0 ? c : -c]};
         }
 #pragma unroll
@@ -134,28 +144,47 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
                     int Gp, int F, int len, const __grid_constant__ LnsTables T)
 {
     extern __shared__ __align__(16) unsigned char smem[];
+    // only the len entries of each table that F uses are held (len is a
+    // multiple of 8, so every region starts on a 16-byte boundary)
     int16_t *log8 = reinterpret_cast<int16_t *>(smem);                  // [kLog8]
-    int16_t *kp = log8 + kLog8;                                         // [kLenMax]
-    int16_t *km = kp + kLenMax;                                         // [kLenMax]
-    short *bins_all = reinterpret_cast<short *>(km + kLenMax);          // [kWarps * 32][128]
-    uint8_t *xs = reinterpret_cast<uint8_t *>(bins_all + kWarps * 32 * 128);   // [G * 128], 16-byte aligned
-    static_assert(((kLog8 + 2 * kLenMax) * 2 + kWarps * 32 * 128 * 2) % 16 == 0, "xs alignment");
+    int16_t *kp = log8 + kLog8;                                         // [len]
+    int16_t *km = kp + len;                                             // [len]
+    short *bins_all = reinterpret_cast<short *>(km + len);              // [128][kThreads]
+    uint8_t *xs = reinterpret_cast<uint8_t *>(bins_all + 128 * kThreads);   // [G][kXStride]
+    static_assert((kLog8 * 2) % 16 == 0, "table alignment");
 
-    for (int i = threadIdx.x; i < kLog8; i += blockDim.x)
-        log8[i] = T.log8[i];
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-        kp[i] = T.kp[i];
-        km[i] = T.km[i];
+    if ((reinterpret_cast<uintptr_t>(&T) & 15u) == 0) {
+        // 16-byte copies: each distinct parameter address a warp reads is a
+        // separate constant-cache access, so wide loads take 8x fewer
+        const uint4 *src = reinterpret_cast<const uint4 *>(&T);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem);
+        constexpr int kLogV = kLog8 / 8, kTabV = kLenMax / 8;
+        const int lv = len / 8;
+        for (int i = threadIdx.x; i < kLogV + 2 * lv; i += blockDim.x) {
+            const int t = i < kLogV ? 0 : 1 + (i - kLogV) / lv;   // 0 log8, 1 kp, 2 km
+            const int o = i < kLogV ? i : (i - kLogV) - (t - 1) * lv;
+            dst[i] = src[t == 0 ? o : kLogV + (t - 1) * kTabV + o];
+        }
+    } else {
+        for (int i = threadIdx.x; i < kLog8; i += blockDim.x)
+            log8[i] = T.log8[i];
+        for (int i = threadIdx.x; i < len; i += blockDim.x) {
+            kp[i] = T.kp[i];
+            km[i] = T.km[i];
+        }
     }
-    for (int i = threadIdx.x; i < G * 128 / 16; i += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(xa) + i);
+    for (int i = threadIdx.x; i < 128 * kThreads / 8; i += blockDim.x)
+        reinterpret_cast<uint4 *>(bins_all)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < G * 32; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(xs)[(i >> 5) * (kXStride / 4) + (i & 31)] =
+            __ldg(reinterpret_cast<const uint32_t *>(xa) + i);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kWarps + warp;
     if (row >= N)
         return;
-    short *bins = bins_all + (size_t)threadIdx.x * 128;
+    short *bins = bins_all + threadIdx.x;
     const int blk = row >> 4, q = row & 7, half = (row >> 3) & 1;
     const int gpl = Gp > 32 ? Gp / 32 : 1;   // groups per lane
 
@@ -173,7 +202,7 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
             if (g < G) {
                 const uint4 *ent = masks + ((size_t)blk * G + g) * 32 + 4 * q;
                 const int e = (int)codes[((size_t)blk * G + g) * 16 + (row & 15)] - 74;
-                group_phases(ent, half, xs + (size_t)g * 128, e, bins, log8, kp, km, len, F, cur);
+                group_phases(ent, half, xs + (size_t)g * kXStride, e, bins, log8, kp, km, len, F, cur);
             } else {
 #pragma unroll
                 for (int p = 0; p < 8; p++)
@@ -259,13 +288,13 @@ int lns8_purelns(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, in
         Gp *= 2;
     if (Gp > 32 * 128)   // a lane's run of groups is at most 128 (the run's eight tree levels)
         return TG_ERR_SHAPE;
-    const size_t smem = (kLog8 + 2 * (size_t)kLenMax) * 2 + (size_t)kWarps * 32 * 128 * 2 + (size_t)G * 128;
+    const size_t smem = (kLog8 + 2 * (size_t)lens[F]) * 2 + (size_t)128 * kThreads * 2 + (size_t)G * kXStride;
     if (smem > 227 * 1024)
         return TG_ERR_SHAPE;
     cudaError_t e = cudaFuncSetAttribute(lns8_purelns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return TG_ERR_CUDA;
-    lns8_purelns_kernel<<<(N + kWarps - 1) / kWarps, kWarps * 32, smem, s>>>(masks, codes, xa, A, S, N, G, Gp, F,
+    lns8_purelns_kernel<<<(N + kWarps - 1) / kWarps, kThreads, smem, s>>>(masks, codes, xa, A, S, N, G, Gp, F,
                                                                               lens[F], tables[F]);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
