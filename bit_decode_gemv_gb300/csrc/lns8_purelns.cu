@@ -101,10 +101,14 @@ __device__ __forceinline__ Lv shfl_down(Lv v, int d)
 __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, short *bins,
                              const int16_t *log8, const int16_t *kp, const int16_t *km, int len, int F, Lv (&ph)[8])
 {
+    uint4 ev[4];   // the four entries' loads issued together
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+        ev[j] = tgi::ldg_stream(ent + j);
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         uint32_t nz0, ng0, nz1, ng1;
-        tgi::lns8_compact_words(tgi::ldg_stream(ent + j), nz0, ng0, nz1, ng1);
+        tgi::lns8_compact_words(ev[j], nz0, ng0, nz1, ng1);
         uint32_t nz = half ? nz1 : nz0;
         const uint32_t ng = half ? ng1 : ng0;
         while (nz) {
@@ -119,7 +123,7 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
             bins[k * kThreads] += (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
         }
     }
-#pragma unroll 1
+#pragma unroll 2
     for (int p = 0; p < 8; p++) {
         Lv v[16];
 #pragma unroll
@@ -138,7 +142,7 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
     }
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads, 3)
 lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                     const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S, int N, int G,
                     int Gp, int F, int len, const __grid_constant__ LnsTables T)
