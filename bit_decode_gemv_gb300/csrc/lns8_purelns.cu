@@ -23,8 +23,12 @@
 // W_nonzero / W_negative words (the byte-permute conversion of the state-set
 // route), walks the set bits into a 128-bin population histogram in shared
 // memory, and folds each phase's sixteen band slots, clearing each bin as it
-// reads it. The histograms are stored bin-major ([bin][thread]), so the lanes
-// of a warp reading the same bin touch consecutive halfwords, and the staged
+// reads it. The histograms are stored bin-major ([bin][thread], rows of 260
+// bytes), so the lanes of a warp reading the same bin touch consecutive bytes
+// and lanes sharing a word that update different bins fall in different banks.
+// Bins are 8-bit: a count lies in [-128, 128], and its two ends wrap to the same
+// byte only when all 128 lanes of the group fell into that one bin, in which
+// case the group's total of signs is that bin's count. The staged
 // activation groups are 132 bytes apart, so lanes of different groups reading
 // the same column fall in different banks. The group tree is a
 // shuffle tree (lane i combines with lane i + 2^l, left operand first), and
@@ -49,6 +53,7 @@ namespace {
 
 constexpr int kWarps = 8;             // rows per CTA (one warp each)
 constexpr int kThreads = kWarps * 32;
+constexpr int kBinStride = 260;       // bytes per histogram bin row (kThreads + a 4-byte bank skew)
 constexpr int kXStride = 132;         // bytes between staged activation groups (33 words)
 constexpr int kMaxF = 6;
 constexpr int kLenMax = (8 * kMaxF + 40) << kMaxF;   // table length at F = 6
@@ -96,12 +101,13 @@ __device__ __forceinline__ Lv shfl_down(Lv v, int d)
 
 // The eight phase aggregates of one (row, group): population histogram, count
 // fold, a balanced tree over the sixteen band slots of each phase. bins is the
-// thread's histogram column (bin k at bins[k * kThreads]); it is all zero on
-// entry and is left all zero.
-__device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, short *bins,
+// thread's histogram column (bin k at bins[k * kBinStride], a count modulo 256);
+// it is all zero on entry and is left all zero.
+__device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint8_t *xg, int e, int8_t *bins,
                              const int16_t *log8, const int16_t *kp, const int16_t *km, int len, int F, Lv (&ph)[8])
 {
     uint4 ev[4];   // the four entries' loads issued together
+    int tot = 0;   // the group's total of signs
 #pragma unroll
     for (int j = 0; j < 4; j++)
         ev[j] = tgi::ldg_stream(ent + j);
@@ -120,7 +126,9 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
             if (code == 0 || k <= 0)
                 continue;
             k = min(k, 127);
-            bins[k * kThreads] += (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
+            const int d = (((ng >> b) & 1u) ^ (a >> 7)) ? -1 : 1;
+            bins[k * kBinStride] = (int8_t)(bins[k * kBinStride] + d);
+            tot += d;
         }
     }
 #pragma unroll 2
@@ -128,9 +136,10 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
         Lv v[16];
 #pragma unroll
         for (int b = 0; b < 16; b++) {
-            short *slot = bins + (8 * b + p) * kThreads;
-            const int c = *slot;
+            int8_t *slot = bins + (8 * b + p) * kBinStride;
+            const int c8 = *slot;
             *slot = 0;
+            const int c = c8 == -128 ? tot : c8;   // +-128: every lane in this bin
             v[b] = c == 0 ? Lv{0, 0} : Lv{c > 0 ? 1 : -1, ((8 * b + p) << F) + log8[c > 0 ? c : -c]};
         }
 #pragma unroll
@@ -142,7 +151,7 @@ __device__ void group_phases(const uint4 *__restrict__ ent, int half, const uint
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
 lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                     const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S, int N, int G,
                     int Gp, int F, int len, const __grid_constant__ LnsTables T)
@@ -153,8 +162,9 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
     int16_t *log8 = reinterpret_cast<int16_t *>(smem);                  // [kLog8]
     int16_t *kp = log8 + kLog8;                                         // [len]
     int16_t *km = kp + len;                                             // [len]
-    short *bins_all = reinterpret_cast<short *>(km + len);              // [128][kThreads]
-    uint8_t *xs = reinterpret_cast<uint8_t *>(bins_all + 128 * kThreads);   // [G][kXStride]
+    int8_t *bins_all = reinterpret_cast<int8_t *>(km + len);            // [128][kBinStride]
+    uint8_t *xs = reinterpret_cast<uint8_t *>(bins_all + 128 * kBinStride);   // [G][kXStride]
+    static_assert((128 * kBinStride) % 16 == 0, "staged activation alignment");
     static_assert((kLog8 * 2) % 16 == 0, "table alignment");
 
     if ((reinterpret_cast<uintptr_t>(&T) & 15u) == 0) {
@@ -177,7 +187,7 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
             km[i] = T.km[i];
         }
     }
-    for (int i = threadIdx.x; i < 128 * kThreads / 8; i += blockDim.x)
+    for (int i = threadIdx.x; i < 128 * kBinStride / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(bins_all)[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < G * 32; i += blockDim.x)
         reinterpret_cast<uint32_t *>(xs)[(i >> 5) * (kXStride / 4) + (i & 31)] =
@@ -188,7 +198,7 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
     const int row = blockIdx.x * kWarps + warp;
     if (row >= N)
         return;
-    short *bins = bins_all + threadIdx.x;
+    int8_t *bins = bins_all + threadIdx.x;
     const int blk = row >> 4, q = row & 7, half = (row >> 3) & 1;
     const int gpl = Gp > 32 ? Gp / 32 : 1;   // groups per lane
 
@@ -292,7 +302,7 @@ int lns8_purelns(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, in
         Gp *= 2;
     if (Gp > 32 * 128)   // a lane's run of groups is at most 128 (the run's eight tree levels)
         return TG_ERR_SHAPE;
-    const size_t smem = (kLog8 + 2 * (size_t)lens[F]) * 2 + (size_t)128 * kThreads * 2 + (size_t)G * kXStride;
+    const size_t smem = (kLog8 + 2 * (size_t)lens[F]) * 2 + (size_t)128 * kBinStride + (size_t)G * kXStride;
     if (smem > 227 * 1024)
         return TG_ERR_SHAPE;
     cudaError_t e = cudaFuncSetAttribute(lns8_purelns_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

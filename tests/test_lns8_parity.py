@@ -180,6 +180,23 @@ def test_purelns_state_cardinality(n_states, F):
     check_pure(w, F)
 
 
+@pytest.mark.parametrize("F", [1, 4])
+def test_purelns_full_bins(F):
+    """Groups whose 128 lanes all fall into one product-code bin with one sign
+    (population counts +128 and -128, the two ends of the count range), rows
+    one lane short of that (127), and rows where every lane clamps into the
+    top code."""
+    N, K = 24, 512
+    t = np.ones((N, K), np.int8)
+    t[1::4] = -1                         # every lane negative
+    t[2::4, ::128] = 0                   # one lane of each group zero
+    xa = np.full(K, 74, np.uint8)        # one code, positive ...
+    xa[256:] |= 0x80                     # ... and negative in groups 2 and 3
+    dcode = np.full((N, K // 128), 74, np.uint8)
+    dcode[3::4] = 200                    # 74 + 200 - 74 > 127: clamped
+    check_pure(dict(t=t, dcode=dcode, xa=xa), F)
+
+
 def test_purelns_zero_rows_and_without_S():
     w = W.lns8(seed=6, N=70, K=512)
     w["t"][::3] = 0
