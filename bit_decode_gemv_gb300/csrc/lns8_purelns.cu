@@ -207,7 +207,14 @@ lns8_purelns_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__
 #pragma unroll
     for (int p = 0; p < 8; p++)
         ph[p] = Lv{0, 0};
-    if (lane * gpl < Gp) {
+    if (gpl == 1) {
+        // one group per lane: its phase aggregates are the lane's run
+        if (lane < G) {
+            const uint4 *ent = masks + ((size_t)blk * G + lane) * 32 + 4 * q;
+            const int e = (int)codes[((size_t)blk * G + lane) * 16 + (row & 15)] - 74;
+            group_phases(ent, half, xs + (size_t)lane * kXStride, e, bins, log8, kp, km, len, F, ph);
+        }
+    } else if (lane * gpl < Gp) {
         Lv run[8][8];   // [phase][level] partial trees of the run (gpl <= 2^7 groups)
         int filled = 0;
         for (int i = 0; i < gpl; i++) {
