@@ -67,7 +67,8 @@ class tg_layout(C.Structure):
         ("total_bytes", C.c_int64), ("max_abs_scale", C.c_int64),
         ("flags", C.c_int64),
         ("frac", C.c_int64),
-        ("reserved", C.c_int64 * 2),
+        ("wait_limit", C.c_int64),
+        ("reserved", C.c_int64 * 1),
     ]
 
 
@@ -96,7 +97,7 @@ def lib():
         L.tg_packed_bytes.restype = sz
         L.tg_pack_weights.argtypes = [C.c_int, i64, i64, p, p, p, sz, lp]
         L.tg_gemv_i8.argtypes = [lp, p, p, i64, p, p]
-        L.tg_gemv_lns8_phase.argtypes = [lp, p, p, p, p, p]
+        L.tg_gemv_lns8_phase.argtypes = [lp, p, p, p, p, p, p]
         L.tg_lmhead_workspace_bytes.argtypes = [lp, i32]
         L.tg_lmhead_workspace_bytes.restype = sz
         L.tg_lmhead_argmax_topk.argtypes = [lp, p, p, i32, p, p, p, p, p, p, sz, p]
@@ -210,8 +211,10 @@ def tg_gemv_i8(layout: tg_layout, w, x, M: int, y, stream=None) -> None:
     _check(st, "tg_gemv_i8")
 
 
-def tg_gemv_lns8_phase(layout: tg_layout, w, xa, A, S=None, stream=None) -> None:
-    _check(lib().tg_gemv_lns8_phase(C.byref(layout), _ptr(w), _ptr(xa), _ptr(A), _ptr(S),
+def tg_gemv_lns8_phase(layout: tg_layout, w, xa, A, S=None, stream=None, F=None) -> None:
+    """F: device fp64 [8] phase constants, or None for the built-in 2^((p-2)/8)
+    (the C argument between xa and A)."""
+    _check(lib().tg_gemv_lns8_phase(C.byref(layout), _ptr(w), _ptr(xa), _ptr(F), _ptr(A), _ptr(S),
                                     _stream(stream)), "tg_gemv_lns8_phase")
 
 

@@ -258,7 +258,7 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         return TG_ERR_ARG;
     if ((L->kind != TG_TERNARY_I8 && L->kind != TG_BINARY_Q1) || L->version != 1)
         return TG_ERR_ARG;
-    if (L->frac < 0 || L->frac > 62)
+    if (L->frac < 0 || L->frac > 62 || L->wait_limit < 0)
         return TG_ERR_ARG;
     if (!tgi::aligned(w, 256) || !tgi::aligned(x, 16) || !tgi::aligned(y, 8))
         return TG_ERR_ARG;
@@ -314,7 +314,7 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
                                  (int)L->frac, pdl, s);
     } else {
         return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale,
-                                L->kind == TG_BINARY_Q1, (int)L->frac, s);
+                                L->kind == TG_BINARY_Q1, (int)L->frac, L->wait_limit, s);
     }
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

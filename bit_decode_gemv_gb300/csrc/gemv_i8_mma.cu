@@ -58,6 +58,12 @@ TGI_DEFINE_DEVICE_ERROR(gemv_mma_take_device_error)
 
 namespace {
 
+using tgi::bulk_copy;
+using tgi::mbar_arrive;
+using tgi::mbar_expect_tx;
+using tgi::mbar_init;
+using tgi::smem_u32;
+
 constexpr int kComputeWarps = 16;   // 4 row quarters x 4 parts (32 weights and 16 tokens each)
 constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd pairs)
 constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
@@ -96,11 +102,6 @@ constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffSlot + 16 + 1024;   // + slack to align the base to 1024 bytes
 static_assert(kStageBytes % 1024 == 0 && kOffStages % 1024 == 0 && kStageX % 1024 == 0 && kStageXBytes % 1024 == 0,
               "bulk copies need 16-byte and the swizzled activation boxes 1024-byte alignment");
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // Shared-memory matrix descriptor, K-major without swizzle: core matrices of
 // 8 rows x 16 bytes stored as 128 contiguous bytes, K-adjacent core matrices
@@ -186,24 +187,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[16])
 }
 
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Bulk (TMA) copy global -> shared, completing `bytes` on the mbarrier.
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // 2D tensor (TMA) copy of the box at (x0, y0) of the tensor map into shared
 // memory, completing its bytes on the mbarrier.
 __device__ __forceinline__ void tensor_copy_2d(uint32_t dst, const CUtensorMap *map, int x0, int y0, uint32_t bar)
@@ -214,10 +197,14 @@ __device__ __forceinline__ void tensor_copy_2d(uint32_t dst, const CUtensorMap *
         : "memory");
 }
 
+// Default bound of every wait in this kernel: 2^32 SM clock cycles (about two
+// seconds at the part's clocks). The layout's wait_limit overrides it.
+constexpr long long kDefaultWaitCycles = 1ll << 32;
+
 // Wait for phase `parity` of an mbarrier: one non-blocking test, then
-// suspending waits. Gives up (returns false) after about two seconds of SM
-// clock, or once *abort is set.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort)
+// suspending waits. Gives up (returns false) after `limit` SM clock cycles, or
+// once *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, long long limit)
 {
     uint32_t done;
     asm volatile(
@@ -238,8 +225,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             : "memory");
         if (done)
             return true;
-        if (*abort || clock64() - start > (4ll << 30))
+        if (*abort || clock64() - start > limit)
             return false;
+    }
+}
+
+// Wait, before the CTA frees its tensor memory and exits, for an asynchronous
+// operation this CTA started (bulk and tensor copies into its shared memory,
+// MMAs committed to an mbarrier) to signal phase `parity` of `bar`. Such an
+// operation always ends, so this wait ignores the abort flag and the caller's
+// limit; it is still bounded (the default limit) and sets the error word if it
+// runs out.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity)
+{
+    const long long start = clock64();
+    while (!tgi::mbar_test(bar, parity)) {
+        if (clock64() - start > kDefaultWaitCycles) {
+            atomicExch(&tgi_device_error_word, 1);
+            return;
+        }
     }
 }
 
@@ -274,11 +278,6 @@ __device__ __forceinline__ uint64_t mad_wide(uint32_t a, int32_t b, uint64_t acc
     uint64_t r;
     asm("mad.wide.s32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(acc));
     return r;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Expand one mask word (16 weights, lanes 16u + 4j + b in bits 8b + 2j, 8b + 2j + 1)
@@ -326,7 +325,7 @@ template <bool kQ1, int kFold>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char *__restrict__ scales,
                    const __grid_constant__ CUtensorMap xmap, int64_t *__restrict__ y, int N, int G, int tiles,
-                   int M, int frac, int ctiles)
+                   int M, int frac, int ctiles, long long wait_limit)
 {
     constexpr bool kNarrow = kFold == kFoldNarrow;
     constexpr uint32_t kMaskBytes = kQ1 ? 512u : 1024u;   // mask bytes of one (tile, group)
@@ -377,7 +376,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
 
     // A bounded wait; once any thread has given up, the others stop waiting too.
     auto wait = [&](int i, uint32_t parity) {
-        if (!mbar_wait(bar(i), parity, &abort_flag) && !abort_flag) {
+        if (!mbar_wait(bar(i), parity, &abort_flag, wait_limit) && !abort_flag) {
             atomicExch(&tgi_device_error_word, 1);
             abort_flag = 1;
         }
@@ -406,7 +405,8 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             }
             __syncwarp();
         };
-        for (int P = 0; P < min(npairs, kStages); P++)
+        int issued = 0;   // pairs whose copies are in flight or landed: 0 .. issued - 1
+        for (int P = 0; P < min(npairs, kStages); P++, issued++)
             copy_inputs(P);
         for (int P = 0; P + kStages < npairs; P++) {
             // every compute warp has read stage P % kStages
@@ -416,12 +416,20 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             if (__shfl_sync(0xffffffffu, abort_flag, 0))
                 break;
             copy_inputs(P + kStages);
+            issued++;
         }
+        // every copy this warp started has landed before the CTA exits (after a
+        // give-up, some stages were never read): the last filling of each stage
+        if (lane == 0)
+            for (int P = max(issued - kStages, 0); P < issued; P++)
+                mbar_drain(bar(kBarMFull + P % kStages), (uint32_t)(P / kStages) & 1u);
+        __syncwarp();
     } else if (warp >= kComputeWarps) {
         // ---------------- MMA warp w: pairs P = w mod 2, A/B slot and D buffer w ----------------
         const uint32_t idesc = instr_desc(nmma);
         const int w = warp - kComputeWarps;
         if (lane == 0) {
+            int last = -1;   // the last pair whose MMAs this warp committed
             for (int P = w; P < npairs && !abort_flag; P += kMmaWarps) {
                 const uint32_t par = (uint32_t)(P / kMmaWarps) & 1u;
                 wait(kBarABFull + w, par);
@@ -440,7 +448,12 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 }
                 mma_commit(bar(kBarABEmpty + w));
                 mma_commit(bar(kBarDFull + w));
+                last = P;
             }
+            // the MMAs this warp issued have completed before tensor memory is freed
+            // (after a give-up their D buffer may never have been read)
+            if (last >= 0)
+                mbar_drain(bar(kBarDFull + w), (uint32_t)(last / kMmaWarps) & 1u);
         }
         __syncwarp();
     } else {
@@ -644,8 +657,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
 namespace tgi {
 
 int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N, int G,
-                int tiles, int M, int64_t max_abs_scale, bool q1, int frac, cudaStream_t s)
+                int tiles, int M, int64_t max_abs_scale, bool q1, int frac, int64_t wait_cycles, cudaStream_t s)
 {
+    const long long wait_limit = wait_cycles > 0 ? (long long)wait_cycles : kDefaultWaitCycles;
     // cuTensorMapEncodeTiled from the driver, looked up once
     using encode_fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -672,7 +686,7 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
         const uint64_t dev_bit = dev < 64 ? 1ull << dev : 0ull;   // (devices past 64: set every call)
         if (!(attr_set & dev_bit)) {
             void (*kernels[6])(const unsigned char *, const unsigned char *, const CUtensorMap, int64_t *, int, int,
-                               int, int, int, int) = {
+                               int, int, int, int, long long) = {
                 gemv_i8_mma_kernel<false, kFoldNarrow>, gemv_i8_mma_kernel<false, kFoldWide>,
                 gemv_i8_mma_kernel<false, kFoldFloor>,  gemv_i8_mma_kernel<true, kFoldNarrow>,
                 gemv_i8_mma_kernel<true, kFoldWide>,    gemv_i8_mma_kernel<true, kFoldFloor>};
@@ -705,7 +719,8 @@ int gemv_i8_mma(const uint4 *masks, const int32_t *scales, const int8_t *x, int6
     const auto *mk = reinterpret_cast<const unsigned char *>(masks);
     const auto *sc = reinterpret_cast<const unsigned char *>(scales);
 #define TGI_MMA_LAUNCH(Q, F) \
-    gemv_i8_mma_kernel<Q, F><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M, frac, ctiles)
+    gemv_i8_mma_kernel<Q, F><<<grid, kThreads, kSmemBytes, s>>>(mk, sc, xmap, y, N, G, tiles, M, frac, ctiles, \
+                                                               wait_limit)
     if (q1) {
         if (fold == kFoldNarrow)
             TGI_MMA_LAUNCH(true, kFoldNarrow);

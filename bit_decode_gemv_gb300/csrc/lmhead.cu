@@ -804,9 +804,10 @@ extern "C" size_t tg_lmhead_workspace_bytes(const tg_layout *L, int32_t k)
     return kClearedBytes + align256((size_t)L->N * 8) + align256((size_t)L->N * 8);
 }
 
-extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const int8_t *x, int32_t k,
-                                     int64_t *logits, int32_t *argmax, int32_t *ids, int64_t *scores,
-                                     int32_t *ncand, void *ws, size_t ws_bytes, void *stream)
+namespace tgi {
+
+int lmhead_check_args(const tg_layout *L, const void *w, const int8_t *x, int32_t k, const int64_t *logits,
+                      const int32_t *argmax, const int32_t *ids, const int64_t *scores, const int32_t *ncand)
 {
     if (!L || !w || !x || !argmax || !ids || !scores)
         return TG_ERR_ARG;
@@ -819,10 +820,23 @@ extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const in
     const int64_t N = L->N, K = L->K;
     if (N < 1 || K < TG_GROUP || K % TG_GROUP || k < 1 || k > TG_MAX_K || k > N)
         return TG_ERR_SHAPE;
+    if ((K / 16 + 31) / 32 > 16)   // 16-byte chunks of a row per lane
+        return TG_ERR_SHAPE;
+    return TG_OK;
+}
+
+}  // namespace tgi
+
+extern "C" int tg_lmhead_argmax_topk(const tg_layout *L, const void *w, const int8_t *x, int32_t k,
+                                     int64_t *logits, int32_t *argmax, int32_t *ids, int64_t *scores,
+                                     int32_t *ncand, void *ws, size_t ws_bytes, void *stream)
+{
+    const int bad = tgi::lmhead_check_args(L, w, x, k, logits, argmax, ids, scores, ncand);
+    if (bad != TG_OK)
+        return bad;
+    const int64_t N = L->N, K = L->K;
     const int C16 = (int)(K / 16);
     const int cpl = (C16 + 31) / 32;
-    if (cpl > 16)
-        return TG_ERR_SHAPE;
     if (!ws || !tgi::aligned(ws, 256) || ws_bytes < tg_lmhead_workspace_bytes(L, k))
         return TG_ERR_WORKSPACE;
     int idx_bits = 1;

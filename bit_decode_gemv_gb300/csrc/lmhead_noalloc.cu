@@ -24,6 +24,7 @@
 #include <mutex>
 
 #include "tg.h"
+#include "tg_internal.h"
 
 namespace {
 
@@ -37,7 +38,10 @@ std::mutex g_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached; NULL on failure.
+// device (with that device current) and cached; NULL on failure. The cache
+// lives as long as the process: after cudaDeviceReset the array's address on
+// that device is no longer valid, so the call must not be used on a device
+// that was reset (tg.h says so).
 void *scratch_for_current_device()
 {
     int dev = 0;
@@ -60,12 +64,12 @@ extern "C" int tg_lmhead_argmax_topk_noalloc(const tg_layout *L, const void *w, 
                                              int32_t *ids, int64_t *scores, int32_t *ncand,
                                              void *stream)
 {
-    if (!L)
-        return TG_ERR_ARG;
-    const size_t need = tg_lmhead_workspace_bytes(L, k);
-    if (need == 0)
-        return L->kind != TG_PLANES8 ? TG_ERR_ARG : TG_ERR_SHAPE;
-    if (need > (size_t)TG_NOALLOC_SCRATCH_BYTES)
+    // the same checks, in the same order, as the workspace-taking call; only then
+    // whether the problem's workspace fits the fixed array
+    const int bad = tgi::lmhead_check_args(L, w, x, k, logits, argmax, ids, scores, ncand);
+    if (bad != TG_OK)
+        return bad;
+    if (tg_lmhead_workspace_bytes(L, k) > (size_t)TG_NOALLOC_SCRATCH_BYTES)
         return TG_ERR_WORKSPACE;
     void *ws = scratch_for_current_device();
     if (!ws)

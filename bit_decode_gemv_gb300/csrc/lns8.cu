@@ -163,7 +163,7 @@ __device__ void clamp_lanes(const uint32_t (&w4)[4], int tq, const int (&e)[2], 
 __global__ void __launch_bounds__(kWarps * 32)
 lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                 const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
-                const __grid_constant__ PhaseF F, int N, int G, int gpc)
+                const __grid_constant__ PhaseF F, const double *__restrict__ Fd, int N, int G, int gpc)
 {
     __shared__ uint2 vfrag[kChunkGroups][8][32];   // V fragments (b0, b1) per group, chunk, lane
     __shared__ unsigned gmin[kChunkGroups], gmax[kChunkGroups];
@@ -354,7 +354,8 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         __syncthreads();
         double *prod = reinterpret_cast<double *>(&arow[0][0]);
         static_assert(kWarps * 32 % 8 == 0, "a thread's phase p = tid & 7 is the same for all its items");
-        const double fp = F.f[tid & 7];   // F is a grid constant: indexed in place, not copied
+        // the caller's F[p] (device memory) when given, else the built-in grid constant
+        const double fp = Fd ? Fd[tid & 7] : F.f[tid & 7];
         for (int item = tid; item < rows_here * 8; item += blockDim.x)
             prod[item] = __dmul_rn((double)arow[item >> 3][item & 7], fp);
         __syncthreads();
@@ -373,8 +374,8 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
 
 }  // namespace
 
-extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8_t *xa, int64_t *A,
-                                  double *S, void *stream)
+extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8_t *xa, const double *F_dev,
+                                  int64_t *A, double *S, void *stream)
 {
     if (!L || !w || !xa || !A)
         return TG_ERR_ARG;
@@ -383,8 +384,10 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
         return TG_ERR_ARG;
     if (pure ? (L->frac < 1 || L->frac > 6 || (L->flags & TG_FLAG_LNS8_STATE_SET)) : L->frac != 0)
         return TG_ERR_ARG;   // frac is the pure route's internal precision, 0 otherwise
+    if (pure && F_dev)
+        return TG_ERR_ARG;   // the pure route's S is a log-domain value; it takes no F
     if (!tgi::aligned(w, 256) || !tgi::aligned(xa, 16) || !tgi::aligned(A, 8) ||
-        (S && !tgi::aligned(S, 8)))
+        (S && !tgi::aligned(S, 8)) || (F_dev && !tgi::aligned(F_dev, 8)))
         return TG_ERR_ARG;
     if (L->N < 1 || L->K < TG_GROUP || L->K % TG_GROUP)
         return TG_ERR_SHAPE;
@@ -401,7 +404,7 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = (int)L->G, N = (int)L->N;
     if (L->flags & TG_FLAG_LNS8_STATE_SET)
-        return tgi::lns8_stateset(masks, codes, xa, A, S, F.f, N, G, (int)L->tiles, s);
+        return tgi::lns8_stateset(masks, codes, xa, A, S, F.f, F_dev, N, G, (int)L->tiles, s);
     if (pure)
         return tgi::lns8_purelns(masks, codes, xa, A, S, N, G, (int)L->frac, s);
     const int gpc = (G + kMaxCluster - 1) / kMaxCluster;   // groups per CTA
@@ -419,7 +422,7 @@ extern "C" int tg_gemv_lns8_phase(const tg_layout *L, const void *w, const uint8
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, lns8_mma_kernel, masks, codes, xa, A, S, F, N, G, gpc) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, lns8_mma_kernel, masks, codes, xa, A, S, F, F_dev, N, G, gpc) != cudaSuccess)
         return TG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }

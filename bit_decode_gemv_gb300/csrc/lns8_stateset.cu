@@ -208,7 +208,8 @@ struct PhaseF {
 __global__ void __launch_bounds__(kWarps * 32)
 lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                      const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
-                     const __grid_constant__ PhaseF F, int N, int G, int tiles, int gpc)
+                     const __grid_constant__ PhaseF F, const double *__restrict__ Fd, int N, int G, int tiles,
+                     int gpc)
 {
     __shared__ __align__(16) uint2 lists[kChunk][4][kListStride];
     __shared__ WordMeta meta[kChunk][4];
@@ -354,7 +355,8 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
         __syncthreads();
         static_assert(kWarps * 32 % 8 == 0, "a thread's phase p = tid & 7 is the same for all its items");
         double *prod = reinterpret_cast<double *>(&arow[0][0]);
-        const double fp = F.f[tid & 7];   // F is a grid constant: indexed in place, not copied
+        // the caller's F[p] (device memory) when given, else the built-in grid constant
+        const double fp = Fd ? Fd[tid & 7] : F.f[tid & 7];
         for (int item = tid; item < rows_here * 8; item += blockDim.x)
             prod[item] = __dmul_rn((double)arow[item >> 3][item & 7], fp);
         __syncthreads();
@@ -376,7 +378,7 @@ lns8_stateset_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict_
 namespace tgi {
 
 int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, int64_t *A, double *S,
-                  const double F[8], int N, int G, int tiles, cudaStream_t s)
+                  const double F[8], const double *F_dev, int N, int G, int tiles, cudaStream_t s)
 {
     PhaseF f;
     for (int p = 0; p < 8; p++)
@@ -396,7 +398,7 @@ int lns8_stateset(const uint4 *masks, const uint8_t *codes, const uint8_t *xa, i
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, lns8_stateset_kernel, masks, codes, xa, A, S, f, N, G, tiles, gpc) !=
+    if (cudaLaunchKernelEx(&cfg, lns8_stateset_kernel, masks, codes, xa, A, S, f, F_dev, N, G, tiles, gpc) !=
         cudaSuccess)
         return TG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;

@@ -151,7 +151,13 @@ typedef struct tg_layout {
     int64_t frac;           /* per-group floor shift (TG_TERNARY_I8, TG_BINARY_Q1): 0..62;
                                internal fractional bits of the pure-LNS route (TG_TERNARY_LNS8
                                with TG_FLAG_LNS8_PURE_LNS): 1..6; otherwise 0. 0 after packing */
-    int64_t reserved[2];
+    int64_t wait_limit;     /* SM clock cycles each bounded device-side wait may last before
+                               the kernel gives up and reports TG_ERR_DEVICE (the tensor-memory
+                               batched GEMM is the kernel with such waits); 0 = the default,
+                               2^32 cycles (about two seconds). A caller that wants a stuck
+                               kernel to fail sooner sets it; tests set it very low to exercise
+                               the give-up path. 0 after packing */
+    int64_t reserved[1];
 } tg_layout;
 
 /*
@@ -256,13 +262,21 @@ int tg_gemv_i8(const tg_layout *layout, const void *w, const int8_t *x, int64_t 
  *   For every lane with t != 0 and code a != 0 the product code is
  *   k = a + d[r][g] - 74 with d the group's scale code; k <= 0 is exact zero,
  *   k > 127 saturates to 127; the sign is the activation sign XOR [t < 0].
+ *   F       device fp64 [8], 8-byte aligned, or NULL: the phase constants of
+ *           the materialisation. NULL uses the built-in F[p] = 2^((p-2)/8)
+ *           (BitState brief §3.1: phase p of band b is worth 2^(b + (p-2)/8 - 9)),
+ *           the correctly rounded fp64 values from the host's exp2. A caller
+ *           that keeps its own table (another rounding, a rescaled basis)
+ *           passes it here. Read by the kernel; the caller keeps it valid until
+ *           the call's work on the stream is done. Must be NULL with
+ *           TG_FLAG_LNS8_PURE_LNS (that route's S is a log-domain value).
  *   A       device int64 [N][8]: A[r][k & 7] += sign * (1 << (k >> 3)).
  *   S       device fp64 [N] or NULL: S[r] = 2^-9 * sum_{p=0..7} A[r][p] * F[p],
- *           F[p] = 2^((p-2)/8), summed in the order p = 0..7, each product and
- *           sum rounded once (no fused multiply-add).
+ *           summed in the order p = 0..7, each product and sum rounded once
+ *           (no fused multiply-add).
  * Errors: TG_ERR_ARG, TG_ERR_SHAPE, TG_ERR_BOUND (K >= 65536), TG_ERR_CUDA.
  */
-int tg_gemv_lns8_phase(const tg_layout *layout, const void *w, const uint8_t *xa,
+int tg_gemv_lns8_phase(const tg_layout *layout, const void *w, const uint8_t *xa, const double *F,
                        int64_t *A, double *S, void *stream);
 
 /* Device workspace bytes tg_lmhead_argmax_topk needs for this layout and k. */
@@ -310,11 +324,15 @@ int tg_lmhead_argmax_topk(const tg_layout *layout, const void *w, const int8_t *
  * library's own device memory, which every GPU that loads the library keeps
  * until the process exits. The call itself allocates nothing.
  *   - Limit: problems whose tg_lmhead_workspace_bytes(layout, k) exceeds
- *     TG_NOALLOC_SCRATCH_BYTES (N above about 258,000 rows) are rejected with
- *     TG_ERR_WORKSPACE before anything is enqueued.
+ *     TG_NOALLOC_SCRATCH_BYTES (N above 259,008 rows) are rejected with
+ *     TG_ERR_WORKSPACE before anything is enqueued. The other arguments are
+ *     checked first, in the same order as tg_lmhead_argmax_topk, so an invalid
+ *     call gets the same TG_ERR_ARG / TG_ERR_SHAPE whatever its size.
  *   - The first call on each device looks up the array's device address with
- *     that device current and caches it; make that first call before any stream
- *     capture. A failed lookup returns TG_ERR_CUDA.
+ *     that device current and caches it for the life of the process; make that
+ *     first call before any stream capture. A failed lookup returns
+ *     TG_ERR_CUDA. The cached address does not survive cudaDeviceReset: after
+ *     resetting a device, do not use this call on it again in the same process.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents (nothing needs to be cleared: each call resets what it counts).
  *     Calls whose work overlaps on the GPU race on it; the caller must order

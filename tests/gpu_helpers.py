@@ -58,3 +58,19 @@ def lmhead(wd, L, x, k, full):
     torch.cuda.synchronize()
     return dict(logits=None if logits is None else logits.cpu().numpy(), argmax=int(argmax.item()),
                 ids=ids.cpu().numpy(), scores=scores.cpu().numpy(), ncand=int(ncand.item()))
+
+
+def oracle_by_row_slices(fn, t, d, *rest, threads=None):
+    """An oracle GEMV over all rows, computed as contiguous row slices on
+    concurrent threads (the oracle's C call releases the GIL) and concatenated
+    along the output's row axis. Every row is still the oracle's own result; the
+    split only spreads the work over the host's cores."""
+    import concurrent.futures as cf
+    import os
+    N = t.shape[0]
+    n = max(1, min(threads or os.cpu_count() or 1, N))
+    cuts = [N * i // n for i in range(n + 1)]
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        parts = list(ex.map(lambda ab: fn(t[ab[0]:ab[1]], d[ab[0]:ab[1]], *rest), zip(cuts[:-1], cuts[1:])))
+    return np.concatenate(parts, axis=-1)
+

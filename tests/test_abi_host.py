@@ -245,6 +245,9 @@ def test_gemv_argument_errors():
         fr = tg.tg_layout.from_buffer_copy(L)
         fr.frac = frac
         assert status_of(f, fr, A256, A256, 1, A256, 0) == tg.TG_ERR_ARG
+    neg = tg.tg_layout.from_buffer_copy(L)
+    neg.wait_limit = -1                                                       # a wait bound below zero
+    assert status_of(f, neg, A256, A256, 17, A256, 0) == tg.TG_ERR_ARG
 
 
 def test_lns8_argument_errors():
@@ -271,6 +274,12 @@ def test_lns8_argument_errors():
     both.flags = tg.TG_FLAG_LNS8_PURE_LNS | tg.TG_FLAG_LNS8_STATE_SET
     both.frac = 3
     assert status_of(f, both, A256, A256, A256, None, 0) == tg.TG_ERR_ARG
+    # the caller's phase constants F: 8-byte aligned, and not with the pure route
+    assert status_of(f, L, A256, A256, A256, None, 0, A256 + 4) == tg.TG_ERR_ARG
+    pl = tg.tg_layout.from_buffer_copy(L)
+    pl.flags = tg.TG_FLAG_LNS8_PURE_LNS
+    pl.frac = 4
+    assert status_of(f, pl, A256, A256, A256, None, 0, A256) == tg.TG_ERR_ARG
 
 
 def test_lmhead_argument_errors():
@@ -298,6 +307,40 @@ def test_lmhead_argument_errors():
     big.max_abs_scale = 1 << 31
     assert status_of(f, big, A256, A256, 10, None, A256, A256, A256, None, A256, wsb, 0) == tg.TG_ERR_BOUND
     assert tg.tg_lmhead_workspace_bytes(tg.tg_layout_init(tg.TG_TERNARY_I8, 8, 128), 4) == 0
+
+
+def test_noalloc_checks_arguments_before_the_scratch_size():
+    """tg_lmhead_argmax_topk_noalloc reports the same argument and shape errors as
+    the workspace-taking call, in the same order, whatever the problem size: a
+    problem too large for the fixed scratch is only refused (TG_ERR_WORKSPACE)
+    once its other arguments are valid. Every case returns before any CUDA call."""
+    f = tg.tg_lmhead_argmax_topk_noalloc
+    L = tg.tg_layout_init(tg.TG_PLANES8, 300000, 128)     # workspace far above the scratch
+    L.max_abs_scale = 1
+    assert tg.tg_lmhead_workspace_bytes(L, 10) > tg.TG_NOALLOC_SCRATCH_BYTES
+
+    def call(layout=L, w=A256, x=A256, k=10, logits=None, argmax=A256, ids=A256, scores=A256, ncand=None):
+        return status_of(f, layout, w, x, k, logits, argmax, ids, scores, ncand, 0)
+
+    assert call() == tg.TG_ERR_WORKSPACE
+    assert call(argmax=None) == tg.TG_ERR_ARG
+    assert call(w=None) == tg.TG_ERR_ARG
+    assert call(x=A256 + 8) == tg.TG_ERR_ARG
+    assert call(scores=A256 + 4) == tg.TG_ERR_ARG
+    assert call(k=0) == tg.TG_ERR_SHAPE
+    assert call(k=tg.TG_MAX_K + 1) == tg.TG_ERR_SHAPE
+    small = tg.tg_layout_init(tg.TG_PLANES8, 8, 128)
+    small.max_abs_scale = 1
+    assert call(layout=small, k=9) == tg.TG_ERR_SHAPE               # k > N
+    wrong = tg.tg_layout_init(tg.TG_TERNARY_I8, 300000, 128)
+    assert call(layout=wrong) == tg.TG_ERR_ARG
+    # the scratch's exact limit: N = 259008 rows fit, one more row does not
+    edge = tg.tg_layout_init(tg.TG_PLANES8, 259008, 128)
+    assert tg.tg_lmhead_workspace_bytes(edge, 10) == tg.TG_NOALLOC_SCRATCH_BYTES
+    edge.N = 259009
+    assert tg.tg_lmhead_workspace_bytes(edge, 10) > tg.TG_NOALLOC_SCRATCH_BYTES
+    edge.max_abs_scale = 1
+    assert call(layout=edge) == tg.TG_ERR_WORKSPACE
 
 
 def test_layout_flags_are_distinct_bits():

@@ -128,6 +128,34 @@ def test_one_state_saturates_or_vanishes(route):
     check(dict(t=t, dcode=dcode, xa=xa), route=route)
 
 
+@pytest.mark.parametrize("route", ROUTES)
+def test_caller_phase_constants(route):
+    """S with the caller's F (a device fp64 [8]): the built-in values passed in
+    give S bit for bit equal to F = NULL; another table (signs, zeros, a scaled
+    basis) gives 2^-9 sum_p A[p] F[p] in the order p = 0..7 with that table,
+    which the oracle's materialisation computes with the same F."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    from gpu_helpers import dev, pack_to_device
+    w = W.lns8(seed=21, N=700, K=1024)
+    wd, L = pack_to_device(tg.TG_TERNARY_LNS8, w["t"], w["dcode"])
+    if route == "stateset":
+        L.flags |= tg.TG_FLAG_LNS8_STATE_SET
+    xa = dev(w["xa"])
+    A = torch.empty((L.N, 8), dtype=torch.int64, device="cuda")
+    S0 = torch.empty((L.N,), dtype=torch.float64, device="cuda")
+    tg.tg_gemv_lns8_phase(L, wd, xa, A, S0)
+    A_ref = oracle.lns8_direct(w["t"], w["dcode"], w["xa"])
+    for F in (oracle.lns8_F(), np.array([0.5, -1.0, 0.0, 3.0, 1e-3, -2.5, 7.0, 1.0 / 3.0])):
+        S = torch.full((L.N,), float("nan"), dtype=torch.float64, device="cuda")
+        tg.tg_gemv_lns8_phase(L, wd, xa, A, S, F=dev(np.asarray(F, np.float64)))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(A.cpu().numpy(), A_ref)
+        S_ref = oracle.lns8_materialise(A_ref, np.asarray(F, np.float64))
+        np.testing.assert_array_equal(S.cpu().numpy(), S_ref)
+    np.testing.assert_array_equal(S0.cpu().numpy(), oracle.lns8_materialise(A_ref))
+
+
 def test_routes_agree_bitwise_on_the_workload():
     """The two routes return the same A and the same S bits on the workload."""
     w = W.lns8(seed=4, N=1024, K=4096)

@@ -65,6 +65,41 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
                 np.testing.assert_array_equal(got["logits"], ref["logits"])
 
 
+@pytest.mark.parametrize("rows", ["random", "all_equal"])
+def test_noalloc_at_the_scratch_limit(rows):
+    """The largest problem the fixed scratch holds: N = 259,008 rows, whose
+    workspace is exactly TG_NOALLOC_SCRATCH_BYTES, so the per-row stage-1 sums and
+    the candidate list reach the array's last byte. With every row equal, every
+    row is a candidate and the candidate list is filled to its end. Both paths,
+    two calls in a row, each compared with the workspace-taking call."""
+    import torch
+    import bit_decode_gemv_gb300 as tg
+    N, K, k = 259008, 128, 16
+    w = W.lm_head(seed=13, N=8 if rows == "all_equal" else N, K=K)
+    if rows == "all_equal":
+        w["planes"] = np.ascontiguousarray(np.broadcast_to(w["planes"][:, :1, :], (8, N, K)))
+        w["s"] = np.full(N, int(w["s"][0]), np.int32)
+    blob, L = tg.tg_pack_weights(tg.TG_PLANES8, w["planes"], w["s"])
+    del w["planes"]
+    assert tg.tg_lmhead_workspace_bytes(L, k) == tg.TG_NOALLOC_SCRATCH_BYTES
+    wd = torch.from_numpy(blob).cuda()
+    for x in (W.x_normal40(14, (K,)), W.x_normal40(15, (K,))):
+        for full in (False, True):
+            got = run(tg, torch, L, wd, x, k, full, noalloc=True)
+            ref = run(tg, torch, L, wd, x, k, full, noalloc=False)
+            np.testing.assert_array_equal(got["ids"], ref["ids"])
+            np.testing.assert_array_equal(got["scores"], ref["scores"])
+            assert got["argmax"] == ref["argmax"] == int(ref["ids"][0])
+            assert got["ncand"] == ref["ncand"]
+            if full:
+                np.testing.assert_array_equal(got["logits"], ref["logits"])
+            if rows == "all_equal":
+                # equal scores: the lowest indices, in order (integer_engine.md §3.3)
+                np.testing.assert_array_equal(got["ids"], np.arange(k))
+                if not full:
+                    assert got["ncand"] == N
+
+
 def test_noalloc_refuses_problems_larger_than_the_scratch():
     import bit_decode_gemv_gb300 as tg
     L = tg.tg_layout_init(tg.TG_PLANES8, 300000, 128)
