@@ -215,13 +215,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         : "memory");
     if (done)
         return true;
+    // each try_wait may suspend the warp until the phase completes, for at most
+    // this many nanoseconds (a quarter of the limit's cycles, so that a short
+    // limit still runs out on time; at most a millisecond): a waiting warp then
+    // issues nothing instead of polling
+    const uint32_t hint_ns = (uint32_t)min(limit >> 2, 1000000ll);
     const long long start = clock64();
     while (true) {
         asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
             : "memory");
         if (done)
             return true;
