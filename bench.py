@@ -377,6 +377,18 @@ def row_lns8(tg, torch, stream, dev):
                     "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
                     "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}
         del g
+    # the same direct route with activation codes over the whole range (about a
+    # fifth of the lanes near an end, so most (row, group) pairs need the exact
+    # clamp correction)
+    xf = dev(W.lns8_activations_full_range(0, L.K))
+    g = capture_graph(torch, lambda i, h: tg.tg_gemv_lns8_phase(L, wd[i % R], xf, A, S, h), R)
+    g.replay()
+    t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
+    out["lns8_full_range_codes"] = {"workload": "N=4096 K=4096 LNS8 eight-phase, direct route, activation codes "
+                                                "uniform over 1..127 (10% zero)",
+                                    "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
+                                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}
+    del g
     return out
 
 

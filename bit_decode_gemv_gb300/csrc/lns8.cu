@@ -16,10 +16,11 @@
 // and add G[q] * 2^(beta + [q + delta >= 8]) into A[(q + delta) & 7]. This is
 // exact when no lane of that (row, group) is clamped (k in 1..127 for every
 // nonzero lane), which is checked per (row, group) from the group's smallest
-// and largest nonzero activation code. In the rare (row, group) that can clamp,
-// the lanes that do clamp are found with bytewise compares, taken back out of
-// G, and their saturated value (+-2^15 in phase 7, or nothing for k <= 0) is
-// added directly; the rest stays on the factorised path.
+// and largest nonzero activation code. In a (row, group) that can clamp, the
+// lanes that do clamp -- found from a per-warp list of the group's lanes that
+// can clamp for any of the warp's rows -- are taken back out of G, and their
+// saturated value (+-2^15 in phase 7, or nothing for k <= 0) is added
+// directly; the rest stays on the factorised path.
 //
 // G is a contraction t (rows x lanes) . V (lanes x 8) with V[i][q] = s_i 2^c_i
 // when a_i & 7 == q, else 0. Every entry (+-1, +-2^c) is exact in bf16 and
@@ -82,81 +83,76 @@ __device__ __forceinline__ uint32_t v_entry(uint32_t xab, uint32_t q)
     return (a != 0u && (a & 7u) == q) ? bf16_pow2(xab >> 7, a >> 3) : 0u;
 }
 
-// Lanes of one (row, group) whose product code k = a + e leaves 1..127, for the
-// 32 lanes this thread holds of that row: each such lane's term +-2^c is taken
-// back out of its class sum (added, negated, into gcorr[a & 7], the row's
-// class corrections in shared memory), and the value the lane really
-// contributes is returned: +-2^15 into phase 7 for k > 127, nothing for k <= 0.
-// With those lanes removed every remaining lane has k in 1..127 and the
-// factorised add is exact again.
-// The flagged lanes of chunk KC (raw: its four activation bytes of this quad
-// thread, w: the thread's mask word holding them).
-template <int KC>
-__device__ __forceinline__ void clamp_chunk(uint32_t raw, uint32_t w, int half, uint32_t TH, uint32_t UL, int e,
-                                            int *gcorr, int &clamp)
+// Exact correction of the lanes that clamp. A lane of a (row, group) clamps when
+// its product code k = a + e leaves 1..127 (e = the row's scale code - 74):
+// k <= 0 contributes nothing and k > 127 contributes +-2^15 in phase 7, but the
+// factorised class sum G[a & 7] holds its +-2^(a >> 3) as if k were in range.
+// For each group, every warp lists once the lanes that can clamp for ANY of its
+// rows -- nonzero codes with a + min(e) <= 0 or a + max(e) > 127, over the
+// warp's rows below N -- and the (row, group) that can clamp walks only that
+// list: each listed lane whose weight is nonzero and that does clamp for the
+// row has its term taken back out of its class sum (into gcorr, the row's class
+// corrections) and its saturated value, if any, added to the phase-7 term. Every
+// other lane stays on the factorised path, where it is exact. The list is split
+// by the quad thread that holds the lane's mask bits (lane 16kc + o of the
+// group: thread (o & 7) >> 1 of the quad, byte (o & 1) + 2 (o >> 3) of chunk kc).
+// Entry: code a (bits 0-6), activation sign (bit 7), chunk kc (bits 8-10), byte
+// bi (bits 11-12).
+constexpr int kListMax = 32;   // lanes of a group one quad thread holds
+
+// Build this warp's lists for one group (called by the whole warp): x4 = the
+// group's activation bytes 4 lane .. 4 lane + 3; emin/emax = the warp's e range.
+__device__ __forceinline__ void build_clamp_lists(uint32_t x4, int emin, int emax, uint16_t (*list)[kListMax],
+                                                  int *cnt)
 {
-    // per byte, on 7-bit codes a (no sum below carries out of its byte):
-    // a > T is bit 7 of a + (127 - T); a < U is bit 7 clear in a + (128 - U);
-    // a != 0 is bit 7 of a + 127
-    const uint32_t a4 = raw & 0x7f7f7f7fu;
-    const uint32_t hi_f = (a4 + TH) & 0x80808080u;
-    const uint32_t lo_f = ~(a4 + UL) & 0x80808080u;
-    const uint32_t nz_f = (a4 + 0x7f7f7f7fu) & 0x80808080u;
-    uint32_t m = hi_f | (lo_f & nz_f);
-    while (m) {
-        const int bi = (__ffs((int)m) - 1) >> 3;
-        m &= m - 1u;
-        const int rp = 4 * (KC & 1) + half + 2 * (bi >> 1);
-        const int h = bi & 1;
-        if (((w >> (16 * h + 7 - rp)) & 1u) == 0u)
-            continue;
-        const uint32_t neg = (w >> (16 * h + 15 - rp)) & 1u;
-        const uint32_t xab = (raw >> (8 * bi)) & 0xffu;
+    const int lane = threadIdx.x & 31;
+    if (lane < 4)
+        cnt[lane] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < 4; b++) {
+        const uint32_t xab = (x4 >> (8 * b)) & 0xffu;
         const int a = (int)(xab & 0x7fu);
-        const bool minus = ((xab >> 7) ^ neg) != 0u;
-        const int v = 1 << (a >> 3);
-        atomicAdd(gcorr + (a & 7), minus ? v : -v);
-        if (a + e > 127)
-            clamp += minus ? -(1 << 15) : (1 << 15);
+        if (a != 0 && (a + emin <= 0 || a + emax > 127)) {
+            const int i = 4 * lane + b, o = i & 15;
+            const int tq = (o & 7) >> 1;
+            const int bi = (o & 1) + 2 * (o >> 3);
+            const int slot = atomicAdd(cnt + tq, 1);
+            list[tq][slot] = (uint16_t)(a | (int)(xab & 0x80u) | ((i >> 4) << 8) | (bi << 11));
+        }
     }
+    __syncwarp();
 }
 
-// Both rows of a quad (halves 0 and 1: rows q and q + 8) hold the same 32 lanes,
-// so one call loads their activation bytes once and scans them for each row
-// that needs it (need[h]), with that row's e[h], corrections gcorr[h] and
-// saturation term clamp[h].
-__device__ void clamp_lanes(const uint32_t (&w4)[4], int tq, const int (&e)[2], const bool (&need)[2],
-                            const uint8_t *xg, int *const (&gcorr)[2], int (&clamp)[2])
+// Walk this quad thread's list for the rows (halves) that need it.
+__device__ __forceinline__ void walk_clamp_list(const uint16_t *list, int n, const uint32_t (&w4)[4], const int (&e)[2],
+                                                const bool (&need)[2], int *const (&gcorr)[2], int (&clamp)[2])
 {
-    uint32_t TH[2], UL[2];
+    clamp[0] = clamp[1] = 0;
+    for (int j = 0; j < n; j++) {
+        const uint32_t ent = list[j];
+        const int a = (int)(ent & 0x7fu);
+        const uint32_t sgn = (ent >> 7) & 1u;
+        const int kc = (int)(ent >> 8) & 7, bi = (int)(ent >> 11) & 3;
+        const int wi = kc >> 1;
+        const uint32_t w = wi == 0 ? w4[0] : wi == 1 ? w4[1] : wi == 2 ? w4[2] : w4[3];
 #pragma unroll
-    for (int h = 0; h < 2; h++) {
-        const uint32_t T = (uint32_t)min(max(127 - e[h], 0), 127);   // a > T = 127 - e saturates
-        const uint32_t U = (uint32_t)min(max(1 - e[h], 1), 128);     // 0 < a < U = 1 - e is zero
-        TH[h] = (127u - T) * 0x01010101u;
-        UL[h] = (128u - U) * 0x01010101u;
-        clamp[h] = 0;
-    }
-    const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xg);
-    // chunk kc: lanes 16kc + 2tq + {0, 1} and 16kc + 8 + 2tq + {0, 1} (byte bi = 2 * rr + h).
-    // All sixteen loads are issued first, so that they are in flight together
-    // (inside the scan, behind its shared-memory atomics, they went one by one).
-    auto ld = [&](int kc) {
-        return (uint32_t)__ldg(x16 + 8 * kc + tq) | ((uint32_t)__ldg(x16 + 8 * kc + 4 + tq) << 16);
-    };
-    const uint32_t r[8] = {ld(0), ld(1), ld(2), ld(3), ld(4), ld(5), ld(6), ld(7)};
-#pragma unroll
-    for (int h = 0; h < 2; h++) {
-        if (!need[h])
-            continue;
-        clamp_chunk<0>(r[0], w4[0], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<1>(r[1], w4[0], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<2>(r[2], w4[1], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<3>(r[3], w4[1], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<4>(r[4], w4[2], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<5>(r[5], w4[2], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<6>(r[6], w4[3], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
-        clamp_chunk<7>(r[7], w4[3], h, TH[h], UL[h], e[h], gcorr[h], clamp[h]);
+        for (int half = 0; half < 2; half++) {
+            if (!need[half])
+                continue;
+            const int rp = 4 * (kc & 1) + half + 2 * (bi >> 1);
+            const int h = bi & 1;
+            if (((w >> (16 * h + 7 - rp)) & 1u) == 0u)
+                continue;
+            const int k = a + e[half];
+            if (k > 0 && k <= 127)
+                continue;
+            const bool minus = (sgn ^ ((w >> (16 * h + 15 - rp)) & 1u)) != 0u;
+            const int v = 1 << (a >> 3);
+            atomicAdd(gcorr[half] + (a & 7), minus ? v : -v);
+            if (k > 127)
+                clamp[half] += minus ? -(1 << 15) : (1 << 15);
+        }
     }
 }
 
@@ -171,6 +167,8 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     __shared__ int stage[kRows + kMaxCluster][8];  // partials of the rows this CTA owns, per source CTA
     __shared__ int gcorr[kWarps][16][8];           // class-sum corrections of clamped lanes, per warp row
     __shared__ int64_t arow[kRows][8];             // int64 A of the rows this CTA owns
+    __shared__ uint16_t clist[kWarps][4][kListMax];  // per warp: the lanes of a group that can clamp, by quad thread
+    __shared__ int ccnt[kWarps][4];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -194,15 +192,18 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         // shared-memory set-up so the weight stream overlaps it
         uint4 wv[kChunkGroups];
         int ec[kChunkGroups][2];
+        uint32_t xw[kChunkGroups];   // activation bytes 4 lane .. 4 lane + 3 of each group (clamp lists)
 #pragma unroll
         for (int gl = 0; gl < kChunkGroups; gl++) {
             wv[gl] = make_uint4(0, 0, 0, 0);
             ec[gl][0] = ec[gl][1] = 0;
+            xw[gl] = 0;
             if (active && gl < ng) {
                 const size_t unit = (size_t)rb * G + c0 + gl;
                 wv[gl] = tgi::ldg_stream(masks + unit * 32 + lane);
                 ec[gl][0] = (int)__ldg(codes + unit * 16 + gq) - 74;
                 ec[gl][1] = (int)__ldg(codes + unit * 16 + gq + 8) - 74;
+                xw[gl] = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)(c0 + gl) * TG_GROUP) + lane);
             }
         }
         __syncthreads();
@@ -285,10 +286,23 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                     need[half] = !(lo > 127 || (lo + e[half] >= 1 && hi + e[half] <= 127) ||
                                    rb * 16 + gq + 8 * half >= N);
                 int clamp[2] = {0, 0};
+                if (__any_sync(0xffffffffu, need[0] || need[1])) {
+                    // the warp's e range over its rows below N, then its lists for this group
+                    int emin = 1 << 20, emax = -(1 << 20);
+#pragma unroll
+                    for (int half = 0; half < 2; half++)
+                        if (rb * 16 + gq + 8 * half < N) {
+                            emin = min(emin, e[half]);
+                            emax = max(emax, e[half]);
+                        }
+                    emin = __reduce_min_sync(0xffffffffu, emin);
+                    emax = __reduce_max_sync(0xffffffffu, emax);
+                    build_clamp_lists(xw[gl], emin, emax, clist[warp], ccnt[warp]);
+                }
                 if (need[0] || need[1]) {
                     int *const gc[2] = {gcorr[warp][gq], gcorr[warp][gq + 8]};
                     const unsigned qmask = 0xfu << (lane & ~3);
-                    clamp_lanes(w4, tq, e, need, xa + (size_t)(c0 + gl) * TG_GROUP, gc, clamp);
+                    walk_clamp_list(clist[warp][tq], ccnt[warp][tq], w4, e, need, gc, clamp);
                     __syncwarp(qmask);
 #pragma unroll
                     for (int half = 0; half < 2; half++) {   // this thread's two classes of each row

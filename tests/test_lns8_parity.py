@@ -52,6 +52,15 @@ def test_lns8_workload_full_size(route):
     check(W.lns8(), route=route)
 
 
+@pytest.mark.parametrize("route", ROUTES)
+def test_lns8_full_range_codes_full_size(route):
+    """The bench's full-range row: codes uniform over 1..127, so most (row, group)
+    pairs of N = K = 4096 have lanes that clamp at scale codes 60..88."""
+    w = W.lns8()
+    w["xa"] = W.lns8_activations_full_range(0, 4096)
+    check(w, route=route)
+
+
 def wide(seed, N, K):
     """Codes over 0..127 and scale codes over the whole byte range, so that both
     clamps (k <= 0 and k > 127) and signed zeros occur often."""

@@ -107,6 +107,18 @@ def lns8_activations(seed: int, k: int) -> np.ndarray:
     return ((sign << 7) | code).astype(np.uint8)
 
 
+def lns8_activations_full_range(seed: int, k: int) -> np.ndarray:
+    """LNS8 activation bytes with codes over the whole range: each lane is exact
+    zero with probability 0.1, otherwise its code is uniform over 1..127 (so a
+    fifth of the nonzero lanes sit within 14 codes of either end, where a
+    product code can leave 1..127 for scale codes 60..88); fair sign."""
+    code = _rng(seed, "code_full").integers(1, 128, size=k, dtype=np.int64)
+    zero = _rng(seed, "zero").random(k) < 0.1
+    code[zero] = 0
+    sign = _rng(seed, "sign").integers(0, 2, size=k, dtype=np.int64)
+    return ((sign << 7) | code).astype(np.uint8)
+
+
 def x_fixed64(seed: int, shape, frac_bits: int = 16, sigma: float = 1.0) -> np.ndarray:
     """int64 fixed-point activations with frac_bits fractional bits:
     rint(N(0, sigma^2) * 2^frac_bits)."""
