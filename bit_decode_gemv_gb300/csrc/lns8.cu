@@ -209,12 +209,12 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         __syncthreads();
         // V fragments: thread (q, j) of chunk kc holds V rows 2j, 2j+1 (b0) and
         // 2j+8, 2j+9 (b1) of column q
-        // (thread tid builds entry (kc, ln) = (tid / 32, tid % 32) of every group of
-        // the chunk; the activation bytes of all groups are loaded first, so that
-        // they are in flight together)
-        static_assert(kWarps * 32 == 256, "one V entry (chunk, lane) per thread and group");
-        {
-            const int kc = tid >> 5, ln = tid & 31;
+        // (entry (kc, ln) = (ve / 32, ve % 32), ve = 0..255, of every group of the
+        // chunk is built by thread ve mod the CTA's threads; the activation bytes of
+        // all groups are loaded first, so that they are in flight together)
+        static_assert(256 % (kWarps * 32) == 0, "V entries (chunk, lane) split evenly over the threads");
+        for (int ve = tid; ve < 256; ve += kWarps * 32) {
+            const int kc = ve >> 5, ln = ve & 31;
             const uint32_t q = (uint32_t)(ln >> 2);
             uint32_t xb[kChunkGroups][4];
 #pragma unroll

@@ -52,6 +52,7 @@ _STREAM_IDS = {
     "sparse_t": 12,
     "states": 13,
     "x64": 14,
+    "code_full": 15,
 }
 
 
