@@ -180,10 +180,9 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     const int g_begin = rank * gpc;
     const int g_end = min(G, g_begin + gpc);
 
-    for (int i = tid; i < kRows * 8; i += blockDim.x) {
-        (&acc[0][0])[i] = 0;
+    // (acc needs no clearing: each warp's first group stores its rows' partials)
+    for (int i = tid; i < kWarps * 16 * 8; i += blockDim.x)
         (&gcorr[0][0][0])[i] = 0;
-    }
 
     const bool active = rb * 16 < N;   // warp-uniform
     for (int c0 = g_begin; c0 < g_end; c0 += kChunkGroups) {
@@ -192,7 +191,10 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         // shared-memory set-up so the weight stream overlaps it
         uint4 wv[kChunkGroups];
         int ec[kChunkGroups][2];
-        uint32_t xw[kChunkGroups];   // activation bytes 4 lane .. 4 lane + 3 of each group (clamp lists)
+        uint32_t xw[kChunkGroups];   // activation bytes 4 lane .. 4 lane + 3 of each group (range, clamp lists)
+        uint32_t xb[kChunkGroups][2];   // this thread's V entry's activation byte pairs, per group
+        static_assert(kWarps * 32 == 256, "one V entry (chunk, lane) per thread and group");
+        const int vkc = tid >> 5, vln = tid & 31;
 #pragma unroll
         for (int gl = 0; gl < kChunkGroups; gl++) {
             wv[gl] = make_uint4(0, 0, 0, 0);
@@ -203,40 +205,36 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 wv[gl] = tgi::ldg_stream(masks + unit * 32 + lane);
                 ec[gl][0] = (int)__ldg(codes + unit * 16 + gq) - 74;
                 ec[gl][1] = (int)__ldg(codes + unit * 16 + gq + 8) - 74;
-                xw[gl] = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)(c0 + gl) * TG_GROUP) + lane);
             }
+            // the activations, for every warp (all threads build V): issued with the weights
+            const int gx = c0 + min(gl, ng - 1);
+            xw[gl] = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)gx * TG_GROUP) + lane);
+            const uint16_t *xg = reinterpret_cast<const uint16_t *>(xa + (size_t)gx * TG_GROUP + 16 * vkc) + (vln & 3);
+            xb[gl][0] = __ldg(xg);
+            xb[gl][1] = __ldg(xg + 4);
         }
         __syncthreads();
         // V fragments: thread (q, j) of chunk kc holds V rows 2j, 2j+1 (b0) and
-        // 2j+8, 2j+9 (b1) of column q
-        // (entry (kc, ln) = (ve / 32, ve % 32), ve = 0..255, of every group of the
-        // chunk is built by thread ve mod the CTA's threads; the activation bytes of
-        // all groups are loaded first, so that they are in flight together)
-        static_assert(256 % (kWarps * 32) == 0, "V entries (chunk, lane) split evenly over the threads");
-        for (int ve = tid; ve < 256; ve += kWarps * 32) {
-            const int kc = ve >> 5, ln = ve & 31;
-            const uint32_t q = (uint32_t)(ln >> 2);
-            uint32_t xb[kChunkGroups][4];
-#pragma unroll
-            for (int gl = 0; gl < kChunkGroups; gl++) {
-                const uint8_t *xg = xa + (size_t)(c0 + min(gl, ng - 1)) * TG_GROUP + 16 * kc + 2 * (ln & 3);
-                xb[gl][0] = xg[0];
-                xb[gl][1] = xg[1];
-                xb[gl][2] = xg[8];
-                xb[gl][3] = xg[9];
-            }
+        // 2j+8, 2j+9 (b1) of column q; thread tid builds entry (kc, ln) =
+        // (tid / 32, tid % 32) of every group of the chunk from the byte pairs it
+        // loaded above (lanes 16 kc + 2 (ln & 3) + {0, 1} and + {8, 9})
+        {
+            const uint32_t q = (uint32_t)(vln >> 2);
 #pragma unroll
             for (int gl = 0; gl < kChunkGroups; gl++) {
                 if (gl < ng) {
-                    const uint32_t b0 = v_entry(xb[gl][0], q) | (v_entry(xb[gl][1], q) << 16);
-                    const uint32_t b1 = v_entry(xb[gl][2], q) | (v_entry(xb[gl][3], q) << 16);
-                    vfrag[gl][kc][ln] = make_uint2(b0, b1);
+                    const uint32_t p0 = xb[gl][0], p1 = xb[gl][1];
+                    const uint32_t b0 = v_entry(p0 & 0xffu, q) | (v_entry(p0 >> 8, q) << 16);
+                    const uint32_t b1 = v_entry(p1 & 0xffu, q) | (v_entry(p1 >> 8, q) << 16);
+                    vfrag[gl][vkc][vln] = make_uint2(b0, b1);
                 }
             }
         }
         // smallest and largest nonzero activation code of each group
-        for (int gl = warp; gl < ng; gl += kWarps) {
-            const uint32_t v4 = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)(c0 + gl) * TG_GROUP) + lane);
+        static_assert(kChunkGroups <= kWarps, "warp gl finds group gl's range");
+        if (warp < ng) {
+            const int gl = warp;
+            const uint32_t v4 = gl == 0 ? xw[0] : gl == 1 ? xw[1] : gl == 2 ? xw[2] : xw[3];
             unsigned lo = 128u, hi = 0u;
 #pragma unroll
             for (int b = 0; b < 4; b++) {
@@ -261,6 +259,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 if (gl >= ng)
                     break;
                 const uint32_t w4[4] = {wv[gl].x, wv[gl].y, wv[gl].z, wv[gl].w};
+                const bool first = c0 == g_begin && gl == 0;   // this warp's first group: store, not add
                 // two independent accumulation chains (even and odd chunks);
                 // each partial is an integer of magnitude below 2^23, so the
                 // fp32 sums and their final sum are exact
@@ -326,7 +325,11 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                         int add = sh >= 0 ? (v << sh) : (v >> -sh);
                         if ((sidx & 7) == 7)
                             add += clamp[half];
-                        acc_row[sidx & 7] += add;
+                        // the quad's eight (thread, j) pairs cover the eight phases once per group
+                        if (first)
+                            acc_row[sidx & 7] = add;
+                        else
+                            acc_row[sidx & 7] += add;
                     }
                 }
                 __syncwarp();
