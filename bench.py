@@ -849,9 +849,11 @@ def run_ours(args):
     xs_dev = torch.empty(xs_host.shape, dtype=xs_host.dtype, device="cuda")
     ys_dev = torch.empty((GEMVS_PER_STEP, L.N), dtype=torch.int64, device="cuda")
     ys_host = torch.empty((GEMVS_PER_STEP, L.N), dtype=torch.int64).pin_memory()
-    x_views = [xs_dev[j] for j in range(GEMVS_PER_STEP)]
-    y_views = [ys_dev[j] for j in range(GEMVS_PER_STEP)]
-    w_views = [wd[j % R] for j in range(GEMVS_PER_STEP)]
+    # the calls take device addresses (the binding accepts tensors or plain
+    # integers); a decode loop resolves its buffers' addresses once, not per call
+    x_views = [xs_dev[j].data_ptr() for j in range(GEMVS_PER_STEP)]
+    y_views = [ys_dev[j].data_ptr() for j in range(GEMVS_PER_STEP)]
+    w_views = [wd[j % R].data_ptr() for j in range(GEMVS_PER_STEP)]
     readback_chunk = 128
     assert GEMVS_PER_STEP % readback_chunk == 0
     copy_stream = torch.cuda.Stream()
