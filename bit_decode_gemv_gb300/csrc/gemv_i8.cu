@@ -24,8 +24,8 @@
 // sign bit per weight (see group_pos_q1). Each group's scaled sum is floored
 // by 2^frac on its own (§4.1/§4.2 arshift) before the sum over groups.
 //
-// This file holds the batch-1 kernel (M = 1) and the entry point, which picks
-// the kernel for M > 1 (see kDp4aMaxTokens below).
+// This file holds the kernel for one to four tokens and the entry point, which
+// picks the kernel for more (see kFewMaxTokens below).
 
 #include <cuda_runtime.h>
 
@@ -92,30 +92,98 @@ __device__ __forceinline__ int group_pos_q1(const uint32_t w[4], const int8_t *x
     return pos;
 }
 
+// Several tokens (TB of them, activations TB rows of stride K apart in shared
+// memory from xg). The masked words depend on the weights only, so each is
+// formed once and fed to every token's dp4a. Ternary: out[t] = sum (t_i + 2) x_i.
+template <int TB>
+__device__ __forceinline__ void group_dot_t2_tokens(const uint32_t w[8], const int8_t *xg, int K, int out[TB])
+{
+    int a[TB][4];
+#pragma unroll
+    for (int t = 0; t < TB; t++)
+        a[t][0] = a[t][1] = a[t][2] = a[t][3] = 0;
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+        const uint32_t c0 = and_xor(w[u], 0x03030303u, 0x02020202u);
+        const uint32_t c1 = and_xor(w[u], 0x0C0C0C0Cu, 0x08080808u);
+        const uint32_t c2 = and_xor(w[u], 0x30303030u, 0x20202020u);
+        const uint32_t c3 = and_xor(w[u], 0xC0C0C0C0u, 0x80808080u);
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xg + t * K + 16 * u);
+            a[t][0] = dp4a_us(c0, xv.x, a[t][0]);
+            a[t][1] = dp4a_us(c1, xv.y, a[t][1]);
+            a[t][2] = dp4a_us(c2, xv.z, a[t][2]);
+            a[t][3] = dp4a_us(c3, xv.w, a[t][3]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TB; t++)
+        out[t] = a[t][0] + (a[t][1] >> 2) + (a[t][2] >> 4) + (a[t][3] >> 6);
+}
+
+// Q1_0 for several tokens: out[t] = sum of x over the +1 weights. Bit j of every
+// byte is moved down to bit 0 ((w >> j) & 0x01010101), so all eight columns of
+// a word accumulate into one sum per token without a shift back.
+template <int TB>
+__device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const int8_t *xg, int K, int out[TB])
+{
+    int a[TB][2];
+#pragma unroll
+    for (int t = 0; t < TB; t++)
+        a[t][0] = a[t][1] = 0;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+        uint32_t c[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            c[j] = (w[u] >> j) & 0x01010101u;
+#pragma unroll
+        for (int t = 0; t < TB; t++) {
+            const uint4 lo = *reinterpret_cast<const uint4 *>(xg + t * K + 32 * u);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(xg + t * K + 32 * u + 16);
+            const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+                a[t][j & 1] = dp4a_us(c[j], xv[j], a[t][j & 1]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TB; t++)
+        out[t] = a[t][0] + a[t][1];
+}
+
 // ---------------------------------------------------------------------------
-// Batch 1. One CTA per tile of 32 rows; lane l of every warp owns row 32T + l;
-// the CTA's W warps split the row's groups (warp w takes g = w, w + W, ...;
-// W = ceil(G / GPW), so each thread holds at most GPW groups), and the per-warp
-// int64 partials are summed through shared memory at the end. Every weight
-// load of the CTA is issued first, so a whole tile is in flight at once.
-// Launched as a programmatic dependent (constant weights), the kernel issues
-// its weight loads, lets the next kernel on the stream launch, and only then
-// waits for the previous one and stages x: the next GEMV's weight stream
-// starts while this one computes. (Measured on ffn_up: triggering right after
-// the loads beats triggering at the start, which floods the memory system
-// with several GEMVs' loads, and triggering after the compute, which leaves
-// the memory idle between GEMVs.)
+// Batch 1 and a few tokens. One CTA per tile of 32 rows; lane l of every warp
+// owns row 32T + l; the CTA's W warps split the row's groups (warp w takes
+// g = w, w + W, ...; W = ceil(G / GPW), so each thread holds at most GPW
+// groups), and the per-warp int64 partials are summed through shared memory at
+// the end. Every weight load of the CTA is issued first, so a whole tile is in
+// flight at once. Launched as a programmatic dependent (constant weights), the
+// kernel issues its weight loads, lets the next kernel on the stream launch,
+// and only then waits for the previous one and stages x: the next GEMV's weight
+// stream starts while this one computes. (Measured on ffn_up: triggering right
+// after the loads beats triggering at the start, which floods the memory
+// system with several GEMVs' loads, and triggering after the compute, which
+// leaves the memory idle between GEMVs.)
+//
+// MT tokens (1..kFewMaxTokens): the weights are read once; each thread keeps MT
+// int64 row sums, and with MT > 1 a group's masked words are formed once per
+// word and fed to every token (group_dot_t2_tokens), four tokens at a time.
 // ---------------------------------------------------------------------------
-template <int GPW, bool kQ1>
+template <int GPW, bool kQ1, int MT>
 __global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
 gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
                   const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac)
 {
     constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
+    constexpr int TB = MT < 4 ? MT : 4;      // tokens per pass over a group's masked words
+    static_assert(MT % TB == 0, "token count must be a multiple of the pass width");
     extern __shared__ __align__(16) unsigned char smem[];
-    int8_t *xs = reinterpret_cast<int8_t *>(smem);                   // [G*128]
-    int *tsum = reinterpret_cast<int *>(smem + G * 128);             // [G]
-    int64_t *red = reinterpret_cast<int64_t *>(smem + G * 128 + ((G * 4 + 15) & ~15));  // [W][32]
+    const int K = G * 128;
+    int8_t *xs = reinterpret_cast<int8_t *>(smem);                                        // [MT][K]
+    int *tsum = reinterpret_cast<int *>(smem + MT * K);                                   // [MT][G]
+    int64_t *red = reinterpret_cast<int64_t *>(smem + MT * K + ((MT * G * 4 + 15) & ~15));  // [W][MT][32]
 
     const int tile = blockIdx.x;
     const int nwarps = blockDim.x >> 5;
@@ -148,47 +216,79 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     // warp stages only its own group's activations behind a warp barrier instead
     // of all of x behind a CTA barrier (measured on ffn_up: 2.19 -> 2.03 us per
     // call with constant weights, 2.95 -> 2.67 us without).
-    const int K = G * 128;
     if (GPW == 1) {
         // one group per warp (warp w owns group w): the warp stages its own
         // group's activations from the loads that also give the group's sum
         if (warp < G) {
-            const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + warp * 128) + lane);
-            reinterpret_cast<uint32_t *>(xs + warp * 128)[lane] = v;
-            const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
-            if (lane == 0)
-                tsum[warp] = s;
+            uint32_t v[MT];
+#pragma unroll
+            for (int t = 0; t < MT; t++)
+                v[t] = __ldg(reinterpret_cast<const uint32_t *>(x + t * K + warp * 128) + lane);
+#pragma unroll
+            for (int t = 0; t < MT; t++) {
+                reinterpret_cast<uint32_t *>(xs + t * K + warp * 128)[lane] = v[t];
+                const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v[t]));
+                if (lane == 0)
+                    tsum[t * G + warp] = s;
+            }
         }
         __syncwarp();
     } else {
-        for (int i = threadIdx.x; i < K / 16; i += blockDim.x)
+        for (int i = threadIdx.x; i < MT * K / 16; i += blockDim.x)
             reinterpret_cast<uint4 *>(xs)[i] = __ldg(reinterpret_cast<const uint4 *>(x) + i);
-        for (int g = warp; g < G; g += nwarps) {
-            const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + g * 128) + lane);
+        for (int tg = warp; tg < MT * G; tg += nwarps) {
+            const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + tg * 128) + lane);
             const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
             if (lane == 0)
-                tsum[g] = s;
+                tsum[tg] = s;
         }
         __syncthreads();
     }
 
-    int64_t acc = 0;
+    int64_t acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; t++)
+        acc[t] = 0;
     for (int g0 = warp;;) {
 #pragma unroll
         for (int j = 0; j < GPW; j++) {
             const int g = g0 + j * nwarps;
             if (g < G) {
-                int P;
-                if (kQ1) {
-                    // 2 * pos_sum - block_total
-                    const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
-                    P = 2 * group_pos_q1(w, xs + g * 128) - tsum[g];
+                if constexpr (MT == 1) {
+                    int P;
+                    if (kQ1) {
+                        // 2 * pos_sum - block_total
+                        const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                        P = 2 * group_pos_q1(w, xs + g * 128) - tsum[g];
+                    } else {
+                        const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                               m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                        P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
+                    }
+                    acc[0] += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
                 } else {
-                    const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
-                                           m1[j].x, m1[j].y, m1[j].z, m1[j].w};
-                    P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
+#pragma unroll
+                    for (int t0 = 0; t0 < MT; t0 += TB) {
+                        int P[TB];
+                        if (kQ1) {
+                            const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                            group_pos_q1_tokens<TB>(w, xs + t0 * K + g * 128, K, P);
+#pragma unroll
+                            for (int t = 0; t < TB; t++)
+                                P[t] = 2 * P[t] - tsum[(t0 + t) * G + g];
+                        } else {
+                            const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                                   m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                            group_dot_t2_tokens<TB>(w, xs + t0 * K + g * 128, K, P);
+#pragma unroll
+                            for (int t = 0; t < TB; t++)
+                                P[t] -= 2 * tsum[(t0 + t) * G + g];
+                        }
+#pragma unroll
+                        for (int t = 0; t < TB; t++)
+                            acc[t0 + t] += ((int64_t)dg[j] * (int64_t)P[t]) >> frac;
+                    }
                 }
-                acc += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
             }
         }
         g0 += nwarps * GPW;
@@ -197,40 +297,49 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         load_batch(g0);
     }
 
-    red[warp * 32 + lane] = acc;
+#pragma unroll
+    for (int t = 0; t < MT; t++)
+        red[(warp * MT + t) * 32 + lane] = acc[t];
     __syncthreads();
-    if (warp == 0) {
+    const int row = tile * kTileRows + lane;
+    for (int t = warp; t < MT; t += nwarps) {
         int64_t sum = 0;
         for (int w = 0; w < nwarps; w++)
-            sum += red[w * 32 + lane];
-        const int row = tile * kTileRows + lane;
+            sum += red[(w * MT + t) * 32 + lane];
         if (row < N)
-            y[row] = sum;
+            y[(size_t)t * N + row] = sum;
     }
 }
 
 // Kernel per token count (measured crossovers on GB300, ffn_up and batched
-// shapes): M = 1 the batch-1 kernel above; 2..kDp4aMaxTokens the CUDA-core
-// dp4a kernel (gemv_i8_mt.cu: cheapest per group when only a few tokens share
-// each weight); then the warp-MMA kernel (gemv_i8_hmma.cu) for one token tile,
-// or two when K is at most kHmmaTwoTileMaxK; above that the tensor-memory
-// kernel (gemv_i8_mma.cu), whose cost hardly grows with M up to 64.
+// shapes): M = 1..kFewMaxTokens the kernel above; then the warp-MMA kernel
+// (gemv_i8_hmma.cu) for one token tile, or two when K is at most
+// kHmmaTwoTileMaxK; above that the tensor-memory kernel (gemv_i8_mma.cu), whose
+// cost hardly grows with M up to 64. The CUDA-core dp4a kernel (gemv_i8_mt.cu)
+// takes int64 activations at every M, and int8 ones at 2..kDp4aMaxTokens when
+// the activations do not fit the kernel above's shared memory (it stages the
+// tokens in chunks).
+constexpr int kFewMaxTokens = 4;
 constexpr int kDp4aMaxTokens = 4;
 constexpr int kHmmaMaxTokens = 16;
 constexpr int kHmmaTwoTileMaxK = 4096;
+constexpr size_t kM1SmemMax = 200 * 1024;
 
-size_t m1_smem_bytes(int G, int warps) { return (size_t)G * 128 + ((G * 4 + 15) & ~15) + warps * 32 * 8; }
+size_t m1_smem_bytes(int G, int warps, int MT)
+{
+    return (size_t)MT * G * 128 + (((size_t)MT * G * 4 + 15) & ~(size_t)15) + (size_t)warps * MT * 32 * 8;
+}
 
-template <int GPW, bool kQ1>
+template <int GPW, bool kQ1, int MT>
 cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
                       int G, int tiles, int frac, bool pdl, cudaStream_t s)
 {
-    auto kern = gemv_i8_m1_kernel<GPW, kQ1>;
+    auto kern = gemv_i8_m1_kernel<GPW, kQ1, MT>;
     const int max_warps = GPW >= 4 ? 16 : 32;
     int warps = (G + GPW - 1) / GPW;
     if (warps > max_warps)
         warps = max_warps;
-    const size_t smem = m1_smem_bytes(G, warps);
+    const size_t smem = m1_smem_bytes(G, warps, MT);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
@@ -247,6 +356,47 @@ cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, frac);
+}
+
+// One token: one group per warp up to K = 4096 (32 warps), then two per warp up
+// to K = 8192; beyond that 16 warps loop over batches of four groups each.
+// Several tokens: two groups per warp up to K = 8192. (Measured per call with
+// constant weights, M = 2 / 3 / 4: on ffn_up (G = 20) one group per warp took
+// 3.20 / 3.79 / 4.38 us and two 3.40 / 3.60 / 4.06 us; on 13824 x 5120
+// (G = 40) two per warp over 20 warps 7.9 / 10.1 / 12.1 us and four per warp
+// over 10 warps 7.9 / 10.7 / 13.5 us. Registers: one token's one-group warps
+// take 32, several tokens' about 64, which leaves fewer CTAs resident.)
+template <int MT, bool kQ1>
+cudaError_t launch_tokens(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
+                          int G, int tiles, int frac, bool pdl, cudaStream_t s)
+{
+    if constexpr (MT == 1) {
+        if (G <= 32)
+            return launch_m1<1, kQ1, 1>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    }
+    if (G <= 64)
+        return launch_m1<2, kQ1, MT>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    return launch_m1<4, kQ1, MT>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+}
+
+template <int MT>
+cudaError_t launch_tokens(bool q1, const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y,
+                          int N, int G, int tiles, int frac, bool pdl, cudaStream_t s)
+{
+    return q1 ? launch_tokens<MT, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s)
+              : launch_tokens<MT, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+}
+
+cudaError_t launch_few(int M, bool q1, const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y,
+                       int N, int G, int tiles, int frac, bool pdl, cudaStream_t s)
+{
+    static_assert(kFewMaxTokens == 4, "one instance per token count");
+    switch (M) {
+    case 1: return launch_tokens<1>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    case 2: return launch_tokens<2>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    case 3: return launch_tokens<3>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    default: return launch_tokens<4>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    }
 }
 
 }  // namespace
@@ -282,33 +432,14 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
         return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, true,
                                (int)L->frac, pdl, s);
 
-    if (M == 1) {
-        if (m1_smem_bytes(G, 32) > 200 * 1024)
-            return TG_ERR_SHAPE;
-        // One group per warp up to K = 4096 (32 warps), then two per warp up to
-        // K = 8192; beyond that 16 warps loop over batches of four groups each.
-        const int frac = (int)L->frac;
-        cudaError_t e;
-        if (L->kind == TG_BINARY_Q1) {
-            if (G <= 32)
-                e = launch_m1<1, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-            else if (G <= 64)
-                e = launch_m1<2, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-            else
-                e = launch_m1<4, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-        } else {
-            if (G <= 32)
-                e = launch_m1<1, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-            else if (G <= 64)
-                e = launch_m1<2, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-            else
-                e = launch_m1<4, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-        }
-        if (e != cudaSuccess)
+    const bool q1 = L->kind == TG_BINARY_Q1;
+    if (M <= kFewMaxTokens && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax) {
+        if (launch_few((int)M, q1, masks, scales, x, y, N, G, tiles, (int)L->frac, pdl, s) != cudaSuccess)
             return TG_ERR_CUDA;
+    } else if (M == 1) {
+        return TG_ERR_SHAPE;
     } else if (M <= kDp4aMaxTokens) {
-        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, false,
-                               (int)L->frac, pdl, s);
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, q1, false, (int)L->frac, pdl, s);
     } else if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G)) {
         return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1,
                                  (int)L->frac, pdl, s);

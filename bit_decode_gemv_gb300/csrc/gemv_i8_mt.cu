@@ -22,6 +22,10 @@
 // planes up to the highest nonzero digit of the staged tokens are processed
 // (one plane for activations in int8 range, three for magnitudes below 2^23).
 //
+// tg_gemv_i8 sends this kernel every call with int64 activations, and int8
+// calls of two to four tokens whose activations do not fit the shared memory
+// of the few-token kernel in gemv_i8.cu (this one stages tokens in chunks).
+//
 // Mapping: one CTA per 32-row tile (lane l of every warp owns row 32T + l),
 // the CTA's warps split the groups GPW at a time with every mask load of a
 // batch issued before its compute, as in the batch-1 kernel. The tokens are

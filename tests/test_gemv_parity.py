@@ -254,18 +254,29 @@ def test_extreme_values_q1_and_floor(M):
     check_frac(dict(t=np.where(t > 0, 1, np.where(rng.random((N, K)) < 0.3, 0, -1)).astype(np.int8), d=d, x=x), 9)
 
 
-# Token counts on both sides of every kernel boundary of tg_gemv_i8 (the dp4a
-# kernel up to 4 tokens, the warp-MMA kernel up to 8, or 16 when K <= 4096 and
-# the activations' fragments fit, the tensor-memory kernel above), at K below
-# and above those limits, ternary and Q1_0, with and without the floor.
+# Token counts on both sides of every kernel boundary of tg_gemv_i8 (the
+# few-token kernel up to 4 tokens, with two groups per warp up to K = 8192 and
+# four above, the warp-MMA kernel up to 8, or 16 when K <= 4096 and the
+# activations' fragments fit, the tensor-memory kernel above), at K below and
+# above those limits, ternary and Q1_0, with and without the floor.
 @pytest.mark.parametrize("K", [640, 4608, 12800, 16384])
-@pytest.mark.parametrize("M", [2, 4, 5, 8, 9, 16, 17])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 8, 9, 16, 17])
 def test_every_token_count_path(M, K):
     N = 97 if K <= 4608 else 40
     check(W.batched(seed=M * K, M=M, N=N, K=K))
     check_frac(W.batched(seed=M * K + 1, M=M, N=N, K=K), 5)
     check_q1(W.ffn_up_q1(seed=M * K + 2, N=N, K=K, M=M))
     check_q1(W.ffn_up_q1(seed=M * K + 3, N=N, K=K, M=M), 11)
+
+
+# Two to four int8 tokens whose activations overflow the few-token kernel's
+# shared memory (M * K bytes above about 200 KB) go to the dp4a kernel, which
+# stages them in chunks; one token at the same K stays on the few-token kernel.
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_few_tokens_wide_rows(M):
+    K = 65536
+    check(W.batched(seed=M + 900, M=M, N=40, K=K))
+    check_q1(W.ffn_up_q1(seed=M + 901, N=40, K=K, M=M), 3)
 
 
 # The tensor-memory kernel gives a CTA one to four 32-row tiles, the fewest that
