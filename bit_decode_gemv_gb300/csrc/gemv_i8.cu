@@ -29,6 +29,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -92,11 +93,11 @@ __device__ __forceinline__ int group_pos_q1(const uint32_t w[4], const int8_t *x
     return pos;
 }
 
-// Several tokens (TB of them, activations TB rows of stride K apart in shared
+// Several tokens (TB of them, their activations `stride` bytes apart in shared
 // memory from xg). The masked words depend on the weights only, so each is
 // formed once and fed to every token's dp4a. Ternary: out[t] = sum (t_i + 2) x_i.
 template <int TB>
-__device__ __forceinline__ void group_dot_t2_tokens(const uint32_t w[8], const int8_t *xg, int K, int out[TB])
+__device__ __forceinline__ void group_dot_t2_tokens(const uint32_t w[8], const int8_t *xg, int stride, int out[TB])
 {
     int a[TB][4];
 #pragma unroll
@@ -110,7 +111,7 @@ __device__ __forceinline__ void group_dot_t2_tokens(const uint32_t w[8], const i
         const uint32_t c3 = and_xor(w[u], 0xC0C0C0C0u, 0x80808080u);
 #pragma unroll
         for (int t = 0; t < TB; t++) {
-            const uint4 xv = *reinterpret_cast<const uint4 *>(xg + t * K + 16 * u);
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xg + t * stride + 16 * u);
             a[t][0] = dp4a_us(c0, xv.x, a[t][0]);
             a[t][1] = dp4a_us(c1, xv.y, a[t][1]);
             a[t][2] = dp4a_us(c2, xv.z, a[t][2]);
@@ -126,7 +127,7 @@ __device__ __forceinline__ void group_dot_t2_tokens(const uint32_t w[8], const i
 // byte is moved down to bit 0 ((w >> j) & 0x01010101), so all eight columns of
 // a word accumulate into one sum per token without a shift back.
 template <int TB>
-__device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const int8_t *xg, int K, int out[TB])
+__device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const int8_t *xg, int stride, int out[TB])
 {
     int a[TB][2];
 #pragma unroll
@@ -140,8 +141,8 @@ __device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const i
             c[j] = (w[u] >> j) & 0x01010101u;
 #pragma unroll
         for (int t = 0; t < TB; t++) {
-            const uint4 lo = *reinterpret_cast<const uint4 *>(xg + t * K + 32 * u);
-            const uint4 hi = *reinterpret_cast<const uint4 *>(xg + t * K + 32 * u + 16);
+            const uint4 lo = *reinterpret_cast<const uint4 *>(xg + t * stride + 32 * u);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(xg + t * stride + 32 * u + 16);
             const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
             for (int j = 0; j < 8; j++)
@@ -152,6 +153,11 @@ __device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const i
     for (int t = 0; t < TB; t++)
         out[t] = a[t][0] + a[t][1];
 }
+
+// Where a CTA, launched as a programmatic dependent, lets the next kernel on
+// the stream launch: right after issuing its first weight loads, right after
+// its wait for the previous kernel, or once its activations are staged.
+constexpr int kTrigAfterLoads = 0, kTrigAfterWait = 1, kTrigAfterStage = 2;
 
 // ---------------------------------------------------------------------------
 // Batch 1 and a few tokens. One CTA per tile of 32 rows; lane l of every warp
@@ -174,7 +180,7 @@ __device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const i
 template <int GPW, bool kQ1, int MT>
 __global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
 gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
-                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac)
+                  const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac, int trigger)
 {
     constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
     constexpr int TB = MT < 4 ? MT : 4;      // tokens per pass over a group's masked words
@@ -209,8 +215,11 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         }
     };
     load_batch(warp);
-    tgi::pdl_launch_dependents();   // this CTA's first weights are in flight
+    if (trigger == kTrigAfterLoads)
+        tgi::pdl_launch_dependents();   // this CTA's first weights are in flight
     tgi::pdl_wait();
+    if (trigger == kTrigAfterWait)
+        tgi::pdl_launch_dependents();
 
     // Stage x and the per-group activation totals. With one group per warp each
     // warp stages only its own group's activations behind a warp barrier instead
@@ -245,6 +254,8 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         __syncthreads();
     }
 
+    if (trigger == kTrigAfterStage)
+        tgi::pdl_launch_dependents();
     int64_t acc[MT];
 #pragma unroll
     for (int t = 0; t < MT; t++)
@@ -311,14 +322,206 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
     }
 }
 
-// Kernel per token count (measured crossovers on GB300, ffn_up and batched
-// shapes): M = 1..kFewMaxTokens the kernel above; then the warp-MMA kernel
-// (gemv_i8_hmma.cu) for one token tile, or two when K is at most
-// kHmmaTwoTileMaxK; above that the tensor-memory kernel (gemv_i8_mma.cu), whose
-// cost hardly grows with M up to 64. The CUDA-core dp4a kernel (gemv_i8_mt.cu)
-// takes int64 activations at every M, and int8 ones at 2..kDp4aMaxTokens when
-// the activations do not fit the kernel above's shared memory (it stages the
-// tokens in chunks).
+// ---------------------------------------------------------------------------
+// Half-tile mapping of the same arithmetic. CTA c takes rows 16 (c & 1) ..
+// 16 (c & 1) + 15 of tile c >> 1 for all groups; lane l owns row 16 (c & 1) +
+// (l & 15), and its half of the warp, s = l >> 4, picks one group of a pair:
+// warp w takes the pairs p = w, w + W, ... and half s group 2p + s. A warp
+// instruction still covers 32 (row, group) lanes, but a CTA holds half as
+// many, so twice as many CTAs spread the same work more evenly over the SMs
+// (ffn_up: 432 CTAs of 10 warps, at most three per SM, instead of 216 of 20
+// with 64 SMs holding two: at most 30 warp-groups of arithmetic per SM after
+// the dependent-launch wait instead of 40). The two halves' sums of a row meet
+// by one shuffle, the warps' through shared memory. Staged activations take
+// kXStride bytes per group, so that the two groups a warp reads with one
+// broadcast load sit in different banks.
+// ---------------------------------------------------------------------------
+constexpr int kXStride = 144;
+
+template <int GPW, bool kQ1, int MT>
+__device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                                             const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G,
+                                             int frac, int trigger)
+{
+    constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
+    constexpr int TB = MT < 4 ? MT : 4;
+    static_assert(MT % TB == 0, "token count must be a multiple of the pass width");
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int K = G * 128;
+    const int XS = G * kXStride;   // staged bytes per token
+    int8_t *xs = reinterpret_cast<int8_t *>(smem);                                          // [MT][G][kXStride]
+    int *tsum = reinterpret_cast<int *>(smem + MT * XS);                                    // [MT][G]
+    int64_t *red = reinterpret_cast<int64_t *>(smem + MT * XS + ((MT * G * 4 + 15) & ~15));  // [W][MT][16]
+
+    const int tile = blockIdx.x >> 1;
+    const int half = (blockIdx.x & 1) * 16;
+    const int nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int side = lane >> 4, r16 = lane & 15;
+    const uint4 *tmask = masks + (size_t)tile * G * kChunks + half + r16;
+    const int32_t *tscale = scales + (size_t)tile * G * kTileRows + half + r16;
+
+    uint4 m0[GPW], m1[GPW];
+    int32_t dg[GPW];
+    auto load_batch = [&](int p0) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = 2 * (p0 + j * nwarps) + side;
+            if (g < G) {
+                m0[j] = tgi::ldg_stream(tmask + g * kChunks);
+                m1[j] = kQ1 ? make_uint4(0, 0, 0, 0) : tgi::ldg_stream(tmask + g * kChunks + 32);
+                dg[j] = __ldg(tscale + g * kTileRows);
+            } else {
+                m0[j] = m1[j] = make_uint4(0, 0, 0, 0);
+                dg[j] = 0;
+            }
+        }
+    };
+    load_batch(warp);
+    if (trigger == kTrigAfterLoads)
+        tgi::pdl_launch_dependents();   // this CTA's first weights are in flight
+    tgi::pdl_wait();
+    if (trigger == kTrigAfterWait)
+        tgi::pdl_launch_dependents();
+
+    if (GPW == 1) {
+        // warp w owns pair w: each half stages its group's 128 activations (8 bytes
+        // a lane) and their sum, behind a warp barrier only
+        const int g = 2 * warp + side;
+        uint2 v[MT];
+#pragma unroll
+        for (int t = 0; t < MT; t++)
+            v[t] = g < G ? __ldg(reinterpret_cast<const uint2 *>(x + t * K + g * 128) + r16) : make_uint2(0, 0);
+#pragma unroll
+        for (int t = 0; t < MT; t++) {
+            int s = tgi::byte_sum_s8(v[t].x) + tgi::byte_sum_s8(v[t].y);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, o);   // within the half
+            if (g < G) {
+                reinterpret_cast<uint2 *>(xs + t * XS + g * kXStride)[r16] = v[t];
+                if (r16 == 0)
+                    tsum[t * G + g] = s;
+            }
+        }
+        __syncwarp();
+    } else {
+        for (int i = threadIdx.x; i < MT * G * 8; i += blockDim.x) {
+            const int tg = i >> 3, c = i & 7;   // (token, group) tg = t * G + g, 16-byte chunk c
+            reinterpret_cast<uint4 *>(xs + (tg / G) * XS + (tg % G) * kXStride)[c] =
+                __ldg(reinterpret_cast<const uint4 *>(x + tg * 128) + c);
+        }
+        for (int tg = warp; tg < MT * G; tg += nwarps) {
+            const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(x + tg * 128) + lane);
+            const int s = tgi::warp_sum_i32(tgi::byte_sum_s8(v));
+            if (lane == 0)
+                tsum[tg] = s;
+        }
+        __syncthreads();
+    }
+
+    if (trigger == kTrigAfterStage)
+        tgi::pdl_launch_dependents();
+    int64_t acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; t++)
+        acc[t] = 0;
+    for (int p0 = warp;;) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = 2 * (p0 + j * nwarps) + side;
+            if (g < G) {
+                const int8_t *xg = xs + g * kXStride;
+                if constexpr (MT == 1) {
+                    int P;
+                    if (kQ1) {
+                        const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                        P = 2 * group_pos_q1(w, xg) - tsum[g];
+                    } else {
+                        const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                               m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                        P = group_dot_t2(w, xg) - 2 * tsum[g];
+                    }
+                    acc[0] += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
+                } else {
+#pragma unroll
+                    for (int t0 = 0; t0 < MT; t0 += TB) {
+                        int P[TB];
+                        if (kQ1) {
+                            const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                            group_pos_q1_tokens<TB>(w, xg + t0 * XS, XS, P);
+#pragma unroll
+                            for (int t = 0; t < TB; t++)
+                                P[t] = 2 * P[t] - tsum[(t0 + t) * G + g];
+                        } else {
+                            const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                                   m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                            group_dot_t2_tokens<TB>(w, xg + t0 * XS, XS, P);
+#pragma unroll
+                            for (int t = 0; t < TB; t++)
+                                P[t] -= 2 * tsum[(t0 + t) * G + g];
+                        }
+#pragma unroll
+                        for (int t = 0; t < TB; t++)
+                            acc[t0 + t] += ((int64_t)dg[j] * (int64_t)P[t]) >> frac;
+                    }
+                }
+            }
+        }
+        p0 += nwarps * GPW;
+        if (2 * p0 >= G)
+            break;
+        load_batch(p0);
+    }
+
+    // the two halves' sums of each row, then the warps'
+#pragma unroll
+    for (int t = 0; t < MT; t++) {
+        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
+        if (side == 0)
+            red[(warp * MT + t) * 16 + r16] = acc[t];
+    }
+    __syncthreads();
+    const int row = tile * kTileRows + half + r16;
+    if (lane < 16)
+        for (int t = warp; t < MT; t += nwarps) {
+            int64_t sum = 0;
+            for (int w = 0; w < nwarps; w++)
+                sum += red[(w * MT + t) * 16 + r16];
+            if (row < N)
+                y[(size_t)t * N + row] = sum;
+        }
+}
+
+template <int GPW, bool kQ1, int MT>
+__global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
+gemv_i8_half_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                    const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac, int trigger)
+{
+    gemv_i8_half<GPW, kQ1, MT>(masks, scales, x, y, N, G, frac, trigger);
+}
+
+// One token, one pair per warp: held to 32 registers a thread (two resident
+// 1024-thread CTAs), so that an SM holds its three CTAs of one call and three
+// of the next, launched as a programmatic dependent, at once (without the
+// minimum the compiler took 50).
+template <bool kQ1>
+__global__ void __launch_bounds__(1024, 2)
+gemv_i8_half1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                     const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac, int trigger)
+{
+    gemv_i8_half<1, kQ1, 1>(masks, scales, x, y, N, G, frac, trigger);
+}
+
+// Kernel per token count: M = 1..kFewMaxTokens the two kernels above (the
+// mapping, trigger position and resident-CTA cap from few_plan); then the
+// warp-MMA kernel (gemv_i8_hmma.cu) for one token tile, or two when K is at
+// most kHmmaTwoTileMaxK; above that the tensor-memory kernel (gemv_i8_mma.cu),
+// whose cost hardly grows with M up to 64. The CUDA-core dp4a kernel
+// (gemv_i8_mt.cu) takes int64 activations at every M, and int8 ones at
+// 2..kDp4aMaxTokens when the activations do not fit the shared memory of the
+// kernels above (it stages the tokens in chunks).
 constexpr int kFewMaxTokens = 4;
 constexpr int kDp4aMaxTokens = 4;
 constexpr int kHmmaMaxTokens = 16;
@@ -330,23 +533,38 @@ size_t m1_smem_bytes(int G, int warps, int MT)
     return (size_t)MT * G * 128 + (((size_t)MT * G * 4 + 15) & ~(size_t)15) + (size_t)warps * MT * 32 * 8;
 }
 
-template <int GPW, bool kQ1, int MT>
-cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
-                      int G, int tiles, int frac, bool pdl, cudaStream_t s)
+size_t half_smem_bytes(int G, int warps, int MT)
 {
-    auto kern = gemv_i8_m1_kernel<GPW, kQ1, MT>;
-    const int max_warps = GPW >= 4 ? 16 : 32;
-    int warps = (G + GPW - 1) / GPW;
-    if (warps > max_warps)
-        warps = max_warps;
-    const size_t smem = m1_smem_bytes(G, warps, MT);
+    return (size_t)MT * G * kXStride + (((size_t)MT * G * 4 + 15) & ~(size_t)15) + (size_t)warps * MT * 16 * 8;
+}
+
+// The launch of one of the kernels above: grid, warps, dynamic shared memory
+// (at least min_smem: a larger reservation caps the CTAs resident on an SM),
+// programmatic dependent launch when the weights are constant. A kernel's
+// dynamic shared-memory limit is raised to the device's opt-in maximum on its
+// first launch there (attr_set: one bit per device), not on every call.
+using FewKernel = void (*)(const uint4 *, const int32_t *, const int8_t *, int64_t *, int, int, int, int);
+
+cudaError_t launch_one(FewKernel kern, std::atomic<uint64_t> &attr_set, int smem_optin, int grid, int warps,
+                       size_t smem, size_t min_smem, const uint4 *masks, const int32_t *scales, const int8_t *x,
+                       int64_t *y, int N, int G, int frac, int trigger, bool pdl, cudaStream_t s)
+{
+    if (smem < min_smem)
+        smem = min_smem;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess)
+            return cudaErrorInvalidDevice;
+        const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;   // (devices past 64: set every call)
+        if (!(attr_set.load(std::memory_order_acquire) & bit)) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+            if (e != cudaSuccess)
+                return e;
+            attr_set.fetch_or(bit, std::memory_order_acq_rel);
+        }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(warps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -355,48 +573,164 @@ cudaError_t launch_m1(const uint4 *masks, const int32_t *scales, const int8_t *x
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, frac);
+    return cudaLaunchKernelEx(&cfg, kern, masks, scales, x, y, N, G, frac, trigger);
 }
 
-// One token: one group per warp up to K = 4096 (32 warps), then two per warp up
-// to K = 8192; beyond that 16 warps loop over batches of four groups each.
-// Several tokens: two groups per warp up to K = 8192. (Measured per call with
-// constant weights, M = 2 / 3 / 4: on ffn_up (G = 20) one group per warp took
-// 3.20 / 3.79 / 4.38 us and two 3.40 / 3.60 / 4.06 us; on 13824 x 5120
-// (G = 40) two per warp over 20 warps 7.9 / 10.1 / 12.1 us and four per warp
-// over 10 warps 7.9 / 10.7 / 13.5 us. Registers: one token's one-group warps
-// take 32, several tokens' about 64, which leaves fewer CTAs resident.)
+struct FewLaunch {
+    int smem_optin;   // the device's opt-in shared memory per CTA
+    const uint4 *masks;
+    const int32_t *scales;
+    const int8_t *x;
+    int64_t *y;
+    int N, G, tiles, frac, trigger;
+    size_t min_smem;
+    bool pdl;
+    cudaStream_t s;
+};
+
+template <int GPW, bool kQ1, int MT>
+cudaError_t launch_whole(const FewLaunch &l)
+{
+    const int max_warps = GPW >= 4 ? 16 : 32;
+    const int warps = min((l.G + GPW - 1) / GPW, max_warps);
+    static std::atomic<uint64_t> attr_set{0};
+    return launch_one(gemv_i8_m1_kernel<GPW, kQ1, MT>, attr_set, l.smem_optin, l.tiles, warps,
+                      m1_smem_bytes(l.G, warps, MT), l.min_smem, l.masks, l.scales, l.x, l.y, l.N, l.G, l.frac,
+                      l.trigger, l.pdl, l.s);
+}
+
+template <int GPW, bool kQ1, int MT>
+cudaError_t launch_half(const FewLaunch &l)
+{
+    FewKernel kern;
+    if constexpr (GPW == 1 && MT == 1)
+        kern = gemv_i8_half1_kernel<kQ1>;
+    else
+        kern = gemv_i8_half_kernel<GPW, kQ1, MT>;
+    const int max_warps = GPW >= 4 ? 16 : 32;
+    const int warps = min(((l.G + 1) / 2 + GPW - 1) / GPW, max_warps);
+    static std::atomic<uint64_t> attr_set{0};
+    return launch_one(kern, attr_set, l.smem_optin, 2 * l.tiles, warps, half_smem_bytes(l.G, warps, MT), l.min_smem,
+                      l.masks, l.scales, l.x, l.y, l.N, l.G, l.frac, l.trigger, l.pdl, l.s);
+}
+
+// Groups per warp. Whole tiles, one token: one group per warp up to K = 4096
+// (32 warps), then two up to K = 8192; several tokens: two up to K = 8192
+// (measured faster than one on ffn_up at M = 3, 4 and on 13824 x 5120); beyond
+// that 16 warps loop over batches of four. Half tiles (a warp covers a pair of
+// groups): one pair per warp up to K = 8192, two up to K = 16384, then four.
 template <int MT, bool kQ1>
-cudaError_t launch_tokens(const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y, int N,
-                          int G, int tiles, int frac, bool pdl, cudaStream_t s)
+cudaError_t launch_tokens(bool half, const FewLaunch &l)
 {
-    if constexpr (MT == 1) {
-        if (G <= 32)
-            return launch_m1<1, kQ1, 1>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    if (half) {
+        if (l.G <= 64)
+            return launch_half<1, kQ1, MT>(l);
+        if (l.G <= 128)
+            return launch_half<2, kQ1, MT>(l);
+        return launch_half<4, kQ1, MT>(l);
     }
-    if (G <= 64)
-        return launch_m1<2, kQ1, MT>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-    return launch_m1<4, kQ1, MT>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    if constexpr (MT == 1) {
+        if (l.G <= 32)
+            return launch_whole<1, kQ1, 1>(l);
+    }
+    if (l.G <= 64)
+        return launch_whole<2, kQ1, MT>(l);
+    return launch_whole<4, kQ1, MT>(l);
 }
 
-template <int MT>
-cudaError_t launch_tokens(bool q1, const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y,
-                          int N, int G, int tiles, int frac, bool pdl, cudaStream_t s)
-{
-    return q1 ? launch_tokens<MT, true>(masks, scales, x, y, N, G, tiles, frac, pdl, s)
-              : launch_tokens<MT, false>(masks, scales, x, y, N, G, tiles, frac, pdl, s);
-}
-
-cudaError_t launch_few(int M, bool q1, const uint4 *masks, const int32_t *scales, const int8_t *x, int64_t *y,
-                       int N, int G, int tiles, int frac, bool pdl, cudaStream_t s)
+template <bool kQ1>
+cudaError_t launch_few(int M, bool half, const FewLaunch &l)
 {
     static_assert(kFewMaxTokens == 4, "one instance per token count");
     switch (M) {
-    case 1: return launch_tokens<1>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
-    case 2: return launch_tokens<2>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
-    case 3: return launch_tokens<3>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
-    default: return launch_tokens<4>(q1, masks, scales, x, y, N, G, tiles, frac, pdl, s);
+    case 1: return launch_tokens<1, kQ1>(half, l);
+    case 2: return launch_tokens<2, kQ1>(half, l);
+    case 3: return launch_tokens<3, kQ1>(half, l);
+    default: return launch_tokens<4, kQ1>(half, l);
     }
+}
+
+// The device's SM count and shared memory per SM (and per CTA reserved by the
+// system), looked up once per device.
+struct DeviceShape {
+    int nsm, smem_sm, smem_reserved, smem_optin;
+};
+
+bool device_shape(DeviceShape &d)
+{
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices][4];
+    static std::atomic<bool> have[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    if (dev >= 0 && dev < kMaxDevices && have[dev].load(std::memory_order_acquire)) {
+        d = {cache[dev][0].load(std::memory_order_relaxed), cache[dev][1].load(std::memory_order_relaxed),
+             cache[dev][2].load(std::memory_order_relaxed), cache[dev][3].load(std::memory_order_relaxed)};
+        return true;
+    }
+    if (cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return false;
+    if (dev >= 0 && dev < kMaxDevices) {
+        cache[dev][0].store(d.nsm, std::memory_order_relaxed);
+        cache[dev][1].store(d.smem_sm, std::memory_order_relaxed);
+        cache[dev][2].store(d.smem_reserved, std::memory_order_relaxed);
+        cache[dev][3].store(d.smem_optin, std::memory_order_relaxed);
+        have[dev].store(true, std::memory_order_release);
+    }
+    return true;
+}
+
+// Launch plan of the one-to-four-token kernels: whole or half tiles, where a
+// CTA lets the next call launch, and at most how many CTAs an SM holds (0 = no
+// cap). Chosen from a sweep of per-call times with constant weights, back to
+// back (N x K = 2560 x 2560, 2560 x 6912, 6912 x 2560, 5120 x 5120,
+// 13824 x 5120, 32000 x 2560; M = 1..4), where each rule below was within a
+// few percent of the fastest of 2 mappings x 3 trigger positions x 5 caps:
+//   - one token, one group per warp (K <= 4096): whole tiles, next call
+//     launched after the wait; when a call has at most two tiles per SM, at
+//     most two CTAs per SM (ffn_up 2.13 -> 1.80 us, 2560 x 2560 1.85 -> 1.46):
+//     fewer calls then prefetch weights at once, which otherwise delays the
+//     running call's activation reads, output writes and completion;
+//   - one token, longer rows: half tiles (5120 x 5120 3.77 -> 2.68 us,
+//     13824 x 5120 6.38 -> 5.03);
+//   - several tokens: half tiles when K <= 4096 and a call has at most two
+//     tiles per SM, else whole tiles, the next call launched once the
+//     activations are staged (13824 x 5120 at M = 4: 12.1 -> 11.1 us,
+//     2560 x 2560 at M = 4: 4.7 -> 2.6).
+struct FewPlan {
+    bool half;
+    int trigger;
+    int cap;
+};
+
+FewPlan few_plan(int M, int G, int tiles, int nsm)
+{
+    const bool few_tiles = tiles <= 2 * nsm;
+    if (M == 1) {
+        if (G <= 32)
+            return {false, kTrigAfterWait, few_tiles ? 2 : 0};
+        return {true, kTrigAfterLoads, 0};
+    }
+    if (G <= 32 && few_tiles)
+        return {true, kTrigAfterStage, 0};
+    return {false, kTrigAfterStage, 0};
+}
+
+// Dynamic shared memory that holds an SM to `cap` resident CTAs: the smallest
+// reservation above a (cap + 1)-th share of the SM's shared memory, plus a
+// third of the range that still fits cap of them (measured: on ffn_up at one
+// token 89.8 KB, in the range 76.8..115.7 KB, gave 1.79 us and 104 KB 1.86).
+size_t cap_smem(const DeviceShape &d, int cap)
+{
+    if (cap <= 0)
+        return 0;
+    const size_t lo = (size_t)d.smem_sm / (cap + 1) - d.smem_reserved + 1;   // cap + 1 no longer fit
+    const size_t hi = (size_t)d.smem_sm / cap - d.smem_reserved;             // cap still fit
+    return lo + (hi - lo) / 3;
 }
 
 }  // namespace
@@ -434,7 +768,16 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
 
     const bool q1 = L->kind == TG_BINARY_Q1;
     if (M <= kFewMaxTokens && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax) {
-        if (launch_few((int)M, q1, masks, scales, x, y, N, G, tiles, (int)L->frac, pdl, s) != cudaSuccess)
+        DeviceShape d;
+        if (!device_shape(d))
+            return TG_ERR_CUDA;
+        FewPlan plan = few_plan((int)M, G, tiles, d.nsm);
+        if (plan.half && half_smem_bytes(G, 32, (int)M) > kM1SmemMax)
+            plan = {false, kTrigAfterLoads, 0};
+        const FewLaunch l = {d.smem_optin, masks, scales, x, y, N, G, tiles, (int)L->frac, plan.trigger,
+                             cap_smem(d, plan.cap), pdl, s};
+        const cudaError_t e = q1 ? launch_few<true>((int)M, plan.half, l) : launch_few<false>((int)M, plan.half, l);
+        if (e != cudaSuccess)
             return TG_ERR_CUDA;
     } else if (M == 1) {
         return TG_ERR_SHAPE;
