@@ -154,6 +154,72 @@ __device__ __forceinline__ void group_pos_q1_tokens(const uint32_t w[4], const i
         out[t] = a[t][0] + a[t][1];
 }
 
+// A thread's int64 row sums of MT tokens: in registers up to four tokens; above
+// that in the thread's own shared-memory slots (32 apart), where eight tokens'
+// sums held in registers spilled (and sums in shared memory were slower at
+// four tokens: 13824 x 5120 at M = 4, 11.1 -> 13.3 us).
+template <int MT, bool kInSmem = (MT > 4)>
+struct RowSums {
+    int64_t v[MT];
+    __device__ __forceinline__ void init(int64_t *)
+    {
+#pragma unroll
+        for (int t = 0; t < MT; t++)
+            v[t] = 0;
+    }
+    __device__ __forceinline__ void add(int t, int64_t a) { v[t] += a; }
+    __device__ __forceinline__ void store(int64_t *slot)
+    {
+#pragma unroll
+        for (int t = 0; t < MT; t++)
+            slot[32 * t] = v[t];
+    }
+};
+
+template <int MT>
+struct RowSums<MT, true> {
+    int64_t *p;
+    __device__ __forceinline__ void init(int64_t *slot)
+    {
+        p = slot;
+#pragma unroll
+        for (int t = 0; t < MT; t++)
+            p[32 * t] = 0;
+    }
+    __device__ __forceinline__ void add(int t, int64_t a) { p[32 * t] += a; }
+    __device__ __forceinline__ void store(int64_t *) {}
+};
+
+// One group of one row for tokens T0..MT-1 in passes of up to four: P of each
+// token from the masked words (formed once per pass), minus the block-total
+// term, scaled by d, floored by 2^frac and added to the token's int64 sum.
+// tsum_g[t * G] is token t's activation sum over the group.
+template <int MT, int T0, bool kQ1>
+__device__ __forceinline__ void tokens_pass(const uint4 &m0, const uint4 &m1, int32_t d, const int8_t *xg, int stride,
+                                            const int *tsum_g, int G, int frac, RowSums<MT> &acc)
+{
+    constexpr int TB = MT - T0 < 4 ? MT - T0 : 4;
+    int P[TB];
+    if constexpr (kQ1) {
+        const uint32_t w[4] = {m0.x, m0.y, m0.z, m0.w};
+        group_pos_q1_tokens<TB>(w, xg + T0 * stride, stride, P);
+#pragma unroll
+        for (int t = 0; t < TB; t++)
+            P[t] = 2 * P[t] - tsum_g[(T0 + t) * G];   // 2 * pos_sum - block_total
+    } else {
+        const uint32_t w[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        group_dot_t2_tokens<TB>(w, xg + T0 * stride, stride, P);
+#pragma unroll
+        for (int t = 0; t < TB; t++)
+            P[t] -= 2 * tsum_g[(T0 + t) * G];
+    }
+#pragma unroll
+    for (int t = 0; t < TB; t++)
+        acc.add(T0 + t, ((int64_t)d * (int64_t)P[t]) >> frac);   // the group's floor (arithmetic shift)
+    if constexpr (T0 + TB < MT)
+        tokens_pass<MT, T0 + TB, kQ1>(m0, m1, d, xg, stride, tsum_g, G, frac, acc);
+}
+
 // Where a CTA, launched as a programmatic dependent, lets the next kernel on
 // the stream launch: right after issuing its first weight loads, right after
 // its wait for the previous kernel, or once its activations are staged.
@@ -175,7 +241,8 @@ constexpr int kTrigAfterLoads = 0, kTrigAfterWait = 1, kTrigAfterStage = 2;
 //
 // MT tokens (1..kFewMaxTokens): the weights are read once; each thread keeps MT
 // int64 row sums, and with MT > 1 a group's masked words are formed once per
-// word and fed to every token (group_dot_t2_tokens), four tokens at a time.
+// word and fed to every token (group_dot_t2_tokens), four tokens at a time,
+// and each thread's per-token int64 sums live in its own shared-memory slots.
 // ---------------------------------------------------------------------------
 template <int GPW, bool kQ1, int MT>
 __global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
@@ -183,8 +250,6 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
                   const int8_t *__restrict__ x, int64_t *__restrict__ y, int N, int G, int frac, int trigger)
 {
     constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
-    constexpr int TB = MT < 4 ? MT : 4;      // tokens per pass over a group's masked words
-    static_assert(MT % TB == 0, "token count must be a multiple of the pass width");
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = G * 128;
     int8_t *xs = reinterpret_cast<int8_t *>(smem);                                        // [MT][K]
@@ -256,10 +321,13 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
 
     if (trigger == kTrigAfterStage)
         tgi::pdl_launch_dependents();
-    int64_t acc[MT];
-#pragma unroll
-    for (int t = 0; t < MT; t++)
-        acc[t] = 0;
+    // one token: the row sum in a register; several: RowSums (this thread's
+    // slots of red, token t at [32 t], at the end or throughout)
+    int64_t acc = 0;
+    int64_t *const slot = red + warp * MT * 32 + lane;
+    RowSums<MT> sums;
+    if (MT > 1)
+        sums.init(slot);
     for (int g0 = warp;;) {
 #pragma unroll
         for (int j = 0; j < GPW; j++) {
@@ -276,29 +344,9 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
                                                m1[j].x, m1[j].y, m1[j].z, m1[j].w};
                         P = group_dot_t2(w, xs + g * 128) - 2 * tsum[g];
                     }
-                    acc[0] += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
+                    acc += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
                 } else {
-#pragma unroll
-                    for (int t0 = 0; t0 < MT; t0 += TB) {
-                        int P[TB];
-                        if (kQ1) {
-                            const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
-                            group_pos_q1_tokens<TB>(w, xs + t0 * K + g * 128, K, P);
-#pragma unroll
-                            for (int t = 0; t < TB; t++)
-                                P[t] = 2 * P[t] - tsum[(t0 + t) * G + g];
-                        } else {
-                            const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
-                                                   m1[j].x, m1[j].y, m1[j].z, m1[j].w};
-                            group_dot_t2_tokens<TB>(w, xs + t0 * K + g * 128, K, P);
-#pragma unroll
-                            for (int t = 0; t < TB; t++)
-                                P[t] -= 2 * tsum[(t0 + t) * G + g];
-                        }
-#pragma unroll
-                        for (int t = 0; t < TB; t++)
-                            acc[t0 + t] += ((int64_t)dg[j] * (int64_t)P[t]) >> frac;
-                    }
+                    tokens_pass<MT, 0, kQ1>(m0[j], m1[j], dg[j], xs + g * 128, K, tsum + g, G, frac, sums);
                 }
             }
         }
@@ -308,9 +356,10 @@ gemv_i8_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ s
         load_batch(g0);
     }
 
-#pragma unroll
-    for (int t = 0; t < MT; t++)
-        red[(warp * MT + t) * 32 + lane] = acc[t];
+    if (MT == 1)
+        red[warp * 32 + lane] = acc;
+    else
+        sums.store(slot);
     __syncthreads();
     const int row = tile * kTileRows + lane;
     for (int t = warp; t < MT; t += nwarps) {
@@ -344,14 +393,12 @@ __device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, co
                                              int frac, int trigger)
 {
     constexpr int kChunks = kQ1 ? 32 : 64;   // uint4 per (tile, group): one or two per row
-    constexpr int TB = MT < 4 ? MT : 4;
-    static_assert(MT % TB == 0, "token count must be a multiple of the pass width");
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = G * 128;
     const int XS = G * kXStride;   // staged bytes per token
     int8_t *xs = reinterpret_cast<int8_t *>(smem);                                          // [MT][G][kXStride]
     int *tsum = reinterpret_cast<int *>(smem + MT * XS);                                    // [MT][G]
-    int64_t *red = reinterpret_cast<int64_t *>(smem + MT * XS + ((MT * G * 4 + 15) & ~15));  // [W][MT][16]
+    int64_t *red = reinterpret_cast<int64_t *>(smem + MT * XS + ((MT * G * 4 + 15) & ~15));  // [W][MT][32]
 
     const int tile = blockIdx.x >> 1;
     const int half = (blockIdx.x & 1) * 16;
@@ -423,10 +470,13 @@ __device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, co
 
     if (trigger == kTrigAfterStage)
         tgi::pdl_launch_dependents();
-    int64_t acc[MT];
-#pragma unroll
-    for (int t = 0; t < MT; t++)
-        acc[t] = 0;
+    // one token: the row sum in a register; several: RowSums (this thread's
+    // slots of red, [W][MT][32]: both halves of the warp, summed at the end)
+    int64_t acc = 0;
+    int64_t *const slot = red + warp * MT * 32 + lane;
+    RowSums<MT> sums;
+    if (MT > 1)
+        sums.init(slot);
     for (int p0 = warp;;) {
 #pragma unroll
         for (int j = 0; j < GPW; j++) {
@@ -443,29 +493,9 @@ __device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, co
                                                m1[j].x, m1[j].y, m1[j].z, m1[j].w};
                         P = group_dot_t2(w, xg) - 2 * tsum[g];
                     }
-                    acc[0] += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
+                    acc += ((int64_t)dg[j] * (int64_t)P) >> frac;   // the group's floor (arithmetic shift)
                 } else {
-#pragma unroll
-                    for (int t0 = 0; t0 < MT; t0 += TB) {
-                        int P[TB];
-                        if (kQ1) {
-                            const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
-                            group_pos_q1_tokens<TB>(w, xg + t0 * XS, XS, P);
-#pragma unroll
-                            for (int t = 0; t < TB; t++)
-                                P[t] = 2 * P[t] - tsum[(t0 + t) * G + g];
-                        } else {
-                            const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
-                                                   m1[j].x, m1[j].y, m1[j].z, m1[j].w};
-                            group_dot_t2_tokens<TB>(w, xg + t0 * XS, XS, P);
-#pragma unroll
-                            for (int t = 0; t < TB; t++)
-                                P[t] -= 2 * tsum[(t0 + t) * G + g];
-                        }
-#pragma unroll
-                        for (int t = 0; t < TB; t++)
-                            acc[t0 + t] += ((int64_t)dg[j] * (int64_t)P[t]) >> frac;
-                    }
+                    tokens_pass<MT, 0, kQ1>(m0[j], m1[j], dg[j], xg, XS, tsum + g, G, frac, sums);
                 }
             }
         }
@@ -476,11 +506,12 @@ __device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, co
     }
 
     // the two halves' sums of each row, then the warps'
-#pragma unroll
-    for (int t = 0; t < MT; t++) {
-        acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
+    if (MT == 1) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
         if (side == 0)
-            red[(warp * MT + t) * 16 + r16] = acc[t];
+            red[warp * 32 + r16] = acc;
+    } else {
+        sums.store(slot);
     }
     __syncthreads();
     const int row = tile * kTileRows + half + r16;
@@ -488,7 +519,7 @@ __device__ __forceinline__ void gemv_i8_half(const uint4 *__restrict__ masks, co
         for (int t = warp; t < MT; t += nwarps) {
             int64_t sum = 0;
             for (int w = 0; w < nwarps; w++)
-                sum += red[(w * MT + t) * 16 + r16];
+                sum += MT == 1 ? red[w * 32 + r16] : red[(w * MT + t) * 32 + r16] + red[(w * MT + t) * 32 + 16 + r16];
             if (row < N)
                 y[(size_t)t * N + row] = sum;
         }
@@ -522,7 +553,7 @@ gemv_i8_half1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict_
 // (gemv_i8_mt.cu) takes int64 activations at every M, and int8 ones at
 // 2..kDp4aMaxTokens when the activations do not fit the shared memory of the
 // kernels above (it stages the tokens in chunks).
-constexpr int kFewMaxTokens = 4;
+constexpr int kFewMaxTokens = 8;
 constexpr int kDp4aMaxTokens = 4;
 constexpr int kHmmaMaxTokens = 16;
 constexpr int kHmmaTwoTileMaxK = 4096;
@@ -535,7 +566,7 @@ size_t m1_smem_bytes(int G, int warps, int MT)
 
 size_t half_smem_bytes(int G, int warps, int MT)
 {
-    return (size_t)MT * G * kXStride + (((size_t)MT * G * 4 + 15) & ~(size_t)15) + (size_t)warps * MT * 16 * 8;
+    return (size_t)MT * G * kXStride + (((size_t)MT * G * 4 + 15) & ~(size_t)15) + (size_t)warps * MT * 32 * 8;
 }
 
 // The launch of one of the kernels above: grid, warps, dynamic shared memory
@@ -641,12 +672,16 @@ cudaError_t launch_tokens(bool half, const FewLaunch &l)
 template <bool kQ1>
 cudaError_t launch_few(int M, bool half, const FewLaunch &l)
 {
-    static_assert(kFewMaxTokens == 4, "one instance per token count");
+    static_assert(kFewMaxTokens == 8, "one instance per token count");
     switch (M) {
     case 1: return launch_tokens<1, kQ1>(half, l);
     case 2: return launch_tokens<2, kQ1>(half, l);
     case 3: return launch_tokens<3, kQ1>(half, l);
-    default: return launch_tokens<4, kQ1>(half, l);
+    case 4: return launch_tokens<4, kQ1>(half, l);
+    case 5: return launch_tokens<5, kQ1>(half, l);
+    case 6: return launch_tokens<6, kQ1>(half, l);
+    case 7: return launch_tokens<7, kQ1>(half, l);
+    default: return launch_tokens<8, kQ1>(half, l);
     }
 }
 
@@ -694,7 +729,8 @@ bool device_shape(DeviceShape &d)
 //     launched after the wait; when a call has at most two tiles per SM, at
 //     most two CTAs per SM (ffn_up 2.13 -> 1.80 us, 2560 x 2560 1.85 -> 1.46):
 //     fewer calls then prefetch weights at once, which otherwise delays the
-//     running call's activation reads, output writes and completion;
+//     running call's activation reads, output writes and completion (one
+//     group per warp beat two on every one-token shape measured);
 //   - one token, longer rows: half tiles (5120 x 5120 3.77 -> 2.68 us,
 //     13824 x 5120 6.38 -> 5.03);
 //   - several tokens: half tiles when K <= 4096 and a call has at most two
@@ -711,13 +747,35 @@ FewPlan few_plan(int M, int G, int tiles, int nsm)
 {
     const bool few_tiles = tiles <= 2 * nsm;
     if (M == 1) {
-        if (G <= 32)
-            return {false, kTrigAfterWait, few_tiles ? 2 : 0};
+        if (G <= 32) {
+            // whole tiles of G warps: threads alone hold an SM to 64 / G CTAs;
+            // where that is three or fewer, reserving shared memory for exactly
+            // that many (no fewer CTAs, a larger shared-memory carveout) was
+            // faster too (32000 x 2560: 5.76 -> 5.55 us)
+            const int by_threads = 64 / G;
+            return {false, kTrigAfterWait, few_tiles ? 2 : by_threads <= 3 ? by_threads : 0};
+        }
         return {true, kTrigAfterLoads, 0};
     }
     if (G <= 32 && few_tiles)
         return {true, kTrigAfterStage, 0};
     return {false, kTrigAfterStage, 0};
+}
+
+// Whether M tokens go to the few-token kernels rather than the warp-MMA one:
+// up to six always (per call on 2560 x 2560 / 6912 x 2560 / 13824 x 5120 /
+// 32000 x 2560 at M = 5: 3.37 / 4.46 / 14.0 / 14.5 us against 6.02 / 6.22 /
+// 18.0 / 20.8); seven or eight where a call has at most one tile per SM, or
+// K <= 4096 and at most two (at M = 8: 2560 x 6912 9.4 against 13.5 us, 6912 x
+// 2560 6.2 against 6.3; with more tiles the warp-MMA kernel was faster:
+// 5120 x 5120 10.9 against 13.9, 13824 x 5120 18.4 against 21.3).
+bool few_takes(int M, int G, int tiles, int nsm)
+{
+    if (M > kFewMaxTokens)
+        return false;
+    if (M <= 6)
+        return true;
+    return tiles <= nsm || (G <= 32 && tiles <= 2 * nsm);
 }
 
 // Dynamic shared memory that holds an SM to `cap` resident CTAs: the smallest
@@ -767,10 +825,10 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
                                (int)L->frac, pdl, s);
 
     const bool q1 = L->kind == TG_BINARY_Q1;
-    if (M <= kFewMaxTokens && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax) {
-        DeviceShape d;
-        if (!device_shape(d))
-            return TG_ERR_CUDA;
+    DeviceShape d;
+    if (!device_shape(d))
+        return TG_ERR_CUDA;
+    if (few_takes((int)M, G, tiles, d.nsm) && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax) {
         FewPlan plan = few_plan((int)M, G, tiles, d.nsm);
         if (plan.half && half_smem_bytes(G, 32, (int)M) > kM1SmemMax)
             plan = {false, kTrigAfterLoads, 0};

@@ -122,9 +122,8 @@ gemv_i8_hmma_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__
     }
         TG_HMMA_LOAD_GROUP(warp >> 1)
         if (m0 == 0) {
-            // launched as a programmatic dependent (constant weights): the next
-            // kernel may start now; x and y are touched only after the wait
-            tgi::pdl_launch_dependents();
+            // launched as a programmatic dependent (constant weights): x and y
+            // are touched only after the wait for the previous kernel
             tgi::pdl_wait();
         }
         // the chunk's activations as fp16 rows (rows past M are zero): eight
@@ -157,6 +156,12 @@ gemv_i8_hmma_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__
         for (int i = threadIdx.x; i < 32 * 8 * NT; i += blockDim.x)
             ysum[i] = 0ull;
         __syncthreads();
+        // the next kernel may launch once this CTA's activations are staged
+        // (measured against releasing it right after the first weight loads:
+        // 2560 x 2560 at M = 5 / 12: 6.24 / 9.59 -> 5.13 / 7.09 us per call,
+        // the larger shapes within 1 %): fewer calls in flight at once
+        if (m0 == 0)
+            tgi::pdl_launch_dependents();
 
         int64_t acc[NT][4];
 #pragma unroll

@@ -255,18 +255,38 @@ def test_extreme_values_q1_and_floor(M):
 
 
 # Token counts on both sides of every kernel boundary of tg_gemv_i8 (the
-# few-token kernel up to 4 tokens, with two groups per warp up to K = 8192 and
-# four above, the warp-MMA kernel up to 8, or 16 when K <= 4096 and the
-# activations' fragments fit, the tensor-memory kernel above), at K below and
-# above those limits, ternary and Q1_0, with and without the floor.
+# few-token kernels up to 8 tokens on these row counts -- sums in registers up
+# to 4, in shared memory above; two groups per warp up to K = 8192 and four
+# above -- the warp-MMA kernel up to 16 when K <= 4096 and the activations'
+# fragments fit, the tensor-memory kernel above), at K below and above those
+# limits, ternary and Q1_0, with and without the floor.
 @pytest.mark.parametrize("K", [640, 4608, 12800, 16384])
-@pytest.mark.parametrize("M", [2, 3, 4, 5, 8, 9, 16, 17])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8, 9, 16, 17])
 def test_every_token_count_path(M, K):
     N = 97 if K <= 4608 else 40
     check(W.batched(seed=M * K, M=M, N=N, K=K))
     check_frac(W.batched(seed=M * K + 1, M=M, N=N, K=K), 5)
     check_q1(W.ffn_up_q1(seed=M * K + 2, N=N, K=K, M=M))
     check_q1(W.ffn_up_q1(seed=M * K + 3, N=N, K=K, M=M), 11)
+
+
+# One token on more 32-row tiles than twice the SM count (32000 rows: 1000
+# tiles), the launch that reserves shared memory at the thread-limited CTA
+# count, and on at most twice the SM count (the two-CTA cap), ternary and Q1_0.
+@pytest.mark.parametrize("N", [32000, 4000])
+def test_one_token_launch_plans(N):
+    check(W.batched(seed=N, M=1, N=N, K=2560))
+    check_q1(W.ffn_up_q1(seed=N + 1, N=N, K=2560, M=1), 2)
+
+
+# Seven and eight tokens on more tiles than SMs with K > 4096 (and more than
+# twice as many with K <= 4096) go to the warp-MMA kernel; five and six stay on
+# the few-token kernels.
+@pytest.mark.parametrize("M", [5, 7, 8])
+@pytest.mark.parametrize("N,K", [(5000, 4608), (10000, 1024)])
+def test_seven_eight_tokens_on_many_tiles(M, N, K):
+    check(W.batched(seed=M + N, M=M, N=N, K=K))
+    check_q1(W.ffn_up_q1(seed=M + N + 1, N=N, K=K, M=M), 1)
 
 
 # Two to four int8 tokens whose activations overflow the few-token kernel's
