@@ -4,12 +4,12 @@
 //   y[m][r] = sum_g d[r][g] * P[m][r][g],   P[m][r][g] = sum_{i in g} t[r][i] * x[m][i]
 //
 // Exactness. t is -1/0/+1 and x an int8, both exact fp16 values. The tensor
-// core sums one group at a time in fp32 into an accumulator that starts at
-// 1.5 * 2^23 (the D buffer is filled with that value before the group's first
-// step); a group's sum has |P| <= 128 * 128 = 2^14, so every partial sum is an
-// integer in (2^23, 2^24), where consecutive fp32 values are exactly 1 apart:
-// nothing is rounded and the accumulator's bit pattern is 0x4B400000 + P. The
-// epilogue multiplies that bit pattern by d[r][g] into a wrapping 64-bit
+// core sums one group at a time in fp32 (the group's first K step overwrites
+// the accumulator); a group's sum has |P| <= 128 * 128 = 2^14, so every
+// partial sum is an integer of magnitude at most 2^14, exact in fp32, and so is
+// P + 1.5 * 2^23, which the epilogue forms with one fp32 add: an integer in
+// (2^23, 2^24), where consecutive fp32 values are exactly 1 apart, with the bit
+// pattern 0x4B400000 + P. The epilogue multiplies that bit pattern by d[r][g] into a wrapping 64-bit
 // accumulator per token and at the end subtracts 0x4B400000 * sum_g d[r][g];
 // the result is exact modulo 2^64 and therefore exact, since y fits in int64
 // (checked on the host).
@@ -30,10 +30,10 @@
 //     P%2 in shared memory, in the canonical K-major layout of 8-row x 16-byte
 //     core matrices, and arrives on the slot's "full" barrier; then it reads
 //     back pair P-1's D buffer for tokens 16p..16p+15 (those MMAs ran while
-//     pair P was prepared), accumulates it, and refills the buffer with the
-//     offset for pair P+1. The compute warps issue no global loads at all.
+//     pair P was prepared) and accumulates it. The compute warps issue no
+//     global loads at all.
 //   - MMA warp w takes the pairs P = w mod 2, with A/B slot w and D buffer w.
-//     When the slot is full and the buffer refilled, one thread issues the
+//     When the slot is full and the buffer read back, one thread issues the
 //     sixteen K=16 steps of the pair and commits them to the slot's "empty" and
 //     the buffer's "full" barriers.
 //   - A copy warp fills a 3-deep ring of input stages with bulk and tensor
@@ -77,7 +77,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;                       // A slots: 128 columns each (2 x 128 fp16 of K per row)
 constexpr uint32_t kColD = 128 * kSlots;            // D buffers: 2 x kMaxN columns each
 static_assert(kColD + kDBufs * kPair * kMaxN <= kTmemCols, "tensor memory plan");
-static_assert(kMaxN == 64, "each compute warp reads and refills 16 D columns of each group");
+static_assert(kMaxN == 64, "each compute warp reads 16 D columns of each group");
 static_assert(kSlots == kMmaWarps && kDBufs == kMmaWarps, "MMA warp w owns A/B slot w and D buffer w");
 constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^23
 
@@ -146,16 +146,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         "%13, %14, %15, %16};"
         ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
-
-// 32 lanes x 16 columns, every column of thread i's lane set to v.
-__device__ __forceinline__ void tmem_st16_same(uint32_t taddr, uint32_t v)
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
-        "%1, %1};"
-        ::"r"(taddr), "r"(v)
         : "memory");
 }
 
@@ -438,7 +428,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             for (int P = w; P < npairs && !abort_flag; P += kMmaWarps) {
                 const uint32_t par = (uint32_t)(P / kMmaWarps) & 1u;
                 wait(kBarABFull + w, par);
-                wait(kBarDEmpty + w, par);   // refilled with the offset
+                wait(kBarDEmpty + w, par);   // read back by every compute warp
                 if (abort_flag)
                     break;
                 fence_after_sync();
@@ -449,7 +439,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                     const uint32_t Bs = sbase + kOffB + (uint32_t)((kPair * w + h) * kBBytes);
 #pragma unroll
                     for (int ks = 0; ks < 8; ks++)
-                        mma_a_tmem(dt, at + 8u * ks, smem_desc(Bs + ks * kKStepBytes), idesc, 1u);
+                        mma_a_tmem(dt, at + 8u * ks, smem_desc(Bs + ks * kKStepBytes), idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(kBarABEmpty + w));
                 mma_commit(bar(kBarDFull + w));
@@ -482,13 +472,9 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         const bool x_ok = xn < M;
         const int xoff = kStageX + xn * TG_GROUP + ((j16 ^ (xn & 7)) << 4);
 
-        // D buffers (both groups of a pair) start at the offset 1.5 * 2^23
+        // D buffers (both groups of a pair): each group's first MMA step overwrites
+        // its buffer, so they start free
         const uint32_t dbase = tmem + lane_off + kColD + 16u * (uint32_t)p;
-#pragma unroll 1
-        for (int c = 0; c < kDBufs * kPair; c++)
-            tmem_st16_same(dbase + (uint32_t)(kMaxN * c), kOffsetBits);
-        tmem_wait_st();
-        fence_before_sync();
         __syncwarp();
         if (lane == 0)
             for (int db = 0; db < kDBufs; db++)
@@ -534,9 +520,10 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 }
             }
         };
-        // read back pair P's D buffer db (ng groups), accumulate it, and refill it
-        // with the offset for pair P + kDBufs if there is one
-        auto epilogue = [&](int db, uint32_t par, int ng, const int (&dprev)[kPair], bool refill) {
+        // read back pair P's D buffer db (ng groups) and accumulate it; the exact
+        // fp32 sums P get 1.5 * 2^23 added (exact: |P| <= 2^14), which leaves
+        // the bit pattern 0x4B400000 + P the folds read
+        auto epilogue = [&](int db, uint32_t par, int ng, const int (&dprev)[kPair]) {
             if (!epi)
                 return;
             wait(kBarDFull + db, par);
@@ -549,9 +536,10 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             tmem_wait_ld(v0);
             if (ng > 1)
                 tmem_wait_ld(v1);
-            if (refill) {
-                tmem_st16_same(dcol, kOffsetBits);
-                tmem_st16_same(dcol + kMaxN, kOffsetBits);
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                v0[j] = __float_as_uint(__fadd_rn(__uint_as_float(v0[j]), 12582912.0f));
+                v1[j] = __float_as_uint(__fadd_rn(__uint_as_float(v1[j]), 12582912.0f));
             }
             fold(v0, dprev[0]);
             if (ng > 1)
@@ -611,8 +599,8 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 }
             }
             dsum += (uint64_t)(int64_t)dg[0] + (uint64_t)(int64_t)dg[1];
-            // hand pair P to its MMA warp: A and B written (and the refill of its D buffer,
-            // done at the end of the previous iteration, complete)
+            // hand pair P to its MMA warp: A and B written (and its D buffer read back
+            // at the end of the previous iteration)
             tmem_wait_st();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before_sync();
@@ -620,12 +608,12 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             if (lane == 0) {
                 mbar_arrive(bar(kBarMEmpty + st));   // this warp is done with input stage st
                 mbar_arrive(bar(kBarABFull + sl));
-                if (P >= kDBufs)   // D buffer sl, read back and refilled for pair P
+                if (P >= kDBufs)   // D buffer sl, read back: free for pair P
                     mbar_arrive(bar(kBarDEmpty + sl));
             }
             // then pair P - 1: its MMAs ran while this pair was prepared
             if (P >= 1)
-                epilogue(sl ^ 1, (uint32_t)((P - 1) >> 1) & 1u, kPair, dprev, P - 1 + kDBufs < npairs);
+                epilogue(sl ^ 1, (uint32_t)((P - 1) >> 1) & 1u, kPair, dprev);
             dprev[0] = dg[0];
             dprev[1] = dg[1];
             if (++st == kStages) {
@@ -635,7 +623,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         }
         if (npairs >= 1)
             epilogue((npairs - 1) & 1, (uint32_t)((npairs - 1) >> 1) & 1u, min(kPair, G - kPair * (npairs - 1)),
-                     dprev, false);
+                     dprev);
         if (kNarrow && epi)
             flush();
         // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); otherwise acc_m
