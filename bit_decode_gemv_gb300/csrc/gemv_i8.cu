@@ -545,6 +545,150 @@ gemv_i8_half1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict_
     gemv_i8_half<1, kQ1, 1>(masks, scales, x, y, N, G, frac, trigger);
 }
 
+// ---------------------------------------------------------------------------
+// One token of int64 fixed-point activations (integer engine §4.4; exact
+// modulo 2^64, §5) on the whole-tile mapping. Each x is split into signed
+// base-256 digits s_0..s_7 in [-128, 127] with x = sum_l 256^l s_l (mod 2^64)
+// -- the bytes of (x + 0x8080...80) XOR 0x8080...80 -- and every digit plane is
+// an int8 activation vector for the lane arithmetic above, four planes to a
+// pass over the group's masked words (as four tokens). Per group the planes'
+// P_l are recombined as sum_l P_l 2^(8l) in wrapping 64-bit arithmetic,
+// multiplied by d, floored and summed, all modulo 2^64. A warp stages exactly
+// the groups it computes, and only as many planes as the group's largest
+// digit needs, rounded up to a pass (a group of zeros takes none): four for
+// magnitudes below 2^31, eight beyond. Planes above a value's top digit are
+// zero bytes, so staging a whole pass changes nothing.
+// ---------------------------------------------------------------------------
+template <int GPW, bool kQ1>
+__global__ void __launch_bounds__(GPW >= 4 ? 512 : 1024)
+gemv_x64_m1_kernel(const uint4 *__restrict__ masks, const int32_t *__restrict__ scales,
+                   const int8_t *__restrict__ xv, int64_t *__restrict__ y, int N, int G, int frac, int trigger)
+{
+    constexpr int kChunks = kQ1 ? 32 : 64;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int K = G * 128;
+    int8_t *xs = reinterpret_cast<int8_t *>(smem);                         // [8 planes][K]
+    int *tsum = reinterpret_cast<int *>(smem + 8 * K);                     // [8][G]
+    int *npl = tsum + 8 * G;                                               // [G] planes staged (0, 4 or 8)
+    uint64_t *red = reinterpret_cast<uint64_t *>(smem + 8 * K + ((9 * G * 4 + 15) & ~15));   // [W][32]
+    const uint64_t *x = reinterpret_cast<const uint64_t *>(xv);
+
+    const int tile = blockIdx.x;
+    const int nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint4 *tmask = masks + (size_t)tile * G * kChunks;
+    const int32_t *tscale = scales + (size_t)tile * G * kTileRows;
+
+    uint4 m0[GPW], m1[GPW];
+    int32_t dg[GPW];
+    auto load_batch = [&](int g0) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = g0 + j * nwarps;
+            if (g < G) {
+                m0[j] = tgi::ldg_stream(tmask + g * kChunks + lane);
+                m1[j] = kQ1 ? make_uint4(0, 0, 0, 0) : tgi::ldg_stream(tmask + g * kChunks + 32 + lane);
+                dg[j] = __ldg(tscale + g * kTileRows + lane);
+            } else {
+                m0[j] = m1[j] = make_uint4(0, 0, 0, 0);
+                dg[j] = 0;
+            }
+        }
+    };
+    load_batch(warp);
+    if (trigger == kTrigAfterLoads)
+        tgi::pdl_launch_dependents();
+    tgi::pdl_wait();
+    if (trigger == kTrigAfterWait)
+        tgi::pdl_launch_dependents();
+
+    // the digit planes of this warp's groups (the groups it computes below):
+    // lane l holds values 4l .. 4l + 3 of the group
+    for (int g = warp; g < G; g += nwarps) {
+        const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(x + (size_t)g * 128 + 4 * lane);
+        const ulonglong2 v01 = __ldg(src), v23 = __ldg(src + 1);
+        const uint64_t dv[4] = {(v01.x + 0x8080808080808080ull) ^ 0x8080808080808080ull,
+                                (v01.y + 0x8080808080808080ull) ^ 0x8080808080808080ull,
+                                (v23.x + 0x8080808080808080ull) ^ 0x8080808080808080ull,
+                                (v23.y + 0x8080808080808080ull) ^ 0x8080808080808080ull};
+        int top = -1;   // highest nonzero digit of the lane's values
+#pragma unroll
+        for (int b = 0; b < 4; b++)
+            if (dv[b])
+                top = max(top, (63 - __clzll((long long)dv[b])) >> 3);
+        top = __reduce_max_sync(0xffffffffu, top);
+        const int np = top < 0 ? 0 : top < 4 ? 4 : 8;
+        for (int l = 0; l < np; l++) {
+            const uint32_t word = (uint32_t)((dv[0] >> (8 * l)) & 0xFF) | ((uint32_t)((dv[1] >> (8 * l)) & 0xFF) << 8) |
+                                  ((uint32_t)((dv[2] >> (8 * l)) & 0xFF) << 16) |
+                                  ((uint32_t)((dv[3] >> (8 * l)) & 0xFF) << 24);
+            reinterpret_cast<uint32_t *>(xs + (size_t)l * K + g * 128)[lane] = word;
+            const int sum = tgi::warp_sum_i32(tgi::byte_sum_s8(word));
+            if (lane == 0)
+                tsum[l * G + g] = sum;
+        }
+        if (lane == 0)
+            npl[g] = np;
+    }
+    __syncwarp();
+    if (trigger == kTrigAfterStage)
+        tgi::pdl_launch_dependents();
+
+    uint64_t acc = 0;   // wrapping
+    for (int g0 = warp;;) {
+#pragma unroll
+        for (int j = 0; j < GPW; j++) {
+            const int g = g0 + j * nwarps;
+            if (g < G && npl[g] > 0) {
+                // sum_l P_l 2^(8l), one pass of four planes at a time, then times
+                // d and floored: all modulo 2^64
+                const int passes = npl[g] > 4 ? 2 : 1;
+                uint64_t p64 = 0;
+#pragma unroll 1
+                for (int h = 0; h < passes; h++) {   // planes 4h .. 4h + 3
+                    const int8_t *xg = xs + (size_t)(4 * h) * K + g * 128;
+                    int P[4];
+                    if (kQ1) {
+                        const uint32_t w[4] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w};
+                        group_pos_q1_tokens<4>(w, xg, K, P);
+#pragma unroll
+                        for (int l = 0; l < 4; l++)
+                            P[l] = 2 * P[l] - tsum[(4 * h + l) * G + g];
+                    } else {
+                        const uint32_t w[8] = {m0[j].x, m0[j].y, m0[j].z, m0[j].w,
+                                               m1[j].x, m1[j].y, m1[j].z, m1[j].w};
+                        group_dot_t2_tokens<4>(w, xg, K, P);
+#pragma unroll
+                        for (int l = 0; l < 4; l++)
+                            P[l] -= 2 * tsum[(4 * h + l) * G + g];
+                    }
+#pragma unroll
+                    for (int l = 0; l < 4; l++)
+                        p64 += (uint64_t)(int64_t)P[l] << (32 * h + 8 * l);
+                }
+                const int64_t v = (int64_t)(p64 * (uint64_t)(int64_t)dg[j]);
+                acc += (uint64_t)(v >> frac);
+            }
+        }
+        g0 += nwarps * GPW;
+        if (g0 >= G)
+            break;
+        load_batch(g0);
+    }
+
+    red[warp * 32 + lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t sum = 0;
+        for (int w = 0; w < nwarps; w++)
+            sum += red[w * 32 + lane];
+        const int row = tile * kTileRows + lane;
+        if (row < N)
+            y[row] = (int64_t)sum;
+    }
+}
+
 // Kernel per token count: M = 1..kFewMaxTokens the two kernels above (the
 // mapping, trigger position and resident-CTA cap from few_plan); then the
 // warp-MMA kernel (gemv_i8_hmma.cu) for one token tile, or two when K is at
@@ -643,6 +787,32 @@ cudaError_t launch_half(const FewLaunch &l)
     static std::atomic<uint64_t> attr_set{0};
     return launch_one(kern, attr_set, l.smem_optin, 2 * l.tiles, warps, half_smem_bytes(l.G, warps, MT), l.min_smem,
                       l.masks, l.scales, l.x, l.y, l.N, l.G, l.frac, l.trigger, l.pdl, l.s);
+}
+
+size_t x64_smem_bytes(int G, int warps)
+{
+    return (size_t)8 * G * 128 + (((size_t)9 * G * 4 + 15) & ~(size_t)15) + (size_t)warps * 32 * 8;
+}
+
+template <int GPW, bool kQ1>
+cudaError_t launch_x64(const FewLaunch &l)
+{
+    const int max_warps = GPW >= 4 ? 16 : 32;
+    const int warps = min((l.G + GPW - 1) / GPW, max_warps);
+    static std::atomic<uint64_t> attr_set{0};
+    return launch_one(gemv_x64_m1_kernel<GPW, kQ1>, attr_set, l.smem_optin, l.tiles, warps,
+                      x64_smem_bytes(l.G, warps), l.min_smem, l.masks, l.scales, l.x, l.y, l.N, l.G, l.frac,
+                      l.trigger, l.pdl, l.s);
+}
+
+template <bool kQ1>
+cudaError_t launch_x64_m1(const FewLaunch &l)
+{
+    if (l.G <= 32)
+        return launch_x64<1, kQ1>(l);
+    if (l.G <= 64)
+        return launch_x64<2, kQ1>(l);
+    return launch_x64<4, kQ1>(l);
 }
 
 // Groups per warp. Whole tiles, one token: one group per warp up to K = 4096
@@ -820,33 +990,46 @@ extern "C" int tg_gemv_i8(const tg_layout *L, const void *w, const int8_t *x, in
     const int tiles = (int)L->tiles;
 
     const bool pdl = (L->flags & TG_FLAG_CONST_WEIGHTS) != 0;
-    if (x64)   // int64 activations: the digit-plane dp4a kernel for every M
-        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1, true,
-                               (int)L->frac, pdl, s);
-
     const bool q1 = L->kind == TG_BINARY_Q1;
+    // shapes no kernel takes are refused before any device query or launch
     DeviceShape d;
-    if (!device_shape(d))
-        return TG_ERR_CUDA;
-    if (few_takes((int)M, G, tiles, d.nsm) && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax) {
-        FewPlan plan = few_plan((int)M, G, tiles, d.nsm);
-        if (plan.half && half_smem_bytes(G, 32, (int)M) > kM1SmemMax)
-            plan = {false, kTrigAfterLoads, 0};
-        const FewLaunch l = {d.smem_optin, masks, scales, x, y, N, G, tiles, (int)L->frac, plan.trigger,
-                             cap_smem(d, plan.cap), pdl, s};
-        const cudaError_t e = q1 ? launch_few<true>((int)M, plan.half, l) : launch_few<false>((int)M, plan.half, l);
-        if (e != cudaSuccess)
-            return TG_ERR_CUDA;
-    } else if (M == 1) {
-        return TG_ERR_SHAPE;
-    } else if (M <= kDp4aMaxTokens) {
-        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, q1, false, (int)L->frac, pdl, s);
-    } else if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G)) {
-        return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, L->kind == TG_BINARY_Q1,
-                                 (int)L->frac, pdl, s);
-    } else {
-        return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale,
-                                L->kind == TG_BINARY_Q1, (int)L->frac, L->wait_limit, s);
+    if (x64) {
+        // int64 activations: one token on the whole-tile digit-plane kernel
+        // (launched like the one-token int8 plan for K <= 4096), else the
+        // chunked dp4a kernel for every M (which refuses what it cannot stage)
+        if (M == 1 && x64_smem_bytes(G, 32) <= kM1SmemMax) {
+            if (!device_shape(d))
+                return TG_ERR_CUDA;
+            const bool few_tiles = tiles <= 2 * d.nsm;
+            const FewLaunch l = {d.smem_optin, masks, scales, x, y, N, G, tiles, (int)L->frac, kTrigAfterWait,
+                                 cap_smem(d, G <= 32 && few_tiles ? 2 : 0), pdl, s};
+            const cudaError_t e = q1 ? launch_x64_m1<true>(l) : launch_x64_m1<false>(l);
+            return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+        }
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, q1, true, (int)L->frac, pdl, s);
     }
-    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+
+    const bool few_fit = M <= kFewMaxTokens && m1_smem_bytes(G, 32, (int)M) <= kM1SmemMax;
+    if (M == 1 && !few_fit)
+        return TG_ERR_SHAPE;
+    if (few_fit) {
+        if (!device_shape(d))
+            return TG_ERR_CUDA;
+        if (few_takes((int)M, G, tiles, d.nsm)) {
+            FewPlan plan = few_plan((int)M, G, tiles, d.nsm);
+            if (plan.half && half_smem_bytes(G, 32, (int)M) > kM1SmemMax)
+                plan = {false, kTrigAfterLoads, 0};
+            const FewLaunch l = {d.smem_optin, masks, scales, x, y, N, G, tiles, (int)L->frac, plan.trigger,
+                                 cap_smem(d, plan.cap), pdl, s};
+            const cudaError_t e =
+                q1 ? launch_few<true>((int)M, plan.half, l) : launch_few<false>((int)M, plan.half, l);
+            return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+        }
+    }
+    if (M <= kDp4aMaxTokens)
+        return tgi::gemv_i8_mt(masks, scales, x, y, N, G, tiles, (int)M, q1, false, (int)L->frac, pdl, s);
+    if ((M <= 8 || (M <= kHmmaMaxTokens && L->K <= kHmmaTwoTileMaxK)) && tgi::gemv_i8_hmma_fits(G))
+        return tgi::gemv_i8_hmma(masks, scales, x, y, N, G, tiles, (int)M, q1, (int)L->frac, pdl, s);
+    return tgi::gemv_i8_mma(masks, scales, x, y, N, G, tiles, (int)M, L->max_abs_scale, q1, (int)L->frac,
+                            L->wait_limit, s);
 }

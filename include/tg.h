@@ -189,7 +189,8 @@ typedef struct tg_layout {
  * exact whenever no step leaves the int64 range, and there is no TG_ERR_BOUND
  * check. Computed by signed base-256 digit planes of x, as many as the largest
  * activation needs; eight planes of one token must fit the kernel's staging
- * area, so K is at most 17,792 (TG_ERR_SHAPE beyond).
+ * area, so K is at most 23,680 for one token and 17,792 for more
+ * (TG_ERR_SHAPE beyond).
  */
 #define TG_FLAG_X_INT64 4
 

@@ -350,14 +350,15 @@ def test_layout_flags_are_distinct_bits():
     assert len(set(flags)) == len(flags) and sum(flags) == (flags[0] | flags[1] | flags[2] | flags[3])
 
 
-def test_int64_activations_k_limit():
-    """Eight digit planes of one token must fit the staging area: K = 17920 is
-    TG_ERR_SHAPE before any launch (K = 17792 runs in the GPU tests' range)."""
+@pytest.mark.parametrize("M,K", [(2, 17920), (1, 23808)])
+def test_int64_activations_k_limit(M, K):
+    """Eight digit planes must fit the staging area: K = 17920 with several
+    tokens and K = 23808 with one are TG_ERR_SHAPE before any device query or
+    launch (17792 and 23680 run in the GPU tests' range)."""
     import bit_decode_gemv_gb300 as tg
-    K = 17920
     _, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, np.zeros((1, K), np.int8), np.ones((1, K // 128), np.int32))
     L.flags |= tg.TG_FLAG_X_INT64
-    assert status_of(tg.tg_gemv_i8, L, A256, A256, 1, A256, 0) == tg.TG_ERR_SHAPE
+    assert status_of(tg.tg_gemv_i8, L, A256, A256, M, A256, 0) == tg.TG_ERR_SHAPE
 
 
 def test_compiled_and_ctypes_call_paths_agree():

@@ -46,14 +46,32 @@ def test_full_range_int64_wraps_like_the_oracle(N, K, M):
     check(w["t"], w["d"], W.x_int64_full(N * K + M, (M, K)))
 
 
+@pytest.mark.parametrize("M", [1, 3])
 @pytest.mark.parametrize("frac", [0, 5, 40])
-@pytest.mark.parametrize("bits", [7, 15, 23, 31, 47])
-def test_fixed_point_magnitudes(bits, frac):
-    """|x| < 2^bits: one plane for int8-range values, more as they grow."""
-    w = W.batched(seed=bits, M=3, N=70, K=768)
-    x = W.x_fixed64(bits, (3, 768), frac_bits=bits - 3)
+@pytest.mark.parametrize("bits", [7, 15, 23, 31, 39, 47])
+def test_fixed_point_magnitudes(bits, frac, M):
+    """|x| < 2^bits: one plane for int8-range values, more as they grow (at one
+    token: one pass of four planes up to 2^31, two beyond)."""
+    w = W.batched(seed=bits, M=M, N=70, K=768)
+    x = W.x_fixed64(bits, (M, 768), frac_bits=bits - 3)
     x = np.clip(x, -(1 << bits), (1 << bits) - 1)
     check(w["t"], w["d"], x, frac)
+
+
+def test_one_token_groups_of_different_sizes():
+    """One token whose groups need no plane (all zero), one pass and two passes,
+    side by side, ternary and Q1_0, on more rows than two tiles per SM."""
+    K = 1280
+    w = W.batched(seed=91, M=1, N=10000, K=K)
+    x = W.x_int64_full(91, (1, K))
+    x[0, 0:128] = 0                                         # group 0: zeros
+    x[0, 128:256] = np.clip(x[0, 128:256], -100, 100)      # group 1: one digit
+    x[0, 256:384] >>= 40                                    # group 2: three digits
+    check(w["t"], w["d"], x)
+    check(w["t"], w["d"], x, 7)
+    bits = (w["t"] > 0)
+    t_pm = np.where(bits, 1, -1).astype(np.int8)
+    check_q1(t_pm, w["d"], x, 3)
 
 
 def test_ffn_up_shape_q16_activations():
@@ -111,13 +129,14 @@ def test_int8_range_values_equal_the_int8_call():
     np.testing.assert_array_equal(y64, gemv(wd, L, w["x"]))
 
 
-def test_const_weights_back_to_back_int64():
+@pytest.mark.parametrize("M", [1, 2])
+def test_const_weights_back_to_back_int64(M):
     """Programmatic dependent launch on the int64 path: a torch kernel rewrites
     x between calls that all write the same y."""
     import torch
     import bit_decode_gemv_gb300 as tg
     from gpu_helpers import dev, pack_to_device
-    N, K, M = 300, 1024, 2
+    N, K = 300, 1024
     cases = [W.batched(seed=300 + i, M=M, N=N, K=K) for i in range(3)]
     packed = []
     for w in cases:
@@ -138,6 +157,9 @@ def test_const_weights_back_to_back_int64():
 
 
 def test_largest_k():
-    """K = 17792, the largest K whose eight digit planes fit the staging area."""
+    """K = 17792, the largest K whose eight digit planes of several tokens fit
+    the staging area, and K = 23680, the largest for one token."""
     w = W.batched(seed=17, M=2, N=40, K=17792)
     check(w["t"], w["d"], W.x_int64_full(17, (2, 17792)))
+    w = W.batched(seed=18, M=1, N=40, K=23680)
+    check(w["t"], w["d"], W.x_int64_full(18, (1, 23680)))
