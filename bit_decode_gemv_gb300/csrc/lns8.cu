@@ -32,9 +32,12 @@
 // conversion, and the warp-level MMA, fed from registers, avoids staging the
 // expanded weights anywhere.
 //
-// Mapping: a CTA owns 128 rows (warp w: rows 16w..16w+15) and a slice of the
-// groups; a cluster of up to 8 CTAs covers all groups of those rows. Each CTA
-// keeps int32 phase partials in shared memory; each CTA of the cluster then
+// Mapping: a CTA owns 128 rows and a slice of the groups; a cluster of up to 8
+// CTAs covers all groups of those rows. Two warps share each 16-row block
+// (warps w and w + 8: rows 16(w % 8)..+15), each taking half of every chunk of
+// four groups, so twice as many warps hide the MMA and conversion latency.
+// Each CTA keeps int32 phase partials in shared memory, one array per group
+// half; each CTA of the cluster then
 // owns a slice of the rows, gathers their partials from the other CTAs through
 // distributed shared memory, sums them into int64 A and materialises S with
 // explicitly rounded fp64 multiplies and adds in the order p = 0..7.
@@ -55,8 +58,9 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kWarps = 8;                  // warps per CTA; warp w owns one 16-row block
-constexpr int kRows = kWarps * 16;         // rows per CTA
+constexpr int kRowWarps = 8;               // 16-row blocks per CTA
+constexpr int kWarps = 2 * kRowWarps;      // warps per CTA: two per 16-row block, each half of a chunk's groups
+constexpr int kRows = kRowWarps * 16;      // rows per CTA
 constexpr int kChunkGroups = 4;            // groups per step: V fragments staged, weights in flight
 constexpr int kMaxCluster = 8;
 
@@ -156,14 +160,14 @@ __device__ __forceinline__ void walk_clamp_list(const uint16_t *list, int n, con
     }
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 2)
 lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ codes,
                 const uint8_t *__restrict__ xa, int64_t *__restrict__ A, double *__restrict__ S,
                 const __grid_constant__ PhaseF F, const double *__restrict__ Fd, int N, int G, int gpc)
 {
     __shared__ uint2 vfrag[kChunkGroups][8][32];   // V fragments (b0, b1) per group, chunk, lane
     __shared__ unsigned gmin[kChunkGroups], gmax[kChunkGroups];
-    __shared__ int acc[kRows][8];                  // int32 phase partials of this CTA's groups
+    __shared__ int acc[2][kRows][8];               // int32 phase partials of this CTA's groups, per group half
     __shared__ int stage[kRows + kMaxCluster][8];  // partials of the rows this CTA owns, per source CTA
     __shared__ int gcorr[kWarps][16][8];           // class-sum corrections of clamped lanes, per warp row
     __shared__ int64_t arow[kRows][8];             // int64 A of the rows this CTA owns
@@ -176,54 +180,72 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int gq = lane >> 2, tq = lane & 3;
-    const int rb = blockIdx.x * kWarps + warp;       // 16-row block of this warp
+    const int rw = warp & (kRowWarps - 1);           // this warp's 16-row block of the CTA
+    const int gh = warp / kRowWarps;                 // and its half of each chunk's groups
+    const int rb = blockIdx.x * kRowWarps + rw;      // 16-row block of this warp in the matrix
     const int g_begin = rank * gpc;
     const int g_end = min(G, g_begin + gpc);
 
-    // (acc needs no clearing: each warp's first group stores its rows' partials)
+    // (acc needs no clearing where a warp has a group: its first group stores its
+    // rows' partials; a warp whose half of the first chunk is empty clears them)
     for (int i = tid; i < kWarps * 16 * 8; i += blockDim.x)
         (&gcorr[0][0][0])[i] = 0;
 
     const bool active = rb * 16 < N;   // warp-uniform
+    if (2 * gh >= min(kChunkGroups, g_end - g_begin))
+        for (int i = lane; i < 16 * 8; i += 32)
+            acc[gh][rw * 16 + (i >> 3)][i & 7] = 0;
     for (int c0 = g_begin; c0 < g_end; c0 += kChunkGroups) {
         const int ng = min(kChunkGroups, g_end - c0);
-        // this warp's masks and scale codes for the chunk, issued before the
-        // shared-memory set-up so the weight stream overlaps it
-        uint4 wv[kChunkGroups];
-        int ec[kChunkGroups][2];
+        // this warp's masks and scale codes for its half of the chunk (groups
+        // 2 gh, 2 gh + 1), issued before the shared-memory set-up so the weight
+        // stream overlaps it
+        constexpr int kHalf = kChunkGroups / 2;
+        uint4 wv[kHalf];
+        int ec[kHalf][2];
         uint32_t xw[kChunkGroups];   // activation bytes 4 lane .. 4 lane + 3 of each group (range, clamp lists)
-        uint32_t xb[kChunkGroups][2];   // this thread's V entry's activation byte pairs, per group
-        static_assert(kWarps * 32 == 256, "one V entry (chunk, lane) per thread and group");
-        const int vkc = tid >> 5, vln = tid & 31;
+        uint32_t xb[kHalf][2];       // this thread's V entries' activation byte pairs
+        static_assert(kRowWarps * 32 == 256 && kWarps == 2 * kRowWarps,
+                      "one V entry (chunk, lane) per thread and group of its half");
+        const int vkc = (tid >> 5) & 7, vln = tid & 31, vgh = tid >> 8;
 #pragma unroll
-        for (int gl = 0; gl < kChunkGroups; gl++) {
-            wv[gl] = make_uint4(0, 0, 0, 0);
-            ec[gl][0] = ec[gl][1] = 0;
-            xw[gl] = 0;
+        for (int j = 0; j < kHalf; j++) {
+            const int gl = kHalf * gh + j;
+            wv[j] = make_uint4(0, 0, 0, 0);
+            ec[j][0] = ec[j][1] = 0;
             if (active && gl < ng) {
                 const size_t unit = (size_t)rb * G + c0 + gl;
-                wv[gl] = tgi::ldg_stream(masks + unit * 32 + lane);
-                ec[gl][0] = (int)__ldg(codes + unit * 16 + gq) - 74;
-                ec[gl][1] = (int)__ldg(codes + unit * 16 + gq + 8) - 74;
+                wv[j] = tgi::ldg_stream(masks + unit * 32 + lane);
+                ec[j][0] = (int)__ldg(codes + unit * 16 + gq) - 74;
+                ec[j][1] = (int)__ldg(codes + unit * 16 + gq + 8) - 74;
             }
-            // the activations, for every warp (all threads build V): issued with the weights
+        }
+        // the activations, for every warp (all threads build V): issued with the weights
+#pragma unroll
+        for (int gl = 0; gl < kChunkGroups; gl++) {
             const int gx = c0 + min(gl, ng - 1);
             xw[gl] = __ldg(reinterpret_cast<const uint32_t *>(xa + (size_t)gx * TG_GROUP) + lane);
+        }
+#pragma unroll
+        for (int j = 0; j < kHalf; j++) {
+            const int gx = c0 + min(kHalf * vgh + j, ng - 1);
             const uint16_t *xg = reinterpret_cast<const uint16_t *>(xa + (size_t)gx * TG_GROUP + 16 * vkc) + (vln & 3);
-            xb[gl][0] = __ldg(xg);
-            xb[gl][1] = __ldg(xg + 4);
+            xb[j][0] = __ldg(xg);
+            xb[j][1] = __ldg(xg + 4);
         }
         __syncthreads();
         // V fragments: thread (q, j) of chunk kc holds V rows 2j, 2j+1 (b0) and
         // 2j+8, 2j+9 (b1) of column q; thread tid builds entry (kc, ln) =
-        // (tid / 32, tid % 32) of every group of the chunk from the byte pairs it
-        // loaded above (lanes 16 kc + 2 (ln & 3) + {0, 1} and + {8, 9})
+        // ((tid / 32) % 8, tid % 32) of the groups of its half of the chunk from
+        // the byte pairs it loaded above (lanes 16 kc + 2 (ln & 3) + {0, 1} and
+        // + {8, 9})
         {
             const uint32_t q = (uint32_t)(vln >> 2);
 #pragma unroll
-            for (int gl = 0; gl < kChunkGroups; gl++) {
+            for (int j = 0; j < kHalf; j++) {
+                const int gl = kHalf * vgh + j;
                 if (gl < ng) {
-                    const uint32_t p0 = xb[gl][0], p1 = xb[gl][1];
+                    const uint32_t p0 = xb[j][0], p1 = xb[j][1];
                     const uint32_t b0 = v_entry(p0 & 0xffu, q) | (v_entry(p0 >> 8, q) << 16);
                     const uint32_t b1 = v_entry(p1 & 0xffu, q) | (v_entry(p1 >> 8, q) << 16);
                     vfrag[gl][vkc][vln] = make_uint2(b0, b1);
@@ -255,11 +277,12 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
 
         if (active) {
 #pragma unroll
-            for (int gl = 0; gl < kChunkGroups; gl++) {
+            for (int j = 0; j < kHalf; j++) {
+                const int gl = kHalf * gh + j;
                 if (gl >= ng)
                     break;
-                const uint32_t w4[4] = {wv[gl].x, wv[gl].y, wv[gl].z, wv[gl].w};
-                const bool first = c0 == g_begin && gl == 0;   // this warp's first group: store, not add
+                const uint32_t w4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+                const bool first = c0 == g_begin && j == 0;   // this warp's first group: store, not add
                 // two independent accumulation chains (even and odd chunks);
                 // each partial is an integer of magnitude below 2^23, so the
                 // fp32 sums and their final sum are exact
@@ -278,7 +301,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 // quad-uniform: the four threads of a quad hold the same two rows.
                 // Rows past N (zero weights, scale code 0) never need the clamp
                 // correction.
-                const int e[2] = {ec[gl][0], ec[gl][1]};
+                const int e[2] = {ec[j][0], ec[j][1]};
                 bool need[2];
 #pragma unroll
                 for (int half = 0; half < 2; half++)
@@ -315,11 +338,11 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
                 }
 #pragma unroll
                 for (int half = 0; half < 2; half++) {
-                    int *acc_row = acc[warp * 16 + gq + 8 * half];
+                    int *acc_row = acc[gh][rw * 16 + gq + 8 * half];
 #pragma unroll
-                    for (int j = 0; j < 2; j++) {
-                        const int q = 2 * tq + j;
-                        const int v = __float2int_rn(d[2 * half + j]);
+                    for (int c = 0; c < 2; c++) {
+                        const int q = 2 * tq + c;
+                        const int v = __float2int_rn(d[2 * half + c]);
                         const int sidx = q + (e[half] & 7);
                         const int sh = max(-31, min(31, (e[half] >> 3) + (sidx >> 3)));
                         int add = sh >= 0 ? (v << sh) : (v >> -sh);
@@ -346,7 +369,7 @@ lns8_mma_kernel(const uint4 *__restrict__ masks, const uint8_t *__restrict__ cod
         const int rl = item >> 3, p = item & 7;
         const int dst = rl / slice;
         int *remote = cluster.map_shared_rank(&stage[0][0], dst);
-        remote[((rank * slice) + (rl - dst * slice)) * 8 + p] = acc[rl][p];
+        remote[((rank * slice) + (rl - dst * slice)) * 8 + p] = acc[0][rl][p] + acc[1][rl][p];
     }
     cluster.sync();
     // A: the owner sums its slice's partials in rank order
