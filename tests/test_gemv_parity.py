@@ -279,6 +279,17 @@ def test_one_token_launch_plans(N):
     check_q1(W.ffn_up_q1(seed=N + 1, N=N, K=2560, M=1), 2)
 
 
+# One token with K > 4096 takes the half-tile kernel: one pair of groups per
+# warp up to K = 8192, two up to K = 16384 (and four beyond, in
+# test_few_tokens_wide_rows), ternary and Q1_0, with and without the floor.
+@pytest.mark.parametrize("K", [5120, 8192, 12800])
+def test_one_token_half_tiles(K):
+    check(W.batched(seed=K, M=1, N=1000, K=K))
+    check_frac(W.batched(seed=K + 1, M=1, N=333, K=K), 9)
+    check_q1(W.ffn_up_q1(seed=K + 2, N=1000, K=K, M=1))
+    check_q1(W.ffn_up_q1(seed=K + 3, N=333, K=K, M=1), 4)
+
+
 # Seven and eight tokens on more tiles than SMs with K > 4096 (and more than
 # twice as many with K <= 4096) go to the warp-MMA kernel; five and six stay on
 # the few-token kernels.

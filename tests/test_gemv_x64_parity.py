@@ -58,6 +58,15 @@ def test_fixed_point_magnitudes(bits, frac, M):
     check(w["t"], w["d"], x, frac)
 
 
+@pytest.mark.parametrize("K", [6144, 12800])
+def test_one_token_two_and_four_groups_per_warp(K):
+    """One token of int64 activations with two groups per warp (K up to 8192)
+    and four (beyond), full range and Q.16, with the floor."""
+    w = W.batched(seed=K, M=1, N=300, K=K)
+    check(w["t"], w["d"], W.x_int64_full(K, (1, K)))
+    check(w["t"], w["d"], W.x_fixed64(K, (1, K)), 11)
+
+
 def test_one_token_groups_of_different_sizes():
     """One token whose groups need no plane (all zero), one pass and two passes,
     side by side, ternary and Q1_0, on more rows than two tiles per SM."""
