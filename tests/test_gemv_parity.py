@@ -279,6 +279,17 @@ def test_one_token_launch_plans(N):
     check_q1(W.ffn_up_q1(seed=N + 1, N=N, K=2560, M=1), 2)
 
 
+# The smallest shapes through every one-to-eight-token launch: one group (the
+# half-tile kernel's second half-warp has no group), three groups (an odd
+# pair), one row, a ragged last tile; ternary and Q1_0, with the floor.
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("N,K", [(1, 128), (31, 384), (33, 128), (65, 256)])
+def test_smallest_shapes_every_token_count(M, N, K):
+    check(W.batched(seed=N * K + M, M=M, N=N, K=K))
+    check_frac(W.batched(seed=N * K + M + 1, M=M, N=N, K=K), 3)
+    check_q1(W.ffn_up_q1(seed=N * K + M + 2, N=N, K=K, M=M), 2)
+
+
 # One token with K > 4096 takes the half-tile kernel: one pair of groups per
 # warp up to K = 8192, two up to K = 16384 (and four beyond, in
 # test_few_tokens_wide_rows), ternary and Q1_0, with and without the floor.
