@@ -23,9 +23,9 @@
 // (one plane for activations in int8 range, three for magnitudes below 2^23).
 //
 // tg_gemv_i8 sends this kernel calls of two or more tokens with int64
-// activations (one token, and one whose digit planes do not fit the one-token
-// kernel of gemv_i8.cu, also land here), and int8 calls of two to four tokens
-// whose activations do not fit the shared memory of the few-token kernels in
+// activations (and one token whose digit planes do not fit the one-token
+// kernel of gemv_i8.cu), and int8 calls of two to four tokens whose
+// activations do not fit the shared memory of the few-token kernels in
 // gemv_i8.cu (this one stages tokens in chunks).
 //
 // Mapping: one CTA per 32-row tile (lane l of every warp owns row 32T + l),
