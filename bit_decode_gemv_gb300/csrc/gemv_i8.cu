@@ -904,9 +904,13 @@ bool device_shape(DeviceShape &d)
 //   - one token, longer rows: half tiles (5120 x 5120 3.77 -> 2.68 us,
 //     13824 x 5120 6.38 -> 5.03);
 //   - several tokens: half tiles when K <= 4096 and a call has at most two
-//     tiles per SM, else whole tiles, the next call launched once the
-//     activations are staged (13824 x 5120 at M = 4: 12.1 -> 11.1 us,
-//     2560 x 2560 at M = 4: 4.7 -> 2.6).
+//     tiles per SM, the next call launched after the wait; else whole tiles,
+//     the next call launched once the activations are staged (13824 x 5120 at
+//     M = 4: 12.1 -> 11.1 us, 2560 x 2560 at M = 4: 4.7 -> 2.6). Checked on seven
+//     more shapes (4096 x 1024, 4096 x 2048, 1024 x 4096, 2048 x 3072,
+//     11008 x 4096, 4096 x 11008, 8192 x 8192): for half tiles the release
+//     after the wait was as fast as after staging at M = 5..8 and up to 25 %
+//     faster at M = 2..4 (4096 x 2048 at M = 4: 3.23 -> 2.44 us).
 struct FewPlan {
     bool half;
     int trigger;
@@ -928,7 +932,7 @@ FewPlan few_plan(int M, int G, int tiles, int nsm)
         return {true, kTrigAfterLoads, 0};
     }
     if (G <= 32 && few_tiles)
-        return {true, kTrigAfterStage, 0};
+        return {true, kTrigAfterWait, 0};
     return {false, kTrigAfterStage, 0};
 }
 
