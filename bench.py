@@ -760,16 +760,23 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    tgbuild.build()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # one rank compiles the in-tree library (when it is stale) before the others
+    # load it, so that no two compilers write the same files
+    if rank == 0:
+        tgbuild.build()
+    barrier()
+    if rank != 0:
+        tgbuild.build()
     stream = torch.cuda.current_stream()
     s_handle = stream.cuda_stream
 
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
 
     # workload and rotating weight copies
     w = W.ffn_up(seed=rank)
