@@ -19,6 +19,11 @@ Also reported on the same line:
   e2e          the same metric with the step's activations copied in from
                pinned host memory, every call made eagerly through the public
                API, and all outputs read back, every step;
+  e2e_graph    the same, with the calls replayed from CUDA graphs captured
+               once before the timed region (the copies stay inside it);
+  wall_us      µs per call: back to back from the graph (with and without the
+               constant-weights flag) and one call at a time (200 reps:
+               median, p10, p90);
   roofline     the GEMV kernel's algorithmic bytes per launch / its average
                launch time, against the measured HBM copy bandwidth;
   cpu_baseline the CPU oracle timed on a bounded sample on the host cores;
@@ -347,6 +352,26 @@ def event_time(torch, fn, reps, stream):
     return e0.elapsed_time(e1) / 1e3
 
 
+def isolated_call_stats(torch, stream, call, reps=200, spacer_cycles=200_000):
+    """Device time of one call at a time, in µs: before each rep the stream runs
+    a short spin kernel (about 0.1 ms), behind which the host queues the rep's
+    two events and its call, so that the interval between the events holds the
+    call alone, with no host submission gap; median, p10 and p90 over the reps.
+    call(i) makes rep i's call (rotate the weights there to keep them out of L2)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        torch.cuda._sleep(spacer_cycles)
+        a, b = evs[i]
+        a.record(stream)
+        call(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+    return {"median": round(float(np.median(us)), 3), "p10": round(float(np.quantile(us, 0.1)), 3),
+            "p90": round(float(np.quantile(us, 0.9)), 3), "reps": reps}
+
+
 def _copies_for(nbytes):
     return max(1, int(math.ceil(4 * L2_BYTES / nbytes)))
 
@@ -468,8 +493,8 @@ def _gemv_m1_row(tg, torch, stream, dev, kind, w, frac):
 def row_tiny(tg, torch, stream, dev):
     """The tiny GEMV (N=256, K=512, batch 1; 36 KB of weights): launch-latency
     bound, reported in µs per call -- back to back from a CUDA graph with the
-    weights flagged constant and without the flag, and one call alone (from its
-    own one-call graph, the stream idle before it)."""
+    weights flagged constant and without the flag, and one call at a time (200
+    reps, each queued behind a short spin kernel: median, p10 and p90)."""
     w = W.tiny()
     blob, L = tg.tg_pack_weights(tg.TG_TERNARY_I8, w["t"], w["d"])
     R = 64
@@ -485,12 +510,10 @@ def row_tiny(tg, torch, stream, dev):
         g.replay()
         out[key] = round(event_time(torch, lambda i: g.replay(), 8, stream) / (8 * 512) * 1e6, 3)
         del g
-    g1 = capture_graph(torch, lambda i, h: tg.tg_gemv_i8(L, wd[0], xd, 1, y, h), 1)
-    g1.replay()
-    singles = []
-    for _ in range(50):
-        singles.append(event_time(torch, lambda i: g1.replay(), 1, stream))
-    out["us_single_call"] = round(float(np.median(singles)) * 1e6, 3)
+    iso = isolated_call_stats(torch, stream, lambda i: tg.tg_gemv_i8(L, wd[i % R], xd, 1, y, stream.cuda_stream))
+    out["us_single_call"] = iso["median"]
+    out["us_single_call_p10_p90"] = [iso["p10"], iso["p90"]]
+    out["single_call_reps"] = iso["reps"]
     out["us"] = out["us_back_to_back_const_weights"]
     return {"tiny": out}
 
@@ -890,6 +913,41 @@ def run_ours(args):
         raise SystemExit("e2e result differs from the device-timed result")
     e2e_val = world * e2e_steps * GEMVS_PER_STEP * wbytes / e2e_dt / 1e9
 
+    # The same step with each chunk's calls replayed from a CUDA graph captured
+    # once before the timed region, as a decode loop does: the activations still
+    # come in from pinned host memory and every output goes back, every step.
+    chunk_graphs = [capture_graph(torch, lambda j, h, c=c: tg.tg_gemv_i8(Lp, w_views[c + j], x_views[c + j], 1,
+                                                                         y_views[c + j], h), readback_chunk)
+                    for c in range(0, GEMVS_PER_STEP, readback_chunk)]
+
+    def e2e_graph_step():
+        xs_dev.copy_(xs_host, non_blocking=True)
+        for ci, gch in enumerate(chunk_graphs):
+            gch.replay()
+            ev = chunk_done[ci]
+            ev.record(stream)
+            copy_stream.wait_event(ev)
+            c = ci * readback_chunk
+            with torch.cuda.stream(copy_stream):
+                ys_host[c:c + readback_chunk].copy_(ys_dev[c:c + readback_chunk], non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(2):
+        e2e_graph_step()
+    ys_host.zero_()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_graph_step()
+    e2e_graph_dt = time.perf_counter() - t0
+    if not np.array_equal(ys_host[-1].numpy(), y[0].cpu().numpy()):
+        raise SystemExit("graph e2e result differs from the device-timed result")
+    e2e_graph_val = world * e2e_steps * GEMVS_PER_STEP * wbytes / e2e_graph_dt / 1e9
+    del chunk_graphs
+
+    # one call at a time (the plain call, no dependent launch), weights rotated
+    iso = isolated_call_stats(torch, stream, lambda i: tg.tg_gemv_i8(L, wd[i % R], xd, 1, y, s_handle))
+
     if rank != 0:
         return
 
@@ -914,6 +972,14 @@ def run_ours(args):
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(xs_host.numel()),
                 "d2h_bytes_per_step": int(ys_host.numel() * 8)},
+        "e2e_graph": {"value": round(e2e_graph_val, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": int(xs_host.numel()),
+                      "d2h_bytes_per_step": int(ys_host.numel() * 8),
+                      "launch": f"each chunk of {readback_chunk} calls replayed from a CUDA graph captured "
+                                "before the timed region; copies in and out inside it"},
+        "wall_us": {"graph_back_to_back": round(per_gemv * 1e6, 3),
+                    "graph_back_to_back_without_const_flag": round(t_plain * 1e6, 3),
+                    "one_call_at_a_time": iso},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
