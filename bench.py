@@ -400,7 +400,9 @@ def row_lns8(tg, torch, stream, dev):
                  tg.TG_FLAG_LNS8_PURE_LNS: "pure fractional-LNS route, F = 4 (approximate)"}[flags]
         out[key] = {"workload": "N=4096 K=4096 LNS8 eight-phase, " + route,
                     "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
-                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R}
+                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "alu", "copies": R,
+                    "us_one_call": isolated_call_stats(
+                        torch, stream, lambda i: tg.tg_gemv_lns8_phase(Lr, wd[i % R], xa, A, S, stream.cuda_stream))}
         del g
     # the same direct route with activation codes over the whole range (about a
     # fifth of the lanes near an end, so most (row, group) pairs need the exact
@@ -449,7 +451,10 @@ def row_lm_head(tg, torch, stream, dev):
         out[key] = {"workload": "N=128256 K=2560 8 base-3 planes, k=200", "us": round(t * 1e6, 2),
                     "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
                     "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "hbm",
-                    "candidates": int(nc.item())}
+                    "candidates": int(nc.item()),
+                    "us_one_call": isolated_call_stats(
+                        torch, stream, lambda i: tg.tg_lmhead_argmax_topk(L, wdl, xd, k, lg, am, ids, sc, nc, ws,
+                                                                          wsb, stream.cuda_stream))}
         del g
     return out
 
@@ -467,9 +472,10 @@ def row_batched(tg, torch, stream, dev):
     t = event_time(torch, lambda i: g.replay(), 2, stream) / (2 * R)
     alg = L.mask_bytes + L.scale_bytes + 64 * L.K + 64 * L.N * 8
     macs = 64 * L.N * L.K
+    iso = isolated_call_stats(torch, stream, lambda i: tg.tg_gemv_i8(L, wd[i % R], xd, 64, y, stream.cuda_stream))
     return {"batched_m64": {"workload": "M=64 N=13824 K=5120 ternary GEMM", "us": round(t * 1e6, 2),
                             "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
-                            "tops_int": round(2 * macs / t / 1e12, 2), "copies": R}}
+                            "tops_int": round(2 * macs / t / 1e12, 2), "copies": R, "us_one_call": iso}}
 
 
 def _gemv_m1_row(tg, torch, stream, dev, kind, w, frac):
@@ -486,8 +492,11 @@ def _gemv_m1_row(tg, torch, stream, dev, kind, w, frac):
     g.replay()
     t = event_time(torch, lambda i: g.replay(), 4, stream) / (4 * R)
     alg = L.mask_bytes + L.scale_bytes + L.K + L.N * 8
+    Lplain = tg.tg_layout.from_buffer_copy(L)
+    Lplain.flags &= ~tg.TG_FLAG_CONST_WEIGHTS
+    iso = isolated_call_stats(torch, stream, lambda i: tg.tg_gemv_i8(Lplain, wd[i % R], xd, 1, y, stream.cuda_stream))
     return {"us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
-            "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "hbm", "copies": R}
+            "frac_hbm": round(alg / t / 1e9 / hbm, 4), "bound": "hbm", "copies": R, "us_one_call": iso}
 
 
 def row_tiny(tg, torch, stream, dev):
@@ -539,7 +548,9 @@ def row_x64(tg, torch, stream, dev):
         out[key] = {"workload": "N=6912 K=2560 ternary, batch 1, int64 activations "
                                 + ("rint(N(0,1) 2^16)" if "q16" in key else "uniform over int64"),
                     "us": round(t * 1e6, 3), "alg_bytes": int(alg), "gbs": round(alg / t / 1e9, 1),
-                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "copies": R}
+                    "frac_hbm": round(alg / t / 1e9 / hbm, 4), "copies": R,
+                    "us_one_call": isolated_call_stats(
+                        torch, stream, lambda i: tg.tg_gemv_i8(L, wd[i % R], xd, 1, y, stream.cuda_stream))}
         del g
     return out
 
