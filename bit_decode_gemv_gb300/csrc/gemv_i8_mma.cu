@@ -16,33 +16,39 @@
 //
 // Mapping. A CTA owns one to four 32-row mask tiles (the MMA's M stays 128;
 // the host picks the fewest tiles per CTA that still fill one wave) for all
-// groups and all tokens. 16 compute warps, two MMA warps and a copy warp hand
-// work to each other through mbarrier rings, with no CTA-wide barrier inside
-// the group loop; work moves between them in pairs of groups, so that each
-// wait, fence and arrival serves two groups.
-//   - Compute warp w reads and writes tensor-memory lanes 32(w%4)..+31 (the
-//     rows of mask tile w%4; a warp whose tile the CTA does not own only
-//     converts activations) and handles part p = w/4. In its iteration for
-//     pair P it expands its 32 weights of each group (group lanes 32p..32p+31,
-//     from the input ring) to fp16, one byte permute per two weights, into A
-//     slot P%2 in tensor memory (row = lane, K along the columns), converts
-//     two 8-byte activation chunks per group (from the input ring) into B slot
-//     P%2 in shared memory, in the canonical K-major layout of 8-row x 16-byte
-//     core matrices, and arrives on the slot's "full" barrier; then it reads
-//     back pair P-1's D buffer for tokens 16p..16p+15 (those MMAs ran while
-//     pair P was prepared) and accumulates it. The compute warps issue no
-//     global loads at all.
+// groups and all tokens. Warps specialised by role -- 8 producers, two MMA
+// warps, a copy warp and 8 folders -- hand work to each other through mbarrier
+// rings, with no CTA-wide barrier inside the group loop; work moves between
+// them in pairs of groups, so that each wait, fence and arrival serves two
+// groups. A warp only touches tensor-memory lanes 32(w%4)..+31, so producers
+// and folders are numbered so that w%4 is the row quarter (mask tile) they own.
+//   - Producer w (quarter q = w%4, parts 2pp, 2pp+1 with pp = w/4): in its
+//     iteration for pair P it expands its 64 weights of each group (group lanes
+//     64pp..64pp+63, from the input ring) to fp16, one byte permute per two
+//     weights, into A slot P%2 in tensor memory (row = lane, K along the
+//     columns), converts two 16-byte activation chunks per group (from the
+//     input ring) into B slot P%2 in shared memory, in the canonical K-major
+//     layout of 8-row x 16-byte core matrices, and arrives on the input stage's
+//     "empty" and the slot's "full" barriers. A producer whose tile the CTA
+//     does not own only converts activations.
 //   - MMA warp w takes the pairs P = w mod 2, with A/B slot w and D buffer w.
 //     When the slot is full and the buffer read back, one thread issues the
 //     sixteen K=16 steps of the pair and commits them to the slot's "empty" and
 //     the buffer's "full" barriers.
+//   - Folder f (quarter q = w%4, tokens 32h..32h+31 with h = f/4): for every
+//     pair it waits for the D buffer, reads its 32 token columns of each group
+//     back from tensor memory, arrives on the buffer's "empty" barrier as soon
+//     as the last read has landed, and accumulates them, scaled by d[r][g]
+//     (loaded from global memory a pair ahead), into its rows' int64 sums.
 //   - A copy warp fills a 3-deep ring of input stages with bulk and tensor
-//     (TMA) copies: per pair the mask bytes and scales of the tiles (a tile's
-//     two groups are adjacent in the blob) and one 64 x 128 activation box per
-//     group (128-byte swizzle, so the compute warps' 16-byte reads of eight
-//     token rows hit eight different bank groups); it refills the stage of pair
-//     P with pair P+3 once every compute warp has arrived on that stage's
-//     "empty" barrier.
+//     (TMA) copies: per pair the mask bytes of the tiles (a tile's two groups
+//     are adjacent in the blob) and one 64 x 128 activation box per group
+//     (128-byte swizzle, so the producers' 16-byte reads of eight token rows
+//     hit eight different bank groups); it refills the stage of pair P with
+//     pair P+3 once every producer has arrived on that stage's "empty" barrier.
+// Splitting the expansion and the fold over two sets of warps lets each run on
+// while the other waits (M = 64 on 13824 x 5120: 33.7 -> 30.2 us; 16 warps that
+// both expanded and folded had to pass every hand-off in turn).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -64,20 +70,22 @@ using tgi::mbar_expect_tx;
 using tgi::mbar_init;
 using tgi::smem_u32;
 
-constexpr int kComputeWarps = 16;   // 4 row quarters x 4 parts (32 weights and 16 tokens each)
+constexpr int kProducerWarps = 8;   // 4 row quarters x 2 parts (64 weights of a group each)
+constexpr int kFolderWarps = 8;     // 4 row quarters x 2 token halves (32 tokens each)
 constexpr int kMmaWarps = 2;   // MMA issue alternates between two warps (even and odd pairs)
-constexpr int kThreads = (kComputeWarps + kMmaWarps + 1) * 32;   // + the MMA warps and the copy warp
+constexpr int kThreads = (kProducerWarps + kMmaWarps + 1 + kFolderWarps) * 32;
+constexpr int kFolderWarp0 = kProducerWarps + kMmaWarps + 1;   // producers, MMA warps, copy warp, folders
 constexpr int kRowsPerCta = 128;          // the MMA's M: one TMEM lane per row
 constexpr int kMaxN = 64;                 // tokens, the MMA's N at most
 constexpr int kPair = 2;                  // groups per handshake: work moves between warps in pairs
-constexpr int kStages = 3;                // input ring stages (masks, scales, activations of one pair)
+constexpr int kStages = 3;                // input ring stages (masks and activations of one pair)
 constexpr int kSlots = 2;                 // A/B slots, one pair each
 constexpr int kDBufs = 2;                 // D buffers, one pair each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;                       // A slots: 128 columns each (2 x 128 fp16 of K per row)
 constexpr uint32_t kColD = 128 * kSlots;            // D buffers: 2 x kMaxN columns each
 static_assert(kColD + kDBufs * kPair * kMaxN <= kTmemCols, "tensor memory plan");
-static_assert(kMaxN == 64, "each compute warp reads 16 D columns of each group");
+static_assert(kMaxN == 64, "each folder reads 32 D columns of each group");
 static_assert(kSlots == kMmaWarps && kDBufs == kMmaWarps, "MMA warp w owns A/B slot w and D buffer w");
 constexpr uint32_t kOffsetBits = 0x4B400000u;   // fp32 bit pattern of 1.5 * 2^23
 
@@ -87,8 +95,7 @@ constexpr int kBBytes = 8 * kKStepBytes;               // one group of B
 constexpr int kOffB = 0;                               // kSlots B slots of a pair each
 constexpr int kOffStages = kOffB + kSlots * kPair * kBBytes;   // 1024-aligned: the activation box is swizzled
 constexpr int kStageMask = 0;                          // masks [tile][group of the pair]: 2 KB per tile
-constexpr int kStageScale = 8192;                      // scales [tile][group]: 256 B per tile
-constexpr int kStageX = 9216;                          // activations [group]: 64 tokens x 128 B, 128-byte swizzle
+constexpr int kStageX = 8192;                          // activations [group]: 64 tokens x 128 B, 128-byte swizzle
 constexpr int kStageXBytes = kMaxN * TG_GROUP;
 constexpr int kStageBytes = kStageX + kPair * kStageXBytes;
 // mbarriers: input stage full/empty, A/B slot full/empty, D buffer full/empty. Every
@@ -346,15 +353,15 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         abort_flag = 0;
         for (int i = 0; i < kStages; i++) {
             mbar_init(bar(kBarMFull + i), 1);
-            mbar_init(bar(kBarMEmpty + i), kComputeWarps);
+            mbar_init(bar(kBarMEmpty + i), kProducerWarps);
         }
         for (int i = 0; i < kSlots; i++) {
-            mbar_init(bar(kBarABFull + i), kComputeWarps);
+            mbar_init(bar(kBarABFull + i), kProducerWarps);
             mbar_init(bar(kBarABEmpty + i), 1);
         }
         for (int i = 0; i < kDBufs; i++) {
             mbar_init(bar(kBarDFull + i), 1);
-            mbar_init(bar(kBarDEmpty + i), kComputeWarps);
+            mbar_init(bar(kBarDEmpty + i), kFolderWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -378,7 +385,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
     };
 
     const int npairs = (G + kPair - 1) / kPair;
-    if (warp == kComputeWarps + kMmaWarps) {
+    if (warp == kProducerWarps + kMmaWarps) {
         // ---------------- copy warp: inputs of pair P -> stage P % kStages ----------------
         auto copy_inputs = [&](int P) {
             const int st = P % kStages, g0 = kPair * P;
@@ -386,13 +393,12 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             const uint32_t sdst = sbase + kOffStages + st * kStageBytes;
             const uint32_t b = bar(kBarMFull + st);
             if (lane == 0)
-                mbar_expect_tx(b, (uint32_t)(tiles_here * ng) * (kMaskBytes + 128u) + (uint32_t)(ng * kStageXBytes));
+                mbar_expect_tx(b, (uint32_t)(tiles_here * ng) * kMaskBytes + (uint32_t)(ng * kStageXBytes));
             __syncwarp();
             if (lane < tiles_here) {
                 // the pair's groups of one tile are adjacent in the blob
                 const size_t unit = (size_t)(blockIdx.x * ctiles + lane) * G + g0;
                 bulk_copy(sdst + kStageMask + lane * 2048, masks + unit * kMaskBytes, (uint32_t)ng * kMaskBytes, b);
-                bulk_copy(sdst + kStageScale + lane * 256, scales + unit * 128, (uint32_t)ng * 128u, b);
             } else if (lane >= 32 - ng) {
                 // 64 token rows x 128 bytes of group g0 + h (rows from M on read as zero)
                 const int h = 31 - lane;
@@ -404,7 +410,7 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
         for (int P = 0; P < min(npairs, kStages); P++, issued++)
             copy_inputs(P);
         for (int P = 0; P + kStages < npairs; P++) {
-            // every compute warp has read stage P % kStages
+            // every producer has read stage P % kStages
             if (lane == 0)
                 wait(kBarMEmpty + P % kStages, (uint32_t)(P / kStages) & 1u);
             __syncwarp();
@@ -419,16 +425,16 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             for (int P = max(issued - kStages, 0); P < issued; P++)
                 mbar_drain(bar(kBarMFull + P % kStages), (uint32_t)(P / kStages) & 1u);
         __syncwarp();
-    } else if (warp >= kComputeWarps) {
+    } else if (warp >= kProducerWarps && warp < kProducerWarps + kMmaWarps) {
         // ---------------- MMA warp w: pairs P = w mod 2, A/B slot and D buffer w ----------------
         const uint32_t idesc = instr_desc(nmma);
-        const int w = warp - kComputeWarps;
+        const int w = warp - kProducerWarps;
         if (lane == 0) {
             int last = -1;   // the last pair whose MMAs this warp committed
             for (int P = w; P < npairs && !abort_flag; P += kMmaWarps) {
                 const uint32_t par = (uint32_t)(P / kMmaWarps) & 1u;
                 wait(kBarABFull + w, par);
-                wait(kBarDEmpty + w, par);   // read back by every compute warp
+                wait(kBarDEmpty + w, par);   // read back by every folder
                 if (abort_flag)
                     break;
                 fence_after_sync();
@@ -451,156 +457,80 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                 mbar_drain(bar(kBarDFull + w), (uint32_t)(last / kMmaWarps) & 1u);
         }
         __syncwarp();
-    } else {
-        // ---------------- compute warps ----------------
-        const int q = warp & 3, p = warp >> 2;
-        // a warp whose quarter q >= ctiles has no rows: it converts activations and keeps
-        // the barrier protocol, and its tensor-memory lanes hold nothing that is read
+    } else if (warp < kProducerWarps) {
+        // ---------------- producer warps: A (expanded weights) and B (converted activations) ----------------
+        const int q = warp & 3, pp = warp >> 2;   // row quarter; parts 2 pp, 2 pp + 1 (64 weights of a group)
         const bool rows_q = q < ctiles;
         const int tile = blockIdx.x * ctiles + q;
         const bool tile_ok = rows_q && tile < tiles;
-        const int row = tile * tgi::kTileRows + lane;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const bool epi = rows_q && 16 * p < M;   // warp-uniform: this warp's rows and tokens exist
-        // int64 accumulators of tokens 16p + j (j = 0..15) for this row: [token][row] layout, + 128 j
-        int64_t *accs = reinterpret_cast<int64_t *>(smem + kOffAcc) + 16 * p * kRowsPerCta + 32 * q + lane;
-
-        // activation chunk: token xn, 16-byte chunk j16 (K elements 16 j16 .. 16 j16 + 15) of each
-        // group, read from the stage's swizzled box (chunk j of row n sits at chunk j ^ (n & 7))
+        // activation chunks: token xn, 16-byte chunks j16 and j16 + 4 of each group, from the
+        // stage's swizzled box (chunk j of row n sits at chunk j ^ (n & 7))
         const int xn = (warp & 7) * 8 + (lane & 7);
-        const int j16 = 4 * (warp >> 3) + (lane >> 3);
         const bool x_ok = xn < M;
-        const int xoff = kStageX + xn * TG_GROUP + ((j16 ^ (xn & 7)) << 4);
-
-        // D buffers (both groups of a pair): each group's first MMA step overwrites
-        // its buffer, so they start free
-        const uint32_t dbase = tmem + lane_off + kColD + 16u * (uint32_t)p;
-        __syncwarp();
-        if (lane == 0)
-            for (int db = 0; db < kDBufs; db++)
-                mbar_arrive(bar(kBarDEmpty + db));
-
-        uint32_t acc32[16];    // narrow fold: the current block of groups, wrapping
-#pragma unroll
-        for (int j = 0; j < 16; j++)
-            acc32[j] = 0;
-        uint64_t dsum = 0;     // wide fold: sum_g d, for the offset correction
-        uint32_t dblk = 0;     // narrow fold: sum of the block's d (wrapping)
-        int nblk = 0;
-        // narrow fold: the block's exact sum of P * d is acc32 - 0x4B400000 * dblk modulo 2^32,
-        // and its magnitude is below 2^31, so the int32 reading of that difference is exact
-        auto flush = [&]() {
-            const uint32_t c = kOffsetBits * dblk;
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-                accs[128 * j] += (int64_t)(int32_t)(acc32[j] - c);
-                acc32[j] = 0;
-            }
-            dblk = 0;
-            nblk = 0;
-        };
-        // accumulate one group's D (tokens 16p..16p+15 of this warp's rows) scaled by dgp
-        auto fold = [&](uint32_t (&v)[16], int dgp) {
-            if (kNarrow) {
-#pragma unroll
-                for (int j = 0; j < 16; j++)
-                    acc32[j] += v[j] * (uint32_t)dgp;
-                dblk += (uint32_t)dgp;
-                if (++nblk == kBlock)
-                    flush();
-            } else if (kFold == kFoldWide) {
-#pragma unroll
-                for (int j = 0; j < 16; j++)
-                    accs[128 * j] = (int64_t)mad_wide(v[j], dgp, (uint64_t)accs[128 * j]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int32_t P = (int32_t)(v[j] - kOffsetBits);
-                    accs[128 * j] += ((int64_t)P * dgp) >> frac;   // the group's floor
-                }
-            }
-        };
-        // read back pair P's D buffer db (ng groups) and accumulate it; the exact
-        // fp32 sums P get 1.5 * 2^23 added (exact: |P| <= 2^14), which leaves
-        // the bit pattern 0x4B400000 + P the folds read
-        auto epilogue = [&](int db, uint32_t par, int ng, const int (&dprev)[kPair]) {
-            if (!epi)
-                return;
-            wait(kBarDFull + db, par);
-            fence_after_sync();
-            const uint32_t dcol = dbase + (uint32_t)(kPair * kMaxN * db);
-            uint32_t v0[16], v1[16];
-            tmem_ld16(dcol, v0);
-            if (ng > 1)
-                tmem_ld16(dcol + kMaxN, v1);
-            tmem_wait_ld(v0);
-            if (ng > 1)
-                tmem_wait_ld(v1);
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-                v0[j] = __float_as_uint(__fadd_rn(__uint_as_float(v0[j]), 12582912.0f));
-                v1[j] = __float_as_uint(__fadd_rn(__uint_as_float(v1[j]), 12582912.0f));
-            }
-            fold(v0, dprev[0]);
-            if (ng > 1)
-                fold(v1, dprev[1]);
-        };
-
-        int dprev[kPair] = {0, 0};   // scales of the previous pair, for its epilogue
-        // this thread's 32 weights of a group: group lanes 32p..32p+31 = words 2(p%2), 2(p%2)+1
-        // of half p/2; Q1: word p of the row's 16 bytes (group lanes 32p..32p+31)
-        const unsigned char *mrow = kQ1 ? smem + kOffStages + kStageMask + q * 2048 + lane * 16 + 4 * p
-                                        : smem + kOffStages + kStageMask + q * 2048 + (p >> 1) * 512 + lane * 16 +
-                                              (p & 1) * 8;
-        const unsigned char *srow = smem + kOffStages + kStageScale + q * 256 + lane * 4;
-        const unsigned char *xrow = smem + kOffStages + xoff;
-        const uint32_t abase = tmem + lane_off + kColA + 16u * (uint32_t)p;
-        // B position of chunks 2 j16 and 2 j16 + 1 of token xn: K-step j16, core matrices 0 and 1
-        unsigned char *bdst = smem + kOffB + j16 * kKStepBytes + (xn >> 3) * 256 + (xn & 7) * 16;
+        const int j16 = lane >> 3;
+        const int xoff0 = kStageX + xn * TG_GROUP + ((j16 ^ (xn & 7)) << 4);
+        const int xoff1 = kStageX + xn * TG_GROUP + (((j16 + 4) ^ (xn & 7)) << 4);
+        // this thread's 64 weights of a group: 16 bytes (Q1: 8) of its row in the stage
+        const unsigned char *mrow = kQ1 ? smem + kOffStages + kStageMask + q * 2048 + lane * 16 + 8 * pp
+                                        : smem + kOffStages + kStageMask + q * 2048 + pp * 512 + lane * 16;
+        const uint32_t abase = tmem + lane_off + kColA + 32u * (uint32_t)pp;
+        unsigned char *bdst0 = smem + kOffB + j16 * kKStepBytes + (xn >> 3) * 256 + (xn & 7) * 16;
+        unsigned char *bdst1 = bdst0 + 4 * kKStepBytes;
 
         int st = 0;
         uint32_t st_par = 0;
 #pragma unroll 1
         for (int P = 0; P < npairs; P++) {
-            const int sl = P & 1;                        // A/B slot and D buffer of pair P (= its MMA warp)
+            const int sl = P & 1;
             const uint32_t sl_par = (uint32_t)(P >> 1) & 1u;
             const int ng = min(kPair, G - kPair * P);
             if (P >= kSlots)   // A/B slot free: the MMAs of pair P - 2 are done
                 wait(kBarABEmpty + sl, sl_par ^ 1u);
             wait(kBarMFull + st, st_par);
-            int dg[kPair] = {0, 0};
 #pragma unroll
             for (int h = 0; h < kPair; h++) {
                 if (h < ng) {
-                    uint2 mw = make_uint2(0, 0);
-                    if (tile_ok) {
-                        const unsigned char *mp = mrow + (size_t)st * kStageBytes + h * kMaskBytes;
-                        mw = kQ1 ? make_uint2(*reinterpret_cast<const uint32_t *>(mp), 0u)
-                                 : *reinterpret_cast<const uint2 *>(mp);
-                        dg[h] = *reinterpret_cast<const int *>(srow + (size_t)st * kStageBytes + h * 128);
-                    }
                     if (rows_q) {
+                        uint4 mw = make_uint4(0, 0, 0, 0);
+                        if (tile_ok) {
+                            const unsigned char *mp = mrow + (size_t)st * kStageBytes + h * kMaskBytes;
+                            if (kQ1) {
+                                const uint2 m2 = *reinterpret_cast<const uint2 *>(mp);
+                                mw = make_uint4(m2.x, m2.y, 0u, 0u);
+                            } else {
+                                mw = *reinterpret_cast<const uint4 *>(mp);
+                            }
+                        }
+                        const uint32_t at = abase + 128u * (uint32_t)sl + 64u * (uint32_t)h;
                         uint32_t a[16];
                         if (kQ1) {
                             expand_word_q1(mw.x, a);
+                            tmem_st16(at, a);
+                            expand_word_q1(mw.y, a);
+                            tmem_st16(at + 16u, a);
                         } else {
                             expand_word(mw.x, a);
                             expand_word(mw.y, a + 8);
+                            tmem_st16(at, a);
+                            expand_word(mw.z, a);
+                            expand_word(mw.w, a + 8);
+                            tmem_st16(at + 16u, a);
                         }
-                        tmem_st16(abase + 128u * (uint32_t)sl + 64u * (uint32_t)h, a);
                     }
                     if (x_ok) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + (size_t)st * kStageBytes +
-                                                                          h * kStageXBytes);
-                        unsigned char *B = bdst + (sl * kPair + h) * kBBytes;
-                        *reinterpret_cast<uint4 *>(B) = fp16_of_int8x8(make_uint2(xv.x, xv.y));
-                        *reinterpret_cast<uint4 *>(B + 128) = fp16_of_int8x8(make_uint2(xv.z, xv.w));
+                        const unsigned char *xs = smem + kOffStages + (size_t)st * kStageBytes + h * kStageXBytes;
+                        const uint4 xv0 = *reinterpret_cast<const uint4 *>(xs + xoff0);
+                        const uint4 xv1 = *reinterpret_cast<const uint4 *>(xs + xoff1);
+                        const int bo = (sl * kPair + h) * kBBytes;
+                        *reinterpret_cast<uint4 *>(bdst0 + bo) = fp16_of_int8x8(make_uint2(xv0.x, xv0.y));
+                        *reinterpret_cast<uint4 *>(bdst0 + bo + 128) = fp16_of_int8x8(make_uint2(xv0.z, xv0.w));
+                        *reinterpret_cast<uint4 *>(bdst1 + bo) = fp16_of_int8x8(make_uint2(xv1.x, xv1.y));
+                        *reinterpret_cast<uint4 *>(bdst1 + bo + 128) = fp16_of_int8x8(make_uint2(xv1.z, xv1.w));
                     }
                 }
             }
-            dsum += (uint64_t)(int64_t)dg[0] + (uint64_t)(int64_t)dg[1];
-            // hand pair P to its MMA warp: A and B written (and its D buffer read back
-            // at the end of the previous iteration)
+            // hand pair P to its MMA warp
             tmem_wait_st();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before_sync();
@@ -608,30 +538,126 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
             if (lane == 0) {
                 mbar_arrive(bar(kBarMEmpty + st));   // this warp is done with input stage st
                 mbar_arrive(bar(kBarABFull + sl));
-                if (P >= kDBufs)   // D buffer sl, read back: free for pair P
-                    mbar_arrive(bar(kBarDEmpty + sl));
             }
-            // then pair P - 1: its MMAs ran while this pair was prepared
-            if (P >= 1)
-                epilogue(sl ^ 1, (uint32_t)((P - 1) >> 1) & 1u, kPair, dprev);
-            dprev[0] = dg[0];
-            dprev[1] = dg[1];
             if (++st == kStages) {
                 st = 0;
                 st_par ^= 1u;
             }
         }
-        if (npairs >= 1)
-            epilogue((npairs - 1) & 1, (uint32_t)((npairs - 1) >> 1) & 1u, min(kPair, G - kPair * (npairs - 1)),
-                     dprev);
+    } else {
+        // ---------------- folder warps: D read back and accumulated ----------------
+        const int f = warp - kFolderWarp0;
+        const int q = warp & 3, th = f >> 2;   // row quarter (the warp's tensor-memory lanes); tokens 32 th..+31
+        const bool rows_q = q < ctiles;
+        const int tile = blockIdx.x * ctiles + q;
+        const bool tile_ok = rows_q && tile < tiles;
+        const int row = tile * tgi::kTileRows + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const bool epi = rows_q && 32 * th < M;   // warp-uniform: this warp's rows and tokens exist
+        // int64 accumulators of tokens 32 th + j (j = 0..31) for this row: [token][row] layout, + 128 j
+        int64_t *accs = reinterpret_cast<int64_t *>(smem + kOffAcc) + 32 * th * kRowsPerCta + 32 * q + lane;
+        // this row's scale of group g: sc_row[32 g] (the blob's scales, 128 bytes per tile and group)
+        const int32_t *sc_row = reinterpret_cast<const int32_t *>(scales) + (size_t)(tile_ok ? tile : 0) * G * 32 + lane;
+        const uint32_t dbase = tmem + lane_off + kColD + 32u * (uint32_t)th;
+
+        // D buffers start free
+        __syncwarp();
+        if (lane == 0)
+            for (int db = 0; db < kDBufs; db++)
+                mbar_arrive(bar(kBarDEmpty + db));
+
+        uint32_t acc32[32];
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+            acc32[j] = 0;
+        uint64_t dsum = 0;
+        uint32_t dblk = 0;
+        int nblk = 0;
+        auto flush = [&]() {
+            const uint32_t c = kOffsetBits * dblk;
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                accs[128 * j] += (int64_t)(int32_t)(acc32[j] - c);
+                acc32[j] = 0;
+            }
+            dblk = 0;
+            nblk = 0;
+        };
+        // one group's 32 accumulator values (bit patterns 0x4B400000 + P once offset), scaled by dgp
+        auto fold = [&](uint32_t (&v0)[16], uint32_t (&v1)[16], int dgp) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                v0[j] = __float_as_uint(__fadd_rn(__uint_as_float(v0[j]), 12582912.0f));
+                v1[j] = __float_as_uint(__fadd_rn(__uint_as_float(v1[j]), 12582912.0f));
+            }
+            if (kNarrow) {
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    acc32[j] += v0[j] * (uint32_t)dgp;
+                    acc32[16 + j] += v1[j] * (uint32_t)dgp;
+                }
+                dblk += (uint32_t)dgp;
+                if (++nblk == kBlock)
+                    flush();
+            } else if (kFold == kFoldWide) {
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    accs[128 * j] = (int64_t)mad_wide(v0[j], dgp, (uint64_t)accs[128 * j]);
+                    accs[128 * (16 + j)] = (int64_t)mad_wide(v1[j], dgp, (uint64_t)accs[128 * (16 + j)]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    accs[128 * j] += ((int64_t)(int32_t)(v0[j] - kOffsetBits) * dgp) >> frac;   // the group's floor
+                    accs[128 * (16 + j)] += ((int64_t)(int32_t)(v1[j] - kOffsetBits) * dgp) >> frac;
+                }
+            }
+        };
+        auto scale_of = [&](int g) { return (tile_ok && g < G) ? __ldg(sc_row + (size_t)32 * g) : 0; };
+        int dcur0 = scale_of(0), dcur1 = scale_of(1);
+#pragma unroll 1
+        for (int P = 0; P < npairs; P++) {
+            const int sl = P & 1;
+            const uint32_t par = (uint32_t)(P >> 1) & 1u;
+            const int ng = min(kPair, G - kPair * P);
+            // the next pair's scales load while this pair is read back
+            const int dn0 = scale_of(kPair * (P + 1)), dn1 = scale_of(kPair * (P + 1) + 1);
+            wait(kBarDFull + sl, par);
+            fence_after_sync();
+            const uint32_t dcol = dbase + (uint32_t)(kPair * kMaxN * sl);
+            uint32_t v0[16], v1[16];
+            if (epi) {
+                tmem_ld16(dcol, v0);
+                tmem_ld16(dcol + 16u, v1);
+                tmem_wait_ld(v0);
+                tmem_wait_ld(v1);
+                fold(v0, v1, dcur0);
+            }
+            if (ng > 1 && epi) {
+                tmem_ld16(dcol + kMaxN, v0);
+                tmem_ld16(dcol + kMaxN + 16u, v1);
+                tmem_wait_ld(v0);
+                tmem_wait_ld(v1);
+            }
+            // D buffer sl read back: free for pair P + 2
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(kBarDEmpty + sl));
+            if (ng > 1 && epi)
+                fold(v0, v1, dcur1);
+            dsum += (uint64_t)(int64_t)dcur0 + (uint64_t)(int64_t)dcur1;
+            dcur0 = dn0;
+            dcur1 = dn1;
+        }
         if (kNarrow && epi)
             flush();
         // wide fold: y[m][r] = acc_m - 0x4B400000 * sum_g d (mod 2^64); otherwise acc_m
         if (epi && tile_ok && row < N) {
             const uint64_t corr = kFold == kFoldWide ? (uint64_t)kOffsetBits * dsum : 0ull;
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int m = 16 * p + j;
+            for (int j = 0; j < 32; j++) {
+                const int m = 32 * th + j;
                 if (m < M)
                     y[(size_t)m * N + row] = (int64_t)((uint64_t)accs[128 * j] - corr);
             }
