@@ -359,17 +359,22 @@ def isolated_call_stats(torch, stream, call, reps=200, spacer_cycles=200_000):
     call alone, with no host submission gap; median, p10 and p90 over the reps.
     call(i) makes rep i's call (rotate the weights there to keep them out of L2)."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    spin = getattr(torch.cuda, "_sleep", None)   # torch's own spin kernel; without it the reps may include host gaps
     torch.cuda.synchronize()
     for i in range(reps):
-        torch.cuda._sleep(spacer_cycles)
+        if spin is not None:
+            spin(spacer_cycles)
         a, b = evs[i]
         a.record(stream)
         call(i)
         b.record(stream)
     torch.cuda.synchronize()
     us = np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
-    return {"median": round(float(np.median(us)), 3), "p10": round(float(np.quantile(us, 0.1)), 3),
-            "p90": round(float(np.quantile(us, 0.9)), 3), "reps": reps}
+    out = {"median": round(float(np.median(us)), 3), "p10": round(float(np.quantile(us, 0.1)), 3),
+           "p90": round(float(np.quantile(us, 0.9)), 3), "reps": reps}
+    if spin is None:
+        out["note"] = "no spin kernel available: the reps include the host's submission gap"
+    return out
 
 
 def _copies_for(nbytes):
