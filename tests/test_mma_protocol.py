@@ -21,16 +21,30 @@ completing at random later times, and checks that
 The kernel's wait bounds and abort path are not modelled.
 """
 
+import os
 import random
+import re
 
 import pytest
 
-N_PRODUCERS = 8
-N_FOLDERS = 8
-N_MMA = 2
-STAGES = 3
-SLOTS = 2
-PAIR = 2
+_SRC = os.path.join(os.path.dirname(__file__), "..", "bit_decode_gemv_gb300", "csrc", "gemv_i8_mma.cu")
+
+
+def _kernel_constant(name):
+    """The value of `constexpr int <name> = <n>;` in the kernel source, so that the
+    model always replays the protocol of the kernel as it stands."""
+    with open(_SRC) as f:
+        m = re.search(r"constexpr\s+int\s+" + name + r"\s*=\s*(\d+)\s*;", f.read())
+    assert m, f"{name} not found in the kernel source"
+    return int(m.group(1))
+
+
+N_PRODUCERS = _kernel_constant("kProducerWarps")
+N_FOLDERS = _kernel_constant("kFolderWarps")
+N_MMA = _kernel_constant("kMmaWarps")
+STAGES = _kernel_constant("kStages")
+SLOTS = _kernel_constant("kSlots")
+PAIR = _kernel_constant("kPair")
 
 
 class Barrier:
