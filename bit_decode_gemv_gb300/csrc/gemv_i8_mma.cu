@@ -439,13 +439,19 @@ gemv_i8_mma_kernel(const unsigned char *__restrict__ masks, const unsigned char 
                     break;
                 fence_after_sync();
                 const int ng = min(kPair, G - kPair * P);
-                for (int h = 0; h < ng; h++) {
-                    const uint32_t dt = tmem + kColD + (uint32_t)(kPair * kMaxN * w + kMaxN * h);
-                    const uint32_t at = tmem + kColA + (uint32_t)(128 * w + 64 * h);
-                    const uint32_t Bs = sbase + kOffB + (uint32_t)((kPair * w + h) * kBBytes);
+                // every operand address of the pair is a constant offset from these three, so no
+                // latency sits between one MMA's issue and the next
+                const uint32_t d0 = tmem + kColD + (uint32_t)(kPair * kMaxN * w);
+                const uint32_t a0 = tmem + kColA + (uint32_t)(128 * w);
+                const uint64_t b0 = smem_desc(sbase + kOffB + (uint32_t)(kPair * w * kBBytes));
 #pragma unroll
-                    for (int ks = 0; ks < 8; ks++)
-                        mma_a_tmem(dt, at + 8u * ks, smem_desc(Bs + ks * kKStepBytes), idesc, ks > 0 ? 1u : 0u);
+                for (int h = 0; h < kPair; h++) {
+                    if (h < ng) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ks++)
+                            mma_a_tmem(d0 + (uint32_t)(kMaxN * h), a0 + (uint32_t)(64 * h + 8 * ks),
+                                       b0 + (uint64_t)((h * kBBytes + ks * kKStepBytes) >> 4), idesc, ks > 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(bar(kBarABEmpty + w));
                 mma_commit(bar(kBarDFull + w));
