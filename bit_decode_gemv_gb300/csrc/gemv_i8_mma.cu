@@ -34,7 +34,10 @@
 //   - MMA warp w takes the pairs P = w mod 2, with A/B slot w and D buffer w.
 //     When the slot is full and the buffer read back, one thread issues the
 //     sixteen K=16 steps of the pair and commits them to the slot's "empty" and
-//     the buffer's "full" barriers.
+//     the buffer's "full" barriers. An MMA issues every ~50 cycles at N = 64,
+//     but any latency in forming its operands sits between one issue and the
+//     next, so every operand of a pair is a constant offset from three bases
+//     (M = 64: 30.1 -> 28.0 us against a loop that built each descriptor).
 //   - Folder f (quarter q = w%4, tokens 32h..32h+31 with h = f/4): for every
 //     pair it waits for the D buffer, reads its 32 token columns of each group
 //     back from tensor memory, arrives on the buffer's "empty" barrier as soon
